@@ -1,0 +1,443 @@
+"""Benchmark of the Quest decode step on one GB300 (or N replicas under torchrun).
+
+Workload: one LongChat-7B-shaped layer (32 MHA heads, d=128, page 16), 32768 prefilled
+tokens, token budget 2048 (128 pages); a step appends one token (quest_append) and runs the
+fused score + top-K + sparse decode (quest_decode).  Steps cycle through the workload's 64
+appended tokens (contexts 32769..32832); before each cycle the cache is rewound (outside
+the timed region).  The L2 is flushed (512 MiB write) before every timed step.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode µs/step & HBM GB/s (frac of roofline), 32K ctx, 2048 budget"
+FLUSH_BYTES = 512 << 20
+PAGE = 16
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="quest", choices=["quest", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------
+# algorithmic bytes (what the step must move): metadata of every page of every head,
+# the K and V rows of every valid token of every selected page, q in, out + lse out.
+# ------------------------------------------------------------------------------------
+def decode_bytes(seq_lens, counts_tokens, B, Hq, Hkv, d=128):
+    meta = sum(math.ceil(L / PAGE) for L in seq_lens) * Hkv * 2 * d * 2
+    kv = counts_tokens * 2 * d * 2
+    qo = B * Hq * d * 2 * 2 + B * Hq * 4
+    return meta + kv + qo
+
+
+def append_bytes(B, Hkv, d=128):
+    # read k_new, v_new; write the K and V rows; read+write the page box (min and max)
+    return B * Hkv * d * 2 * (2 + 2 + 4)
+
+
+def selected_tokens(idx, cnt, seq_lens):
+    import numpy as np
+    idx = idx.cpu().numpy()
+    cnt = cnt.cpu().numpy()
+    total = 0
+    for b in range(idx.shape[0]):
+        L = int(seq_lens[b])
+        for g in range(idx.shape[1]):
+            for p in idx[b, g, :cnt[b, g]]:
+                total += min(PAGE, L - int(p) * PAGE)
+    return total
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        else:
+            self.lines = []
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        busy = [s for s in sm if mx is None or s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm, and the cpu_baseline key)
+# ------------------------------------------------------------------------------------
+def oracle_timing(w, budget_s: float, max_steps: int):
+    import numpy as np
+    import oracle
+    oracle.build()
+    ref = oracle.Cache.from_arrays(w.k_pool.cpu().numpy(), w.v_pool.cpu().numpy(),
+                                   w.block_table.cpu().numpy(), w.seq_lens.cpu().numpy(),
+                                   w.num_q_heads)
+    oracle.build_meta(ref)
+    qs, ks, vs = w.q.cpu().numpy(), w.k_new.cpu().numpy(), w.v_new.cpu().numpy()
+    times = []
+    t_start = time.perf_counter()
+    n = 0
+    while n < max_steps:
+        t = n % w.steps
+        if t == 0 and n > 0:
+            ref.seq_lens[:] = w.seq_lens.cpu().numpy()
+            oracle.build_meta(ref)  # rewind (outside the per-step timing)
+        t0 = time.perf_counter()
+        oracle.decode_step(ref, qs[t], w.top_k, ks[t], vs[t])
+        times.append(time.perf_counter() - t0)
+        n += 1
+        if time.perf_counter() - t_start > budget_s:
+            break
+    us = 1e6 * sum(times) / len(times)
+    return us, len(times)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from query_aware_kv_gb300 import workloads as wl
+    w = wl.longchat_32k(seed=0, device="cpu")
+    us, n = oracle_timing(w, budget_s=min(240.0, 0.05 * max(1, args.steps) + 60.0),
+                          max_steps=max(1, args.steps))
+    cpu = {"value": us, "unit": "us/step", "cores": 1, "kind": "oracle",
+           "sample": f"{n} of the {args.steps} requested decode steps (append + score + "
+                     f"top-K + attend), single-threaded C oracle, contexts 32769..32832"}
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/step",
+            "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": us / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, **w.describe()},
+            "cpu_baseline": cpu,
+            "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------
+def run_quest(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import query_aware_kv_gb300 as q
+    from query_aware_kv_gb300 import build as cuda_build
+    from query_aware_kv_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        cuda_build.build()
+    if world > 1:
+        dist.barrier()
+    q.load()
+
+    # each rank decodes its own independent sequence (weak scaling, no collective)
+    w = wl.longchat_32k(seed=rank, device=dev)
+    cache = q.PagedCache.allocate_meta(w.k_pool, w.v_pool, w.block_table, w.seq_lens.clone(),
+                                       w.num_q_heads)
+    K = w.top_k
+    ws = q.workspace(cache, K)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    q.build_meta(cache, ws)
+    t1.record()
+    torch.cuda.synchronize()
+    build_meta_us = 1e3 * t0.elapsed_time(t1)
+    meta0 = cache.meta.clone()
+    len0 = w.seq_lens.clone()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = torch.empty((1, w.num_q_heads, 128), dtype=torch.float16, device=dev)
+    lse = torch.empty((1, w.num_q_heads), dtype=torch.float32, device=dev)
+    idx = torch.empty((1, w.num_kv_heads, K), dtype=torch.int32, device=dev)
+    cnt = torch.empty((1, w.num_kv_heads), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def rewind():
+        cache.meta.copy_(meta0)
+        cache.seq_lens.copy_(len0)
+
+    def step(t):
+        q.append(cache, w.k_new[t], w.v_new[t], ws)
+        q.decode(cache, w.q[t], K, ws, out=out, lse=lse, idx_out=idx, count_out=cnt)
+
+    # warm-up
+    rewind()
+    for i in range(args.warmup):
+        if i % w.steps == 0:
+            rewind()
+        step(i % w.steps)
+    torch.cuda.synchronize()
+    rc, detail = q.read_status(ws)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} {detail}")
+
+    # ---- timed: append + fused decode per step, L2 flushed before each step
+    n = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    rewind()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(n):
+            t = i % w.steps
+            if t == 0 and i > 0:
+                rewind()
+            flush.zero_()
+            ev[i][0].record()
+            step(t)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    step_us = [1e3 * a.elapsed_time(b) for a, b in ev]
+    mean_step = sum(step_us) / n
+    rc, detail = q.read_status(ws)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} {detail}")
+
+    # ---- kernel-only: quest_decode alone at one context (seq_len = 32832)
+    rewind()
+    for t in range(w.steps):
+        q.append(cache, w.k_new[t], w.v_new[t], ws)
+    L_fixed = [int(x) for x in cache.seq_lens.cpu().tolist()]
+    kn = min(n, 512)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(kn)]
+    for i in range(kn):
+        flush.zero_()
+        kev[i][0].record()
+        q.decode(cache, w.q[i % w.steps], K, ws, out=out, lse=lse, idx_out=idx, count_out=cnt)
+        kev[i][1].record()
+    torch.cuda.synchronize()
+    dec_us = sum(1e3 * a.elapsed_time(b) for a, b in kev) / kn
+    tok = selected_tokens(idx, cnt, L_fixed)
+    dec_bytes = decode_bytes(L_fixed, tok, 1, w.num_q_heads, w.num_kv_heads)
+
+    # ---- unfused chain and dense baseline at the same context
+    def timed(fn, reps=64):
+        es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in es:
+            flush.zero_()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(1e3 * a.elapsed_time(b) for a, b in es) / reps
+
+    scores = torch.empty((1, w.num_kv_heads, cache.max_pages), dtype=torch.float32, device=dev)
+    qv = w.q[0]
+
+    def chain():
+        q.estimate(cache, qv, ws, scores=scores)
+        i2, c2 = q.topk(cache, scores, K, ws)
+        q.sparse_decode(cache, qv, i2, c2, K, ws, out=out, lse=lse)
+
+    chain_us = timed(chain)
+    dense_us = timed(lambda: q.dense_decode(cache, qv, ws, out=out, lse=lse), reps=32)
+    rc, detail = q.read_status(ws)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} {detail}")
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    hq = w.q.cpu().pin_memory()
+    hk = w.k_new.cpu().pin_memory()
+    hv = w.v_new.cpu().pin_memory()
+    hout = torch.empty_like(out, device="cpu").pin_memory()
+    hlse = torch.empty_like(lse, device="cpu").pin_memory()
+    dq = torch.empty_like(w.q[0])
+    dk = torch.empty_like(w.k_new[0])
+    dv = torch.empty_like(w.v_new[0])
+    en = min(n, 512)
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(en)]
+    rewind()
+    for i in range(en):
+        t = i % w.steps
+        if t == 0 and i > 0:
+            rewind()
+        flush.zero_()
+        eev[i][0].record()
+        dq.copy_(hq[t], non_blocking=True)
+        dk.copy_(hk[t], non_blocking=True)
+        dv.copy_(hv[t], non_blocking=True)
+        q.append(cache, dk, dv, ws)
+        q.decode(cache, dq, K, ws, out=out, lse=lse)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        eev[i][1].record()
+    torch.cuda.synchronize()
+    e2e_us = sum(1e3 * a.elapsed_time(b) for a, b in eev) / en
+    h2d = dq.numel() * 2 + dk.numel() * 2 + dv.numel() * 2
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+
+    # ---- max over ranks
+    def rmax(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    mean_step = rmax(mean_step)
+    dec_us = rmax(dec_us)
+    e2e_us = rmax(e2e_us)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    peak, peak_kind = peaks()
+    step_bytes = dec_bytes + append_bytes(1, w.num_kv_heads)
+    achieved = dec_bytes / (dec_us * 1e-6) / 1e9
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": round(mean_step, 3), "unit": "us/step", "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": round(mean_step / 1e3, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) fp16 K/V, 4 key channels x8, 8 planted needles/head)",
+        "config": {**w.describe(), "storage": "fp16 K/V/q/out, fp32 arithmetic",
+                   "l2": "flushed before every timed step (512 MiB write)",
+                   "step": "quest_append + quest_decode (fused score, top-K, split-K decode)",
+                   "replicas": world},
+        "gbs": round(world * step_bytes / (mean_step * 1e-6) / 1e9, 1),
+        "roofline": {"bound": "hbm", "kernel": "quest_decode (fused)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
+                     "algorithmic_bytes": dec_bytes, "launch_us": round(dec_us, 3),
+                     "traffic": traffic},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * n,
+        "clocks": clk.summary(),
+        "detail_us": {"step_mean": round(mean_step, 3), "step_p50": round(statistics.median(step_us), 3),
+                      "quest_decode": round(dec_us, 3), "unfused_chain": round(chain_us, 3),
+                      "dense_decode": round(dense_us, 3), "build_meta": round(build_meta_us, 3),
+                      "timed_wall_s": round(wall, 3)},
+    }
+    if not args.no_cpu_baseline:
+        us, k = oracle_timing(w, budget_s=args.cpu_seconds, max_steps=w.steps)
+        line["cpu_baseline"] = {
+            "value": round(us, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
+            "sample": f"{k} decode steps (append + score + top-K + attend) of the same "
+                      f"workload, single-threaded C oracle"}
+    print(json.dumps(line), flush=True)
+
+
+def profiled_traffic():
+    """DRAM bytes per quest_decode launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else null)."""
+    try:
+        import hashlib
+        with open(os.path.join(ROOT, "profiles", "quest_decode_traffic.json")) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        csrc = os.path.join(ROOT, "query_aware_kv_gb300", "csrc")
+        for name in sorted(os.listdir(csrc)):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+        if rec.get("csrc_sha256") != h.hexdigest():
+            return None
+        return rec.get("dram_bytes_per_launch_full_workload")
+    except Exception:
+        return None
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_quest(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * quest.h - C ABI of libquest.so, Quest's decode-time hot path on GB300 (sm_103a).
+ *
+ * Quest (Tang et al., ICML 2024) keeps the whole paged KV cache, summarises every page
+ * by the per-dimension minimum and maximum of its keys, scores each page against the
+ * current query with an upper bound on q.k, keeps the K best pages per head, and runs
+ * exact attention over those pages only.  Sources, cited below by title:
+ *   [Guide]   "Guide to Quest: Query-Aware KV Cache Sparsity for LLMs"
+ *   [Summary] "Quest: Query-Aware Sparsity for Efficient Long-Context LLM Inference"
+ *             (Tang 2024 paper summary page)
+ *   [Project] the sourcepulse project page of the published implementation
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer in quest_cache_t and every tensor argument is a DEVICE pointer owned
+ *   by the caller.  The library allocates no memory and keeps no state except a
+ *   thread-local error string.  All tensors are dense, row-major, 16-byte aligned.
+ * - fp16 means IEEE binary16.  head_dim must be 128, page_size 16 or 32, and
+ *   num_q_heads / num_kv_heads (the group size G) one of 1, 2, 4, 8.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *   and return a status code.  A non-zero code from the host-side checks means nothing
+ *   was launched.  quest_last_error() describes the last failure of this thread.
+ * - Faults that only the device can see (a block-table entry outside [0, num_phys), a
+ *   sequence length outside [0, max_pages * page_size], an inter-CTA wait that ran out)
+ *   never trap: the kernel skips the offending page, records the first such fault in the
+ *   workspace status word and finishes.  quest_read_status() synchronises the stream,
+ *   returns that code and clears it.  Outputs of a call that recorded a fault are
+ *   unspecified; re-initialise the workspace (quest_workspace_init) after one.
+ * - The workspace is caller-owned device scratch of quest_workspace_size() bytes.  It
+ *   must be zeroed once before first use (quest_workspace_init) and is then reused
+ *   across calls: its counters return to zero at the end of each call.  Calls that share
+ *   one workspace must be ordered (same stream, or events); concurrent calls need
+ *   separate workspaces.
+ */
+#ifndef QUEST_H
+#define QUEST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QUEST_VERSION 1
+
+/* Status codes. */
+#define QUEST_OK 0
+#define QUEST_ERR_INVALID_ARG 1   /* null / misaligned pointer, negative size, bad top_k  */
+#define QUEST_ERR_UNSUPPORTED 2   /* head_dim != 128, page_size not 16/32, G not 1/2/4/8,
+                                     max_pages above QUEST_MAX_PAGES                        */
+#define QUEST_ERR_WORKSPACE 3     /* workspace null or smaller than quest_workspace_size() */
+#define QUEST_ERR_CUDA 4          /* a CUDA runtime call failed (message in last_error)    */
+#define QUEST_ERR_TIMEOUT 5       /* device: a bounded inter-CTA wait ran out              */
+#define QUEST_ERR_BAD_PAGE 6      /* device: block-table entry outside [0, num_phys)       */
+#define QUEST_ERR_BAD_LENGTH 7    /* device: seq_len outside [0, max_pages * page_size], or
+                                     an append into a row with no room                      */
+#define QUEST_ERR_BAD_SELECTION 8 /* device: quest_sparse_decode got a page index outside
+                                     [0, N_b) or a count outside [0, min(top_k, N_b)]        */
+
+/* Largest block-table row (pages per sequence) the selection kernels hold on chip. */
+#define QUEST_MAX_PAGES 16384
+
+typedef void* quest_stream_t; /* cudaStream_t */
+
+/*
+ * One layer's paged KV cache ([Guide] Implementation step 1: physical K/V pages,
+ * per-page key min/max, block table and per-sequence page counts; here lengths are
+ * kept in tokens).
+ *   k_pool, v_pool : fp16 [num_phys][num_kv_heads][page_size][128]; token t of sequence
+ *                    b lives in physical page block_table[b][t / page_size], slot
+ *                    t % page_size.  One (page, kv head) chunk is contiguous.
+ *   meta           : fp16 [num_phys][num_kv_heads][2][128]: per (page, kv head) the
+ *                    per-dimension key minimum (row 0) and maximum (row 1) over the
+ *                    tokens present ([Guide] Solution step 1).
+ *   block_table    : int32 [batch][max_pages], logical page -> physical page.  Entries at
+ *                    or past ceil(seq_len / page_size) are never read.
+ *   seq_lens       : int32 [batch], tokens present; only quest_append writes it.
+ */
+typedef struct quest_cache {
+    int32_t batch;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t page_size;
+    int32_t max_pages;
+    int32_t num_phys;
+    void* k_pool;
+    void* v_pool;
+    void* meta;
+    const int32_t* block_table;
+    int32_t* seq_lens;
+} quest_cache_t;
+
+/* Optional launch tuning (pass NULL for defaults).  Results do not depend on it beyond
+ * floating-point rounding of the split-K merge. */
+typedef struct quest_opts {
+    int32_t pages_per_split;  /* selected pages per decode work item (default 8)          */
+    int32_t score_tile_pages; /* pages per scoring work item (default 128)                */
+    int32_t max_ctas;         /* fused kernel: cap on persistent CTAs (0 = all that fit)  */
+    int32_t debug_flags;      /* QUEST_DEBUG_* (0 in normal use)                          */
+    int64_t wait_limit_ns;    /* bound on any inter-CTA wait (default 1e9 ns)             */
+} quest_opts_t;
+
+/* quest_decode only: never publish the selection, so that every decode work item's
+ * bounded wait runs out and the call reports QUEST_ERR_TIMEOUT.  For testing the
+ * timeout path; outputs are then unspecified. */
+#define QUEST_DEBUG_WITHHOLD_SELECTION 1
+
+/* Bytes of workspace the calls below need for this cache, top_k and opts; 0 if the
+ * arguments are invalid (see quest_last_error). */
+size_t quest_workspace_size(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts);
+
+/* Zero `ws_bytes` bytes of workspace on `stream` (cudaMemsetAsync). */
+int quest_workspace_init(void* ws, size_t ws_bytes, quest_stream_t stream);
+
+/*
+ * Bounding boxes after prefill.  [Guide] Solution step 1 (min-max key bounding box
+ * equations) and Implementation step 1 (min/max along the page's token axis): for every
+ * sequence b, page p < ceil(seq_lens[b] / P) and kv head, meta[...][0][i] = min and
+ * meta[...][1][i] = max of k[t][i] over the tokens t < seq_lens[b] of that page (a
+ * partial last page is boxed over its valid tokens).  Exact (fp16 min/max).  Reads the
+ * keys of every present token once.
+ */
+int quest_build_meta(const quest_cache_t* cache, void* ws, size_t ws_bytes,
+                     quest_stream_t stream);
+
+/*
+ * Decode-time append.  [Guide] Solution step 1: the box is formed as pages fill during
+ * prompt prefill or token generation.  k_new, v_new: fp16 [batch][num_kv_heads][128].
+ * For each sequence b the token goes to position L = seq_lens[b] (page L / P, which the
+ * caller must have mapped in block_table, slot L % P); slot 0 starts the page's box,
+ * any other slot widens it; then seq_lens[b] becomes L + 1.  A sequence with no room
+ * (L + 1 > max_pages * P) or an unmapped page is skipped and reported.
+ */
+int quest_append(const quest_cache_t* cache, const void* k_new, const void* v_new, void* ws,
+                 size_t ws_bytes, quest_stream_t stream);
+
+/*
+ * Query-aware criticality.  [Guide] Solution step 2, the upper-bound inequality:
+ *   score[b][g][p] = sum_i max(q_i * Kmin_i, q_i * Kmax_i)
+ * for the query heads h of kv head g (h / G == g), taking the maximum over those G
+ * heads (selection per kv head).  The 1/sqrt(d) factor of the page's formula is left
+ * out: a positive constant that cannot change the ranking.  Products are exact in fp32,
+ * the sum is fp32.  q: fp16 [batch][num_q_heads][128].  scores: fp32
+ * [batch][num_kv_heads][max_pages]; pages at or past ceil(seq_len / P) get -inf.
+ */
+int quest_estimate(const quest_cache_t* cache, const void* q, float* scores, void* ws,
+                   size_t ws_bytes, quest_stream_t stream);
+
+/*
+ * Top-K page selection.  [Guide] Solution step 3; [Summary] "Top-K highest-scoring
+ * pages".  For each (b, g) keeps K_b = min(top_k, N_b) pages, N_b = ceil(seq_len / P):
+ * the pages with the largest scores, equal scores going to the lower page index.  If
+ * N_b <= top_k every page is kept.  idx: int32 [batch][num_kv_heads][top_k], the kept
+ * logical pages in ASCENDING page order, -1 after the first K_b; count: int32
+ * [batch][num_kv_heads] = K_b.  Selection is an exact radix select on the fp32 scores.
+ */
+int quest_topk(const quest_cache_t* cache, const float* scores, int32_t top_k, int32_t* idx,
+               int32_t* count, void* ws, size_t ws_bytes, quest_stream_t stream);
+
+/*
+ * Attention over the kept pages.  [Summary] Summary: exact attention is computed only
+ * over the Top-K pages; [Guide] Solution step 3 and Implementation step 3.  For query
+ * head h (kv head g = h / G):
+ *   out[b][h] = sum_t softmax_t(q.k_t / sqrt(128)) v_t,  lse[b][h] = log sum_t exp(q.k_t / sqrt(128))
+ * over every token t < seq_len of the pages idx[b][g][0..count-1].  Split-K over the
+ * kept pages with a log-sum-exp merge; fp32 arithmetic on fp16 data.  out: fp16
+ * [batch][num_q_heads][128]; lse: fp32 [batch][num_q_heads] or NULL.  No kept token:
+ * out = 0, lse = -inf.
+ */
+int quest_sparse_decode(const quest_cache_t* cache, const void* q, const int32_t* idx,
+                        const int32_t* count, int32_t top_k, void* out, float* lse, void* ws,
+                        size_t ws_bytes, const quest_opts_t* opts, quest_stream_t stream);
+
+/*
+ * The whole decode step in one persistent launch: quest_estimate, quest_topk and
+ * quest_sparse_decode fused ([Guide] Best Practices step 3 suggests fusing the bound
+ * estimation with the page gather).  Work items (scoring tiles, then split-K decode
+ * items) are taken from a queue in the workspace; the last scoring tile of a (b, g)
+ * selects its pages, and that (b, g)'s decode items wait for the selection (a bounded
+ * wait).  Same results as the three calls.  idx_out / count_out (layouts of
+ * quest_topk) receive the selection if non-NULL.
+ */
+int quest_decode(const quest_cache_t* cache, const void* q, int32_t top_k, void* out,
+                 float* lse, int32_t* idx_out, int32_t* count_out, void* ws, size_t ws_bytes,
+                 const quest_opts_t* opts, quest_stream_t stream);
+
+/*
+ * Full-context attention over every token (every page kept): the library's own dense
+ * baseline ([Summary] Key points compare Quest's attention with a dense kernel).
+ */
+int quest_dense_decode(const quest_cache_t* cache, const void* q, void* out, float* lse,
+                       void* ws, size_t ws_bytes, const quest_opts_t* opts,
+                       quest_stream_t stream);
+
+/*
+ * Synchronise `stream`, return the device status recorded in the workspace (QUEST_OK
+ * or a QUEST_ERR_* code) and clear it.  detail (nullable, 3 ints) receives the first
+ * fault's sequence, logical page and a kernel-specific code.
+ */
+int quest_read_status(void* ws, size_t ws_bytes, quest_stream_t stream, int32_t* detail);
+
+/* Text of the last failure on this thread ("" if none). */
+const char* quest_last_error(void);
+
+/* Name of a status code. */
+const char* quest_status_string(int code);
+
+int quest_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QUEST_H */

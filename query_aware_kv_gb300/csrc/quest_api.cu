@@ -1,0 +1,356 @@
+// quest_api.cu - the C ABI of libquest.so (declared in include/quest.h): host-side
+// argument checks, work decomposition, workspace layout and kernel dispatch.  No call
+// allocates memory or synchronises, except quest_read_status.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "quest_internal.h"
+
+using namespace quest;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(QUEST_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+int check_cache(const quest_cache_t* c) {
+  if (!c) return fail(QUEST_ERR_INVALID_ARG, "cache descriptor is NULL");
+  if (c->head_dim != kHeadDim)
+    return fail(QUEST_ERR_UNSUPPORTED, "head_dim %d: only 128 is supported", c->head_dim);
+  if (c->page_size != 16 && c->page_size != 32)
+    return fail(QUEST_ERR_UNSUPPORTED, "page_size %d: only 16 and 32 are supported", c->page_size);
+  if (c->batch < 0 || c->num_q_heads < 1 || c->num_kv_heads < 1 || c->max_pages < 1 ||
+      c->num_phys < 1)
+    return fail(QUEST_ERR_INVALID_ARG,
+                "bad sizes: batch %d, num_q_heads %d, num_kv_heads %d, max_pages %d, num_phys %d",
+                c->batch, c->num_q_heads, c->num_kv_heads, c->max_pages, c->num_phys);
+  if (c->num_q_heads % c->num_kv_heads)
+    return fail(QUEST_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                c->num_q_heads, c->num_kv_heads);
+  const int G = c->num_q_heads / c->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(QUEST_ERR_UNSUPPORTED, "group size %d: only 1, 2, 4, 8 are supported", G);
+  if (c->max_pages > QUEST_MAX_PAGES)
+    return fail(QUEST_ERR_UNSUPPORTED, "max_pages %d exceeds %d", c->max_pages, QUEST_MAX_PAGES);
+  if ((long long)c->batch * c->num_kv_heads > 65535)
+    return fail(QUEST_ERR_UNSUPPORTED, "batch * num_kv_heads exceeds 65535");
+  if (c->batch == 0) return QUEST_OK;
+  if (!c->k_pool || !c->v_pool || !c->meta || !c->block_table || !c->seq_lens)
+    return fail(QUEST_ERR_INVALID_ARG, "a cache pointer is NULL");
+  if (!aligned(c->k_pool, 16) || !aligned(c->v_pool, 16) || !aligned(c->meta, 16) ||
+      !aligned(c->block_table, 4) || !aligned(c->seq_lens, 4))
+    return fail(QUEST_ERR_INVALID_ARG, "pools and meta must be 16-byte aligned");
+  return QUEST_OK;
+}
+
+int check_topk(int top_k) {
+  if (top_k < 1 || top_k > QUEST_MAX_PAGES)
+    return fail(QUEST_ERR_INVALID_ARG, "top_k %d outside [1, %d]", top_k, QUEST_MAX_PAGES);
+  return QUEST_OK;
+}
+
+Tiling make_tiling(const quest_cache_t* c, int top_k, const quest_opts_t* o) {
+  Tiling t{};
+  t.topk_cap = top_k;
+  int stp = (o && o->score_tile_pages > 0) ? o->score_tile_pages : kDefaultScoreTilePages;
+  if (stp > c->max_pages) stp = c->max_pages;
+  t.score_tile_pages = stp;
+  t.n_score_tiles = (int)cdiv(c->max_pages, stp);
+  const int pps = (o && o->pages_per_split > 0) ? o->pages_per_split : kDefaultPagesPerSplit;
+  const int kcap = top_k < c->max_pages ? top_k : c->max_pages;
+  t.pps_sparse = (int)std::max<long long>(pps, cdiv(kcap, kMaxSplits));
+  t.n_splits_sparse = (int)cdiv(kcap, t.pps_sparse);
+  t.pps_dense = (int)std::max<long long>(pps, cdiv(c->max_pages, 64));
+  t.n_splits_dense = (int)cdiv(c->max_pages, t.pps_dense);
+  t.max_splits = std::max(t.n_splits_sparse, t.n_splits_dense);
+  return t;
+}
+
+WsLayout make_layout(const quest_cache_t* c, const Tiling& t) {
+  WsLayout L{};
+  const size_t nbg = (size_t)c->batch * c->num_kv_heads;
+  const size_t nbh = (size_t)c->batch * c->num_q_heads;
+  size_t off = sizeof(WsHeader);
+  L.score_arrive = off;  off = up256(off + nbg * 4);
+  L.ready = off;         off = up256(off + nbg * 4);
+  L.decode_arrive = off; off = up256(off + nbg * 4);
+  L.scores = off;        off = up256(off + nbg * c->max_pages * 4);
+  L.sel_idx = off;       off = up256(off + nbg * (size_t)t.topk_cap * 4);
+  L.sel_count = off;     off = up256(off + nbg * 4);
+  L.part_ml = off;       off = up256(off + nbh * t.max_splits * 2 * 4);
+  L.part_acc = off;      off = up256(off + nbh * t.max_splits * kHeadDim * 4);
+  L.total = off;
+  return L;
+}
+
+Params make_params(const quest_cache_t* c, void* ws, const WsLayout& L, const Tiling& t,
+                   const quest_opts_t* o) {
+  Params p{};
+  p.B = c->batch;
+  p.Hq = c->num_q_heads;
+  p.Hkv = c->num_kv_heads;
+  p.P = c->page_size;
+  p.max_pages = c->max_pages;
+  p.num_phys = c->num_phys;
+  p.k_pool = static_cast<__half*>(c->k_pool);
+  p.v_pool = static_cast<__half*>(c->v_pool);
+  p.meta = static_cast<__half*>(c->meta);
+  p.block_table = c->block_table;
+  p.seq_lens = c->seq_lens;
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  WsHeader* h = reinterpret_cast<WsHeader*>(w);
+  p.status = &h->status;
+  p.ticket = &h->ticket;
+  p.exited = &h->exited;
+  p.epoch = &h->epoch;
+  p.score_arrive = reinterpret_cast<unsigned*>(w + L.score_arrive);
+  p.ready = reinterpret_cast<unsigned*>(w + L.ready);
+  p.decode_arrive = reinterpret_cast<unsigned*>(w + L.decode_arrive);
+  p.scores = reinterpret_cast<float*>(w + L.scores);
+  p.sel_idx = reinterpret_cast<int*>(w + L.sel_idx);
+  p.sel_count = reinterpret_cast<int*>(w + L.sel_count);
+  p.part_ml = reinterpret_cast<float*>(w + L.part_ml);
+  p.part_acc = reinterpret_cast<float*>(w + L.part_acc);
+  p.top_k = t.topk_cap;
+  p.score_tile_pages = t.score_tile_pages;
+  p.n_score_tiles = t.n_score_tiles;
+  p.wait_limit_ns = (o && o->wait_limit_ns > 0) ? o->wait_limit_ns : kDefaultWaitNs;
+  p.debug_flags = o ? o->debug_flags : 0;
+  p.qscale = (float)(1.4426950408889634 / std::sqrt((double)kHeadDim));
+  return p;
+}
+
+// Common checks of the workspace; `need` = bytes this call requires.
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return fail(QUEST_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(QUEST_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < need)
+    return fail(QUEST_ERR_WORKSPACE, "workspace has %zu bytes, this call needs %zu", ws_bytes, need);
+  return QUEST_OK;
+}
+
+int launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return QUEST_OK;
+}
+
+int group_of(const quest_cache_t* c) { return c->num_q_heads / c->num_kv_heads; }
+
+}  // namespace
+
+extern "C" {
+
+int quest_version(void) { return QUEST_VERSION; }
+
+const char* quest_last_error(void) { return g_err.c_str(); }
+
+const char* quest_status_string(int code) {
+  switch (code) {
+    case QUEST_OK: return "QUEST_OK";
+    case QUEST_ERR_INVALID_ARG: return "QUEST_ERR_INVALID_ARG";
+    case QUEST_ERR_UNSUPPORTED: return "QUEST_ERR_UNSUPPORTED";
+    case QUEST_ERR_WORKSPACE: return "QUEST_ERR_WORKSPACE";
+    case QUEST_ERR_CUDA: return "QUEST_ERR_CUDA";
+    case QUEST_ERR_TIMEOUT: return "QUEST_ERR_TIMEOUT";
+    case QUEST_ERR_BAD_PAGE: return "QUEST_ERR_BAD_PAGE";
+    case QUEST_ERR_BAD_LENGTH: return "QUEST_ERR_BAD_LENGTH";
+    case QUEST_ERR_BAD_SELECTION: return "QUEST_ERR_BAD_SELECTION";
+    default: return "QUEST_ERR_UNKNOWN";
+  }
+}
+
+size_t quest_workspace_size(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts) {
+  if (check_cache(cache) != QUEST_OK || check_topk(top_k) != QUEST_OK) return 0;
+  return make_layout(cache, make_tiling(cache, top_k, opts)).total;
+}
+
+int quest_workspace_init(void* ws, size_t ws_bytes, quest_stream_t stream) {
+  if (!ws) return fail(QUEST_ERR_WORKSPACE, "workspace is NULL");
+  return launched(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)),
+                  "cudaMemsetAsync(workspace)");
+}
+
+int quest_build_meta(const quest_cache_t* cache, void* ws, size_t ws_bytes, quest_stream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (cache->batch == 0) return QUEST_OK;
+  if ((rc = check_ws(ws, ws_bytes, sizeof(WsHeader)))) return rc;
+  const Tiling t = make_tiling(cache, 1, nullptr);
+  const Params p = make_params(cache, ws, make_layout(cache, t), t, nullptr);
+  return launched(launch_build_meta(p, static_cast<cudaStream_t>(stream)), "quest_build_meta");
+}
+
+int quest_append(const quest_cache_t* cache, const void* k_new, const void* v_new, void* ws,
+                 size_t ws_bytes, quest_stream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (cache->batch == 0) return QUEST_OK;
+  if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16))
+    return fail(QUEST_ERR_INVALID_ARG, "k_new / v_new must be non-NULL and 16-byte aligned");
+  if ((rc = check_ws(ws, ws_bytes, sizeof(WsHeader)))) return rc;
+  const Tiling t = make_tiling(cache, 1, nullptr);
+  const Params p = make_params(cache, ws, make_layout(cache, t), t, nullptr);
+  return launched(launch_append(p, static_cast<const __half*>(k_new),
+                                static_cast<const __half*>(v_new),
+                                static_cast<cudaStream_t>(stream)),
+                  "quest_append");
+}
+
+int quest_estimate(const quest_cache_t* cache, const void* q, float* scores, void* ws,
+                   size_t ws_bytes, quest_stream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (cache->batch == 0) return QUEST_OK;
+  if (!q || !scores || !aligned(q, 16) || !aligned(scores, 4))
+    return fail(QUEST_ERR_INVALID_ARG, "q must be 16-byte aligned, scores 4-byte aligned");
+  if ((rc = check_ws(ws, ws_bytes, sizeof(WsHeader)))) return rc;
+  const Tiling t = make_tiling(cache, 1, nullptr);
+  Params p = make_params(cache, ws, make_layout(cache, t), t, nullptr);
+  p.q = static_cast<const __half*>(q);
+  p.scores = scores;
+  return launched(launch_estimate(p, group_of(cache), static_cast<cudaStream_t>(stream)),
+                  "quest_estimate");
+}
+
+int quest_topk(const quest_cache_t* cache, const float* scores, int32_t top_k, int32_t* idx,
+               int32_t* count, void* ws, size_t ws_bytes, quest_stream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if ((rc = check_topk(top_k))) return rc;
+  if (cache->batch == 0) return QUEST_OK;
+  if (!scores || !idx || !count || !aligned(scores, 4) || !aligned(idx, 4) || !aligned(count, 4))
+    return fail(QUEST_ERR_INVALID_ARG, "scores / idx / count must be non-NULL and 4-byte aligned");
+  if ((rc = check_ws(ws, ws_bytes, sizeof(WsHeader)))) return rc;
+  const Tiling t = make_tiling(cache, top_k, nullptr);
+  Params p = make_params(cache, ws, make_layout(cache, t), t, nullptr);
+  p.scores = const_cast<float*>(scores);
+  p.sel_idx = idx;
+  p.sel_count = count;
+  p.top_k = top_k;
+  return launched(launch_topk(p, static_cast<cudaStream_t>(stream)), "quest_topk");
+}
+
+int quest_sparse_decode(const quest_cache_t* cache, const void* q, const int32_t* idx,
+                        const int32_t* count, int32_t top_k, void* out, float* lse, void* ws,
+                        size_t ws_bytes, const quest_opts_t* opts, quest_stream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if ((rc = check_topk(top_k))) return rc;
+  if (cache->batch == 0) return QUEST_OK;
+  if (!q || !idx || !count || !out || !aligned(q, 16) || !aligned(out, 16) || !aligned(idx, 4) ||
+      !aligned(count, 4) || !aligned(lse, 4))
+    return fail(QUEST_ERR_INVALID_ARG, "q / idx / count / out must be non-NULL and aligned");
+  const Tiling t = make_tiling(cache, top_k, opts);
+  const WsLayout L = make_layout(cache, t);
+  if ((rc = check_ws(ws, ws_bytes, L.total))) return rc;
+  Params p = make_params(cache, ws, L, t, opts);
+  p.q = static_cast<const __half*>(q);
+  p.out = static_cast<__half*>(out);
+  p.lse = lse;
+  p.sel_idx = const_cast<int*>(idx);
+  p.sel_count = const_cast<int*>(count);
+  p.top_k = top_k;
+  p.pps = t.pps_sparse;
+  p.n_splits = t.n_splits_sparse;
+  p.dense = 0;
+  return launched(launch_decode(p, group_of(cache), static_cast<cudaStream_t>(stream)),
+                  "quest_sparse_decode");
+}
+
+int quest_decode(const quest_cache_t* cache, const void* q, int32_t top_k, void* out, float* lse,
+                 int32_t* idx_out, int32_t* count_out, void* ws, size_t ws_bytes,
+                 const quest_opts_t* opts, quest_stream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if ((rc = check_topk(top_k))) return rc;
+  if (cache->batch == 0) return QUEST_OK;
+  if (!q || !out || !aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(idx_out, 4) || !aligned(count_out, 4))
+    return fail(QUEST_ERR_INVALID_ARG, "q / out must be non-NULL and aligned");
+  const Tiling t = make_tiling(cache, top_k, opts);
+  const WsLayout L = make_layout(cache, t);
+  if ((rc = check_ws(ws, ws_bytes, L.total))) return rc;
+  Params p = make_params(cache, ws, L, t, opts);
+  p.q = static_cast<const __half*>(q);
+  p.out = static_cast<__half*>(out);
+  p.lse = lse;
+  if (idx_out) p.sel_idx = idx_out;
+  if (count_out) p.sel_count = count_out;
+  p.top_k = top_k;
+  p.pps = t.pps_sparse;
+  p.n_splits = t.n_splits_sparse;
+  p.dense = 0;
+  const long long items = (long long)cache->batch * cache->num_kv_heads *
+                          ((long long)t.n_score_tiles + t.n_splits_sparse);
+  if (items > 0x7fffffffLL) return fail(QUEST_ERR_UNSUPPORTED, "too many work items");
+  return launched(launch_fused(p, group_of(cache), opts ? opts->max_ctas : 0,
+                               static_cast<cudaStream_t>(stream)),
+                  "quest_decode");
+}
+
+int quest_dense_decode(const quest_cache_t* cache, const void* q, void* out, float* lse, void* ws,
+                       size_t ws_bytes, const quest_opts_t* opts, quest_stream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (cache->batch == 0) return QUEST_OK;
+  if (!q || !out || !aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return fail(QUEST_ERR_INVALID_ARG, "q / out must be non-NULL and aligned");
+  const Tiling t = make_tiling(cache, 1, opts);
+  const WsLayout L = make_layout(cache, t);
+  if ((rc = check_ws(ws, ws_bytes, L.total))) return rc;
+  Params p = make_params(cache, ws, L, t, opts);
+  p.q = static_cast<const __half*>(q);
+  p.out = static_cast<__half*>(out);
+  p.lse = lse;
+  p.top_k = cache->max_pages;
+  p.pps = t.pps_dense;
+  p.n_splits = t.n_splits_dense;
+  p.dense = 1;
+  return launched(launch_decode(p, group_of(cache), static_cast<cudaStream_t>(stream)),
+                  "quest_dense_decode");
+}
+
+int quest_read_status(void* ws, size_t ws_bytes, quest_stream_t stream, int32_t* detail) {
+  if (!ws || ws_bytes < sizeof(WsHeader)) return fail(QUEST_ERR_WORKSPACE, "workspace too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int h[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  if (detail) {
+    detail[0] = h[1];
+    detail[1] = h[2];
+    detail[2] = h[3];
+  }
+  if (h[0] != QUEST_OK) {
+    e = cudaMemset(ws, 0, sizeof(h));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+    fail(h[0], "device reported %s (sequence %d, page %d, site %d)", quest_status_string(h[0]),
+         h[1], h[2], h[3]);
+  }
+  return h[0];
+}
+
+}  // extern "C"

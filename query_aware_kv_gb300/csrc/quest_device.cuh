@@ -1,0 +1,742 @@
+// quest_device.cuh - device building blocks of the Quest decode path (sm_103a).
+//
+//   score_tile    : criticality bound of a run of pages for one (sequence, kv head)
+//                   ("Guide to Quest", Solution step 2).
+//   topk_select   : exact top-K of a score row, ties to the lower page index
+//                   ("Guide to Quest", Solution step 3).
+//   decode_tile   : flash-decode over a run of kept pages, staged into shared memory by
+//                   1-D bulk copies (TMA) with an mbarrier ring; writes one split-K partial
+//                   (Tang 2024 summary: exact attention over the Top-K pages).
+//   merge_splits  : log-sum-exp merge of the partials of one (sequence, kv head).
+#pragma once
+
+#include <math_constants.h>
+
+#include "quest_internal.h"
+
+namespace quest {
+
+// ------------------------------------------------------------------------------------
+// shared-memory map of the decode-capable kernels
+// ------------------------------------------------------------------------------------
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct SmemMap {
+  size_t ring, full, empty, nvalid, wsc, st, mscale, hist, scratch, misc, bt, total;
+};
+
+// ring      : kStages x (K chunk + V chunk) of one (page, kv head); also reused, when idle,
+//             for the warp-merge buffer and for the top-K keys
+// full/empty: mbarriers of the ring
+// wsc       : per consumer warp, G x P logits then weights of the page in hand
+// st        : per consumer warp and head: running max (log2 units), running sum, rescale
+// mscale    : per head, the merge scale of every split, then the merged max and sum
+__host__ __device__ inline SmemMap make_smem_map(int G, int P, int topk_keys, int stp) {
+  SmemMap m{};
+  const size_t ring = (size_t)kStages * 2 * P * kHeadDim * 2;
+  const size_t red = (size_t)kConsumerWarps * G * kHeadDim * 4;
+  const size_t keys = (size_t)topk_keys * 4;
+  size_t a = ring;
+  if (red > a) a = red;
+  if (keys > a) a = keys;
+  size_t o = 0;
+  m.ring = o;    o = align_up(o + a, 128);
+  m.full = o;    o += kStages * 8;
+  m.empty = o;   o += kStages * 8;
+  m.nvalid = o;  o = align_up(o + kStages * 4, 16);
+  m.wsc = o;     o = align_up(o + (size_t)kConsumerWarps * G * P * 4, 16);
+  m.st = o;      o = align_up(o + (size_t)kConsumerWarps * G * 3 * 4, 16);
+  m.mscale = o;  o = align_up(o + (size_t)G * (kMaxSplits + 2) * 4, 16);
+  m.hist = o;    o += 256 * 4;
+  m.scratch = o; o += 64 * 4;
+  m.misc = o;    o += 16 * 4;
+  m.bt = o;      o = align_up(o + (size_t)stp * 4, 16);
+  m.total = o;
+  return m;
+}
+
+// ------------------------------------------------------------------------------------
+// PTX helpers
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return (long long)t;
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* ptr) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(ptr));
+  return r;
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_relaxed_s32(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds_u2(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ float2 h2f(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+// First device fault wins; later ones are dropped.
+__device__ __forceinline__ void report(const Params& p, int code, int b, int page, int site) {
+  if (atomicCAS(p.status, 0, code) == 0) {
+    p.status[1] = b;
+    p.status[2] = page;
+    p.status[3] = site;
+  }
+}
+
+// Tokens present in sequence b, or 0 (and a report) if seq_lens[b] is out of range.
+__device__ __forceinline__ int load_len(const Params& p, int b, int site) {
+  const int L = p.seq_lens[b];
+  if (L < 0 || (long long)L > (long long)p.max_pages * p.P) {
+    report(p, QUEST_ERR_BAD_LENGTH, b, -1, site);
+    return 0;
+  }
+  return L;
+}
+
+// Bounded wait on an mbarrier phase; false (and a report) once wait_limit_ns has passed.
+__device__ __forceinline__ bool mbar_wait_bounded(const Params& p, uint64_t* bar,
+                                                  uint32_t parity, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > p.wait_limit_ns) {
+      report(p, QUEST_ERR_TIMEOUT, -1, -1, site);
+      return false;
+    }
+  }
+}
+
+// Bounded wait until *flag == target (acquire).  Gives up early once another CTA timed out.
+__device__ __forceinline__ bool wait_flag_bounded(const Params& p, const unsigned* flag,
+                                                  unsigned target, int b, int site) {
+  if (ld_acquire_u32(flag) == target) return true;
+  const long long t0 = global_ns();
+  while (true) {
+    __nanosleep(100);
+    if (ld_acquire_u32(flag) == target) return true;
+    if (ld_relaxed_s32(p.status) == QUEST_ERR_TIMEOUT) return false;
+    if (global_ns() - t0 > p.wait_limit_ns) {
+      report(p, QUEST_ERR_TIMEOUT, b, -1, site);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Inclusive prefix sum over the block (blockDim.x a multiple of 32).  scratch >= 32 ints.
+__device__ __forceinline__ int block_incl_scan(int v, int* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int t = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += n;
+    }
+    if (lane < nw) scratch[lane] = t;
+  }
+  __syncthreads();
+  const int add = warp > 0 ? scratch[warp - 1] : 0;
+  __syncthreads();
+  return v + add;
+}
+
+// Arrival on a per-(b, g) counter; true in the one CTA that arrives last.  The last CTA
+// sees every write the others made before arriving.
+__device__ __forceinline__ bool arrive_last(unsigned* counter, unsigned target, int* s_flag) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *s_flag = (atomicAdd(counter, 1u) == target - 1u) ? 1 : 0;
+  __syncthreads();
+  const bool last = *s_flag != 0;
+  if (last) __threadfence();
+  __syncthreads();
+  return last;
+}
+
+// ------------------------------------------------------------------------------------
+// scoring: U(q, p) = sum_i max(q_i Kmin_i, q_i Kmax_i)  ("Guide to Quest", Solution
+// step 2), evaluated in its sign-split form: per dimension the box corner that the sign of
+// q_i picks (Kmax for q_i > 0, Kmin otherwise) is selected with one bitwise op on packed
+// halves, widened, and multiplied (exact) into an fp32 sum.
+// ------------------------------------------------------------------------------------
+template <int G>
+struct QueryFrag {
+  float qf[G][8];   // q of each head of the group, dims [8c, 8c+8)
+  uint32_t neg[G][4];  // per packed pair, 0xFFFF in the halves whose q is negative
+};
+
+template <int G>
+__device__ __forceinline__ void load_query_frag(const Params& p, int b, int g, int c,
+                                                QueryFrag<G>& f) {
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const uint4 raw =
+        *reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.Hq + g * G + j) * kHeadDim + 8 * c);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f.neg[j][k] = ((w[k] >> 15) & 0x00010001u) * 0xFFFFu;
+      const float2 v = h2f(w[k]);
+      f.qf[j][2 * k] = v.x;
+      f.qf[j][2 * k + 1] = v.y;
+    }
+  }
+}
+
+template <int G>
+__device__ __forceinline__ float corner_dot(const QueryFrag<G>& f, int j, const uint4& mn,
+                                            const uint4& mx) {
+  const uint32_t a[4] = {mn.x, mn.y, mn.z, mn.w};
+  const uint32_t c[4] = {mx.x, mx.y, mx.z, mx.w};
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t sel = (a[k] & f.neg[j][k]) | (c[k] & ~f.neg[j][k]);
+    const float2 v = h2f(sel);
+    s = fmaf(f.qf[j][2 * k], v.x, s);
+    s = fmaf(f.qf[j][2 * k + 1], v.y, s);
+  }
+  return s;
+}
+
+// Scores pages [p0, p0 + n_live) of (b, g) into dst[0 .. n_live).  Half-warp per page,
+// 16 B of the min row and 16 B of the max row per lane, 4 pages in flight per half-warp.
+// bt_s: shared scratch of >= n_live ints.  Called by the whole block.
+template <int G>
+__device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, float* dst,
+                           int* bt_s) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int* bt_row = p.block_table + (size_t)b * p.max_pages + p0;
+  for (int i = tid; i < n_live; i += nthr) bt_s[i] = bt_row[i];
+  const int hw = tid >> 4, c = tid & 15, nhw = nthr >> 4;
+  QueryFrag<G> f;
+  load_query_frag<G>(p, b, g, c, f);
+  __syncthreads();
+  const __half* meta_g = p.meta + (size_t)g * 2 * kHeadDim + 8 * c;
+  const size_t page_stride = (size_t)p.Hkv * 2 * kHeadDim;
+  constexpr int U = 4;
+  for (int base = 0; base < n_live; base += U * nhw) {
+    uint4 mn[U], mx[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int r = base + u * nhw + hw;
+      ok[u] = false;
+      mn[u] = make_uint4(0, 0, 0, 0);
+      mx[u] = make_uint4(0, 0, 0, 0);
+      if (r < n_live) {
+        const int phys = bt_s[r];
+        if (phys >= 0 && phys < p.num_phys) {
+          const __half* src = meta_g + (size_t)phys * page_stride;
+          mn[u] = ld_stream_v4(src);
+          mx[u] = ld_stream_v4(src + kHeadDim);
+          ok[u] = true;
+        } else if (c == 0) {
+          report(p, QUEST_ERR_BAD_PAGE, b, p0 + r, kSiteScore);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float best = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float s = corner_dot<G>(f, j, mn[u], mx[u]);
+        s += __shfl_xor_sync(0xffffffffu, s, 8);
+        s += __shfl_xor_sync(0xffffffffu, s, 4);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        best = fmaxf(best, s);
+      }
+      const int r = base + u * nhw + hw;
+      if (c == 0 && r < n_live) dst[r] = ok[u] ? best : -CUDART_INF_F;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// top-K: "Guide to Quest", Solution step 3.  Scores become order-preserving unsigned keys
+// (sign flip); an MSB-first radix select (8-bit digits, shared-memory histogram, block
+// scan) finds the K-th largest key; a block scan then compacts, in ascending page order,
+// every key above the threshold and the lowest-indexed keys equal to it.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t score_key(float s) {
+  const uint32_t u = __float_as_uint(s + 0.0f);  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// row: N scores (global, may have been written by other CTAs of this grid); writes K
+// entries of idx_out and *count_out.  keys: shared >= N uint32.  Called by the whole block.
+static __device__ void topk_select(const float* row, int N, int K, int* idx_out, int* count_out,
+                            uint32_t* keys, int* hist, int* scratch) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  if (N <= K) {
+    for (int r = tid; r < K; r += nthr) idx_out[r] = r < N ? r : -1;
+    if (tid == 0) *count_out = N;
+    return;
+  }
+  for (int i = tid; i < N; i += nthr) keys[i] = score_key(__ldcg(row + i));
+  uint32_t prefix = 0, mask = 0;
+  int need = K;
+  int* sel = scratch + 40;  // digit, keys above, keys in the digit's bucket
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += nthr) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < N; i += nthr) {
+      const uint32_t k = keys[i];
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    const int cnt = tid < 256 ? hist[255 - tid] : 0;
+    const int incl = block_incl_scan(cnt, scratch);
+    if (tid < 256 && incl >= need && incl - cnt < need) {
+      sel[0] = 255 - tid;
+      sel[1] = incl - cnt;
+      sel[2] = cnt;
+    }
+    __syncthreads();
+    const int digit = sel[0], above = sel[1], bucket = sel[2];
+    need -= above;
+    prefix |= (uint32_t)digit << shift;
+    mask |= 0xFFu << shift;
+    __syncthreads();
+    if (bucket == need) break;  // the whole bucket is kept: threshold found
+  }
+  const int chunk = (N + nthr - 1) / nthr;
+  const int lo = min(N, tid * chunk), hi = min(N, lo + chunk);
+  int ngt = 0, neq = 0;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t m = keys[i] & mask;
+    ngt += m > prefix;
+    neq += m == prefix;
+  }
+  const int packed = (ngt << 16) | neq;
+  const int excl = block_incl_scan(packed, scratch) - packed;
+  int eq_before = excl & 0xFFFF;
+  int pos = (excl >> 16) + min(eq_before, need);
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t m = keys[i] & mask;
+    if (m > prefix) {
+      idx_out[pos++] = i;
+    } else if (m == prefix) {
+      if (eq_before < need) idx_out[pos++] = i;
+      ++eq_before;
+    }
+  }
+  if (tid == 0) *count_out = K;
+}
+
+// ------------------------------------------------------------------------------------
+// decode: one page of one kv head against the G query heads of its group, in one warp.
+// Lane l owns dims [4l, 4l+4).  Logits: 16 (head, token) partial dot products per chunk
+// are summed across the warp with a transposing butterfly (15 shuffles leave each lane
+// pair holding one full logit).  Softmax: running max / sum per head (log2 domain).
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ float transpose_reduce16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool hi = lane & 16;
+    const float send = hi ? v[i] : v[i + 8];
+    const float keep = hi ? v[i + 8] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool hi = lane & 8;
+    const float send = hi ? v[i] : v[i + 4];
+    const float keep = hi ? v[i + 4] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool hi = lane & 4;
+    const float send = hi ? v[i] : v[i + 2];
+    const float keep = hi ? v[i + 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  {
+    const bool hi = lane & 2;
+    const float send = hi ? v[0] : v[1];
+    const float keep = hi ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+  return v[0];
+}
+// Which of the 16 values lane `lane` holds after transpose_reduce16.
+__device__ __forceinline__ int reduced_index(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
+template <int G, int P>
+__device__ __forceinline__ void page_update(const float (&qf)[G][4], float (&acc)[G][4],
+                                            const __half* Ks, const __half* Vs, int nv,
+                                            float* sc, float* st, int lane) {
+  constexpr int TC = 16 / G;  // tokens per chunk of 16 (head, token) values
+  constexpr int NCH = P / TC;
+  // 1. logits (log2 units; q was pre-scaled by log2(e)/sqrt(d)) into sc[G][P]
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    float v[16];
+#pragma unroll
+    for (int tj = 0; tj < TC; ++tj) {
+      const int t = ch * TC + tj;
+      const uint2 raw = lds_u2(Ks + t * kHeadDim + 4 * lane);
+      const float2 k01 = h2f(raw.x), k23 = h2f(raw.y);
+#pragma unroll
+      for (int j = 0; j < G; ++j)
+        v[j * TC + tj] =
+            fmaf(qf[j][0], k01.x, fmaf(qf[j][1], k01.y, fmaf(qf[j][2], k23.x, qf[j][3] * k23.y)));
+    }
+    const float r = transpose_reduce16(v, lane);
+    const int vi = reduced_index(lane);
+    const int j = vi / TC, t = ch * TC + vi % TC;
+    if ((lane & 1) == 0) sc[j * P + t] = (t < nv) ? r : -CUDART_INF_F;
+  }
+  __syncwarp();
+  // 2. per head: tile max, new running max, weights, tile sum
+  constexpr int GP = G * P;
+  constexpr int NV = GP >= 32 ? GP / 32 : 1;
+  constexpr int SEG = P < 32 ? P : 32;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int vidx = GP >= 32 ? lane + 32 * i : (lane % GP);
+    const int j = vidx / P, t = vidx % P;
+    const float x = sc[j * P + t];
+    float mt = x;
+#pragma unroll
+    for (int o = SEG / 2; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+    const float m_old = st[j * 3 + 0];
+    const float m_new = fmaxf(m_old, mt);
+    const float w = (x == -CUDART_INF_F) ? 0.f : exp2f(x - m_new);
+    float sum = w;
+#pragma unroll
+    for (int o = SEG / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    __syncwarp();
+    sc[j * P + t] = w;
+    if (t == 0 && (GP >= 32 || lane < GP)) {
+      const float alpha = (m_new == -CUDART_INF_F) ? 1.f : exp2f(m_old - m_new);
+      st[j * 3 + 1] = st[j * 3 + 1] * alpha + sum;
+      st[j * 3 + 0] = m_new;
+      st[j * 3 + 2] = alpha;
+    }
+    __syncwarp();
+  }
+  // 3. acc = acc * alpha + sum_t w_t v_t  (tokens past the end contribute nothing, even junk)
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const float a = st[j * 3 + 2];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[j][k] *= a;
+  }
+#pragma unroll
+  for (int t4 = 0; t4 < P / 4; ++t4) {
+    float vv[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = 4 * t4 + u;
+      const uint2 raw = lds_u2(Vs + t * kHeadDim + 4 * lane);
+      const float2 a = h2f(raw.x), c = h2f(raw.y);
+      const bool live = t < nv;
+      vv[u][0] = live ? a.x : 0.f;
+      vv[u][1] = live ? a.y : 0.f;
+      vv[u][2] = live ? c.x : 0.f;
+      vv[u][3] = live ? c.y : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float4 w4 = *reinterpret_cast<const float4*>(sc + j * P + 4 * t4);
+      const float ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[j][k] = fmaf(ws[u], vv[u][k], acc[j][k]);
+    }
+  }
+  __syncwarp();
+}
+
+// Flash-decode over kept pages r0 .. r0 + n_tile - 1 of (b, g) (ranks in sel_row, or
+// logical pages r0.. when sel_row is null) and write this work item's split-K partial.
+// pc: pages this CTA has already pushed through its ring (mbarrier phase bookkeeping).
+// Called by the whole block (kDecodeThreads threads): warps 0..7 compute, warp 8 issues
+// the bulk copies.  n_tile >= 1.
+template <int G, int P>
+__device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap& m, int b,
+                            int g, int split, int r0, int n_tile, int L, int N_b,
+                            const int* sel_row, uint32_t pc) {
+  constexpr uint32_t kChunk = P * kHeadDim * 2;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned char* ring = smem + m.ring;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + m.empty);
+  int* nvalid_s = reinterpret_cast<int*>(smem + m.nvalid);
+  float* st_all = reinterpret_cast<float*>(smem + m.st);
+  float acc[G][4];
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[j][k] = 0.f;
+
+  if (warp == kConsumerWarps) {
+    // ---- producer warp: resolve pages 32 at a time, then issue their copies in order
+    const size_t chunk_elems = (size_t)P * kHeadDim;
+    for (int base = 0; base < n_tile; base += 32) {
+      const int r = base + lane;
+      int nv = 0;
+      const __half* ksrc = nullptr;
+      const __half* vsrc = nullptr;
+      if (r < n_tile) {
+        const int lp = sel_row ? __ldcg(sel_row + r0 + r) : r0 + r;
+        if (lp < 0 || lp >= N_b) {
+          report(p, QUEST_ERR_BAD_SELECTION, b, lp, kSiteSelection);
+        } else {
+          const int phys = p.block_table[(size_t)b * p.max_pages + lp];
+          if (phys < 0 || phys >= p.num_phys) {
+            report(p, QUEST_ERR_BAD_PAGE, b, lp, kSiteDecode);
+          } else {
+            nv = min(P, L - lp * P);
+            const size_t off = ((size_t)phys * p.Hkv + g) * chunk_elems;
+            ksrc = p.k_pool + off;
+            vsrc = p.v_pool + off;
+          }
+        }
+      }
+      const int cnt = min(32, n_tile - base);
+      for (int j = 0; j < cnt; ++j) {
+        if (lane == j) {
+          const uint32_t k = pc + (uint32_t)r;
+          const int stage = (int)(k % kStages);
+          const uint32_t par = ((k / kStages) & 1u) ^ 1u;
+          const bool ok = mbar_wait_bounded(p, &empty[stage], par, kSiteWaitSlot);
+          nvalid_s[stage] = ok ? nv : 0;
+          if (ok && nv > 0) {
+            unsigned char* dst = ring + (size_t)stage * 2 * kChunk;
+            mbar_arrive_expect_tx(&full[stage], 2 * kChunk);
+            bulk_g2s(dst, ksrc, kChunk, &full[stage]);
+            bulk_g2s(dst + kChunk, vsrc, kChunk, &full[stage]);
+          } else {
+            mbar_arrive(&full[stage]);
+          }
+        }
+        __syncwarp();
+      }
+    }
+  } else {
+    // ---- consumer warps
+    float qf[G][4];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(
+          p.q + ((size_t)b * p.Hq + g * G + j) * kHeadDim + 4 * lane);
+      const float2 a = h2f(raw.x), c = h2f(raw.y);
+      qf[j][0] = a.x * p.qscale;
+      qf[j][1] = a.y * p.qscale;
+      qf[j][2] = c.x * p.qscale;
+      qf[j][3] = c.y * p.qscale;
+    }
+    float* sc = reinterpret_cast<float*>(smem + m.wsc) + warp * G * P;
+    float* st = st_all + warp * G * 3;
+    if (lane < G) {
+      st[lane * 3 + 0] = -CUDART_INF_F;
+      st[lane * 3 + 1] = 0.f;
+      st[lane * 3 + 2] = 1.f;
+    }
+    __syncwarp();
+    for (int r = warp; r < n_tile; r += kConsumerWarps) {
+      const uint32_t k = pc + (uint32_t)r;
+      const int stage = (int)(k % kStages);
+      const uint32_t par = (k / kStages) & 1u;
+      const bool ok = mbar_wait_bounded(p, &full[stage], par, kSiteWaitStage);
+      const int nv = ok ? nvalid_s[stage] : 0;
+      if (nv > 0) {
+        const __half* Ks = reinterpret_cast<const __half*>(ring + (size_t)stage * 2 * kChunk);
+        page_update<G, P>(qf, acc, Ks, Ks + P * kHeadDim, nv, sc, st, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+  }
+  __syncthreads();  // ring idle: every copy of this tile has landed and been read
+
+  // ---- merge the 8 warps' states into this work item's partial
+  float* red = reinterpret_cast<float*>(ring);  // [warp][G][128]
+  if (warp < kConsumerWarps) {
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+      *reinterpret_cast<float4*>(red + ((size_t)warp * G + j) * kHeadDim + 4 * lane) =
+          make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+  }
+  __syncthreads();
+  for (int o = tid; o < G * kHeadDim; o += blockDim.x) {
+    const int j = o / kHeadDim, i = o % kHeadDim;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, st_all[(w * G + j) * 3]);
+    float A = 0.f, Ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = st_all[(w * G + j) * 3];
+      if (mw != -CUDART_INF_F) {
+        const float s = exp2f(mw - M);
+        A = fmaf(red[((size_t)w * G + j) * kHeadDim + i], s, A);
+        Ls = fmaf(st_all[(w * G + j) * 3 + 1], s, Ls);
+      }
+    }
+    const size_t slot = (size_t)(b * p.Hq + g * G + j) * p.n_splits + split;
+    p.part_acc[slot * kHeadDim + i] = A;
+    if (i == 0) {
+      p.part_ml[slot * 2] = M;
+      p.part_ml[slot * 2 + 1] = Ls;
+    }
+  }
+  fence_proxy_async_smem();  // generic use of the ring ends before the next bulk copies
+}
+
+// Log-sum-exp merge of the first n_live partials of every head of (b, g) into out / lse.
+template <int G>
+__device__ void merge_splits(const Params& p, unsigned char* smem, const SmemMap& m, int b,
+                             int g, int n_live) {
+  float* msc = reinterpret_cast<float*>(smem + m.mscale);  // [G][kMaxSplits + 2]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp < G) {
+    const int h = g * G + warp;
+    const float* ml = p.part_ml + (size_t)(b * p.Hq + h) * p.n_splits * 2;
+    float* row = msc + warp * (kMaxSplits + 2);
+    float M = -CUDART_INF_F;
+    for (int s = lane; s < n_live; s += 32) M = fmaxf(M, __ldcg(ml + 2 * s));
+    M = warp_max(M);
+    float Ls = 0.f;
+    for (int s = lane; s < n_live; s += 32) {
+      const float ms = __ldcg(ml + 2 * s);
+      const float f = (ms == -CUDART_INF_F) ? 0.f : exp2f(ms - M);
+      row[s] = f;
+      Ls = fmaf(__ldcg(ml + 2 * s + 1), f, Ls);
+    }
+    Ls = warp_sum(Ls);
+    if (lane == 0) {
+      row[kMaxSplits] = M;
+      row[kMaxSplits + 1] = Ls;
+    }
+  }
+  __syncthreads();
+  for (int o = tid; o < G * kHeadDim; o += blockDim.x) {
+    const int j = o / kHeadDim, i = o % kHeadDim;
+    const int h = g * G + j;
+    const float* row = msc + j * (kMaxSplits + 2);
+    const float Ls = row[kMaxSplits + 1];
+    const float* accp = p.part_acc + (size_t)(b * p.Hq + h) * p.n_splits * kHeadDim + i;
+    float A = 0.f;
+    for (int s = 0; s < n_live; ++s) {
+      const float f = row[s];
+      if (f != 0.f) A = fmaf(__ldcg(accp + (size_t)s * kHeadDim), f, A);
+    }
+    p.out[(size_t)(b * p.Hq + h) * kHeadDim + i] = __float2half_rn(Ls > 0.f ? A / Ls : 0.f);
+    if (i == 0 && p.lse)
+      p.lse[b * p.Hq + h] =
+          Ls > 0.f ? (row[kMaxSplits] + log2f(Ls)) * 0.69314718055994531f : -CUDART_INF_F;
+  }
+  __syncthreads();
+}
+
+// Shared prologue of the decode-capable kernels: ring barriers.
+__device__ __forceinline__ void init_ring(unsigned char* smem, const SmemMap& m) {
+  if (threadIdx.x == 0) {
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.full);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + m.empty);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+}
+
+}  // namespace quest

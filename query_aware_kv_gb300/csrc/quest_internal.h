@@ -1,0 +1,125 @@
+// quest_internal.h - declarations shared by the CUDA translation units of libquest.so.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "quest.h"
+
+namespace quest {
+
+constexpr int kHeadDim = 128;
+constexpr int kConsumerWarps = 8;           // warps that compute
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kDecodeThreads = kConsumerThreads + 32;  // + one bulk-copy producer warp
+constexpr int kStages = 8;                  // smem ring depth (pages in flight per CTA)
+constexpr int kMaxSplits = 256;             // split-K partials per (sequence, q head)
+constexpr int kDefaultPagesPerSplit = 8;
+constexpr int kDefaultScoreTilePages = 128;
+constexpr long long kDefaultWaitNs = 1000000000LL;
+
+// Places in the code that record a device fault (third detail word).
+enum FaultSite : int {
+  kSiteMeta = 1, kSiteAppend = 2, kSiteScore = 3, kSiteTopk = 4, kSiteDecode = 5,
+  kSiteWaitSelection = 6, kSiteWaitStage = 7, kSiteWaitSlot = 8, kSiteSelection = 9,
+};
+
+// First 256 bytes of the workspace.
+struct WsHeader {
+  int status;        // QUEST_OK or the first QUEST_ERR_* the device saw
+  int detail[3];     // sequence, logical page, fault site
+  unsigned ticket;   // fused kernel: next work item
+  unsigned exited;   // fused kernel: CTAs that left the work loop
+  unsigned epoch;    // fused kernel: launches completed (selection flags carry epoch + 1)
+  unsigned pad[57];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+struct Tiling {
+  int topk_cap;          // min(top_k, max_pages): slots per selection row
+  int score_tile_pages;  // pages per scoring work item
+  int n_score_tiles;     // scoring work items per (b, g)
+  int pps_sparse, n_splits_sparse;  // selected pages per decode item, items per (b, g)
+  int pps_dense, n_splits_dense;
+  int max_splits;
+};
+
+struct WsLayout {
+  size_t score_arrive, ready, decode_arrive;  // u32 [B*Hkv] each
+  size_t scores;                              // f32 [B*Hkv*max_pages]
+  size_t sel_idx, sel_count;                  // i32 [B*Hkv*topk_cap], [B*Hkv]
+  size_t part_ml, part_acc;                   // f32 [B*Hq*max_splits*2], [..*128]
+  size_t total;
+};
+
+// Everything a kernel needs, passed by value.
+struct Params {
+  int B, Hq, Hkv, P, max_pages, num_phys;
+  __half* k_pool;
+  __half* v_pool;
+  __half* meta;
+  const int* block_table;
+  int* seq_lens;
+
+  const __half* q;       // [B][Hq][128]
+  __half* out;           // [B][Hq][128]
+  float* lse;            // [B][Hq] or null
+  float* scores;         // [B][Hkv][max_pages]
+  int* sel_idx;          // [B][Hkv][top_k]
+  int* sel_count;        // [B][Hkv]
+  int top_k;             // row length of sel_idx (= requested K, capped at max_pages)
+
+  int score_tile_pages, n_score_tiles;
+  int pps, n_splits;     // decode work-item size and count per (b, g)
+  int dense;             // decode every page instead of a selection
+
+  int* status;           // -> WsHeader::status (detail follows it)
+  unsigned* ticket;
+  unsigned* exited;
+  unsigned* epoch;
+  unsigned* score_arrive;
+  unsigned* ready;
+  unsigned* decode_arrive;
+  float* part_ml;        // [B][Hq][n_splits][2]  (running max in log2 units, sum)
+  float* part_acc;       // [B][Hq][n_splits][128]
+
+  long long wait_limit_ns;
+  int debug_flags;
+  float qscale;          // log2(e) / sqrt(128)
+};
+
+// Launch with programmatic dependent launch allowed: the kernel may start while the
+// previous kernel on the stream finishes; every kernel calls griddepcontrol.wait before
+// touching memory an earlier kernel wrote.
+inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// Dynamic shared memory of the decode-capable kernels (bytes), see quest_device.cuh.
+size_t decode_smem_bytes(int G, int P, int topk_keys, int score_tile_pages);
+// Raise a kernel's dynamic shared-memory cap (once per device and kernel).
+cudaError_t ensure_smem(const void* fn, size_t bytes);
+
+cudaError_t launch_build_meta(const Params& p, cudaStream_t s);
+cudaError_t launch_append(const Params& p, const __half* k_new, const __half* v_new,
+                          cudaStream_t s);
+cudaError_t launch_estimate(const Params& p, int G, cudaStream_t s);
+cudaError_t launch_topk(const Params& p, cudaStream_t s);
+cudaError_t launch_decode(const Params& p, int G, cudaStream_t s);
+cudaError_t launch_fused(const Params& p, int G, int max_ctas, cudaStream_t s);
+
+}  // namespace quest

@@ -1,0 +1,161 @@
+// quest_step_kernels.cu - the three steps of a Quest decode step as separate launches:
+// page scoring, top-K selection, split-K sparse (or dense) flash-decode.
+#include <mutex>
+#include <unordered_map>
+
+#include "quest_device.cuh"
+
+namespace quest {
+
+size_t decode_smem_bytes(int G, int P, int topk_keys, int score_tile_pages) {
+  return make_smem_map(G, P, topk_keys, score_tile_pages).total;
+}
+
+// Raise the dynamic shared-memory cap of `fn` once per device.
+cudaError_t ensure_smem(const void* fn, size_t bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, size_t> done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto& m = done[dev & 63];
+  auto it = m.find(fn);
+  if (it != m.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) m[fn] = bytes;
+  return e;
+}
+
+// ---------------------------------------------------------------- scoring
+// grid (n_score_tiles, B*Hkv), 256 threads; dynamic smem: the tile's block-table slice.
+template <int G>
+__global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
+  extern __shared__ __align__(16) int bt_s[];
+  pdl_wait();
+  const int tile = blockIdx.x, bg = blockIdx.y;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int L = load_len(p, b, kSiteScore);
+  const int N = (L + p.P - 1) / p.P;
+  const int p0 = tile * p.score_tile_pages;
+  const int np = min(p.score_tile_pages, p.max_pages - p0);
+  const int n_live = max(0, min(N - p0, np));
+  float* row = p.scores + (size_t)bg * p.max_pages + p0;
+  for (int i = n_live + (int)threadIdx.x; i < np; i += blockDim.x) row[i] = -CUDART_INF_F;
+  if (n_live > 0) score_tile<G>(p, b, g, p0, n_live, row, bt_s);
+}
+
+// ---------------------------------------------------------------- top-K
+// grid (B*Hkv), 256 threads; dynamic smem: keys of one score row + histogram + scratch.
+__global__ void __launch_bounds__(kConsumerThreads) topk_kernel(Params p) {
+  extern __shared__ __align__(16) unsigned char sm[];
+  pdl_wait();
+  const int bg = blockIdx.x, b = bg / p.Hkv;
+  const int L = load_len(p, b, kSiteTopk);
+  const int N = (L + p.P - 1) / p.P;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(sm);
+  int* hist = reinterpret_cast<int*>(sm + align_up((size_t)p.max_pages * 4, 16));
+  int* scratch = hist + 256;
+  topk_select(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
+              p.sel_idx + (size_t)bg * p.top_k, p.sel_count + bg, keys, hist, scratch);
+}
+
+// ---------------------------------------------------------------- decode
+// grid (n_splits, B*Hkv), kDecodeThreads threads.  Work item `split` of (b, g) attends
+// over kept pages [split*pps, split*pps + pps); the last work item of (b, g) to finish
+// merges the partials.
+template <int G, int P>
+__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const SmemMap m = make_smem_map(G, P, 0, 0);
+  init_ring(smem, m);
+  pdl_wait();
+  const int split = blockIdx.x, bg = blockIdx.y;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int L = load_len(p, b, kSiteDecode);
+  const int N = (L + P - 1) / P;
+  int count = N;
+  const int* sel_row = nullptr;
+  if (!p.dense) {
+    count = p.sel_count[bg];
+    const int cap = min(p.top_k, N);
+    if (count < 0 || count > cap) {
+      if (threadIdx.x == 0 && split == 0) report(p, QUEST_ERR_BAD_SELECTION, b, count, kSiteSelection);
+      count = max(0, min(count, cap));
+    }
+    sel_row = p.sel_idx + (size_t)bg * p.top_k;
+  }
+  const int r0 = split * p.pps;
+  const int n_tile = max(0, min(count - r0, p.pps));
+  if (n_tile > 0) decode_tile<G, P>(p, smem, m, b, g, split, r0, n_tile, L, N, sel_row, 0u);
+  int* misc = reinterpret_cast<int*>(smem + m.misc);
+  if (arrive_last(&p.decode_arrive[bg], (unsigned)p.n_splits, misc)) {
+    merge_splits<G>(p, smem, m, b, g, (count + p.pps - 1) / p.pps);
+    if (threadIdx.x == 0) p.decode_arrive[bg] = 0u;
+  }
+}
+
+template <int G>
+static const void* estimate_fn() { return (const void*)estimate_kernel<G>; }
+
+template <int G, int P>
+static const void* decode_fn() { return (const void*)decode_kernel<G, P>; }
+
+static const void* pick_estimate(int G) {
+  switch (G) {
+    case 1: return estimate_fn<1>();
+    case 2: return estimate_fn<2>();
+    case 4: return estimate_fn<4>();
+    default: return estimate_fn<8>();
+  }
+}
+
+static const void* pick_decode(int G, int P) {
+  if (P == 16) {
+    switch (G) {
+      case 1: return decode_fn<1, 16>();
+      case 2: return decode_fn<2, 16>();
+      case 4: return decode_fn<4, 16>();
+      default: return decode_fn<8, 16>();
+    }
+  }
+  switch (G) {
+    case 1: return decode_fn<1, 32>();
+    case 2: return decode_fn<2, 32>();
+    case 4: return decode_fn<4, 32>();
+    default: return decode_fn<8, 32>();
+  }
+}
+
+cudaError_t launch_estimate(const Params& p, int G, cudaStream_t s) {
+  const void* fn = pick_estimate(G);
+  const size_t smem = align_up((size_t)p.score_tile_pages * 4, 16);
+  cudaError_t e = ensure_smem(fn, smem);
+  if (e != cudaSuccess) return e;
+  Params pp = p;
+  void* args[] = {&pp};
+  return launch_pdl(fn, dim3(p.n_score_tiles, p.B * p.Hkv), dim3(kConsumerThreads), smem, s,
+                    args);
+}
+
+cudaError_t launch_topk(const Params& p, cudaStream_t s) {
+  const void* fn = (const void*)topk_kernel;
+  const size_t smem = align_up((size_t)p.max_pages * 4, 16) + (256 + 64) * 4;
+  cudaError_t e = ensure_smem(fn, smem);
+  if (e != cudaSuccess) return e;
+  Params pp = p;
+  void* args[] = {&pp};
+  return launch_pdl(fn, dim3(p.B * p.Hkv), dim3(kConsumerThreads), smem, s, args);
+}
+
+cudaError_t launch_decode(const Params& p, int G, cudaStream_t s) {
+  const void* fn = pick_decode(G, p.P);
+  const size_t smem = decode_smem_bytes(G, p.P, 0, 0);
+  cudaError_t e = ensure_smem(fn, smem);
+  if (e != cudaSuccess) return e;
+  Params pp = p;
+  void* args[] = {&pp};
+  return launch_pdl(fn, dim3(p.n_splits, p.B * p.Hkv), dim3(kDecodeThreads), smem, s, args);
+}
+
+}  // namespace quest

@@ -1,0 +1,104 @@
+"""The C-ABI library builds, loads and exports every symbol include/quest.h declares; its
+host-side argument checks reject bad calls before any CUDA work (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import query_aware_kv_gb300 as q
+from query_aware_kv_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return q.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "quest.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(quest_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(q.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.quest_version() == 1
+
+
+def test_status_strings(lib):
+    assert lib.quest_status_string(0) == b"QUEST_OK"
+    assert lib.quest_status_string(q.QUEST_ERR_TIMEOUT) == b"QUEST_ERR_TIMEOUT"
+    assert lib.quest_status_string(99) == b"QUEST_ERR_UNKNOWN"
+
+
+def desc(**kw):
+    base = dict(batch=1, num_q_heads=4, num_kv_heads=4, head_dim=128, page_size=16,
+                max_pages=64, num_phys=64, k_pool=16, v_pool=32, meta=48, block_table=64,
+                seq_lens=80)
+    base.update(kw)
+    return q.QuestCacheDesc(*[base[f] for f, _ in q.QuestCacheDesc._fields_])
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(head_dim=64), "head_dim"),
+    (dict(page_size=8), "page_size"),
+    (dict(num_q_heads=12, num_kv_heads=4), "group size"),
+    (dict(num_q_heads=6, num_kv_heads=4), "multiple"),
+    (dict(max_pages=q.QUEST_MAX_PAGES + 1), "max_pages"),
+    (dict(k_pool=0), "NULL"),
+    (dict(meta=40), "aligned"),
+])
+def test_workspace_size_rejects_bad_descriptors(lib, kw, needle):
+    d = desc(**kw)
+    assert lib.quest_workspace_size(ctypes.byref(d), 16, None) == 0
+    assert needle in lib.quest_last_error().decode()
+
+
+def test_workspace_size_grows_with_top_k(lib):
+    d = desc()
+    a = lib.quest_workspace_size(ctypes.byref(d), 16, None)
+    b = lib.quest_workspace_size(ctypes.byref(d), 64, None)
+    assert 0 < a < b
+    assert lib.quest_workspace_size(ctypes.byref(d), 0, None) == 0
+
+
+def test_calls_reject_bad_arguments_without_launching(lib):
+    d = desc()
+    assert lib.quest_decode(None, 16, 16, 16, None, None, None, 256, 1 << 20, None, None) == \
+        q.QUEST_ERR_INVALID_ARG
+    # NULL workspace
+    assert lib.quest_decode(ctypes.byref(d), 16, 16, 16, None, None, None, None, 0, None,
+                            None) == q.QUEST_ERR_WORKSPACE
+    # workspace too small for this top_k
+    assert lib.quest_sparse_decode(ctypes.byref(d), 16, 16, 16, 16, 16, None, 256, 1024, None,
+                                   None) == q.QUEST_ERR_WORKSPACE
+    assert "needs" in lib.quest_last_error().decode()
+    # misaligned query
+    assert lib.quest_estimate(ctypes.byref(d), 18, 16, 256, 1 << 20, None) == \
+        q.QUEST_ERR_INVALID_ARG
+    # top_k out of range
+    assert lib.quest_topk(ctypes.byref(d), 16, 0, 16, 16, 256, 1 << 20, None) == \
+        q.QUEST_ERR_INVALID_ARG
+    # unsupported geometry
+    d2 = desc(page_size=64)
+    assert lib.quest_build_meta(ctypes.byref(d2), 256, 1 << 20, None) == q.QUEST_ERR_UNSUPPORTED
+    # an empty batch is a no-op
+    d3 = desc(batch=0)
+    assert lib.quest_append(ctypes.byref(d3), 16, 16, 256, 1 << 20, None) == q.QUEST_OK
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from query_aware_kv_gb300 import _lib
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _lib.load()

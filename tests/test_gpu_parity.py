@@ -1,0 +1,287 @@
+"""GPU parity of every step of the decode path against the CPU oracle, through the C ABI.
+
+Acceptance rules (see harness.py): boxes / appended tokens / lengths / top-K of identical
+scores bit-exact; scores within the fp32 reordering bound; selections equal outside the
+1e-5 relative tie window of the K-th score; attention |gpu - oracle| <= 2e-3 + 1e-2|oracle|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+import oracle
+import query_aware_kv_gb300 as q
+from query_aware_kv_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def small(name="small", batch=3, hq=4, hkv=4, P=16, lens=(300, 1, 77), steps=4, budget=128,
+          seed=0, **kw):
+    return wl.build(name, batch=batch, num_q_heads=hq, num_kv_heads=hkv, page_size=P,
+                    prefill_lens=list(lens), steps=steps, budget=budget, seed=seed, **kw)
+
+
+GEOMS = [
+    dict(hq=4, hkv=4, P=16),
+    dict(hq=8, hkv=4, P=16),
+    dict(hq=16, hkv=4, P=32),
+    dict(hq=32, hkv=4, P=16),
+    dict(hq=8, hkv=1, P=32),
+]
+
+
+@pytest.mark.parametrize("geom", GEOMS, ids=lambda g: f"hq{g['hq']}_hkv{g['hkv']}_p{g['P']}")
+def test_build_meta_bit_exact(geom):
+    w = small(lens=(300, 1, 77, 0, 64), batch=5, spare_pages=3, **geom)
+    pair = H.on_device(w)
+    H.assert_status_ok(pair.ws)
+    H.assert_meta_equal(pair)
+
+
+@pytest.mark.parametrize("geom", GEOMS[:3], ids=lambda g: f"hq{g['hq']}_hkv{g['hkv']}_p{g['P']}")
+def test_append_bit_exact(geom):
+    w = small(lens=(30, 0, 47), steps=40, **geom)
+    pair = H.on_device(w)
+    for t in range(w.steps):
+        q.append(pair.cache, w.k_new[t].cuda(), w.v_new[t].cuda(), pair.ws)
+        oracle.append(pair.ref, w.k_new[t].numpy(), w.v_new[t].numpy())
+    H.assert_status_ok(pair.ws)
+    assert pair.cache.seq_lens.cpu().tolist() == pair.ref.seq_lens.tolist()
+    H.assert_meta_equal(pair)
+    kp = pair.cache.k_pool.cpu().numpy()
+    vp = pair.cache.v_pool.cpu().numpy()
+    for b, p, ph in H.valid_pages(pair.ref):
+        n = min(w.page_size, int(pair.ref.seq_lens[b]) - p * w.page_size)
+        np.testing.assert_array_equal(kp[ph, :, :n].astype(np.float32), pair.ref.k_pool[ph, :, :n])
+        np.testing.assert_array_equal(vp[ph, :, :n].astype(np.float32), pair.ref.v_pool[ph, :, :n])
+
+
+@pytest.mark.parametrize("geom", GEOMS, ids=lambda g: f"hq{g['hq']}_hkv{g['hkv']}_p{g['P']}")
+def test_estimate_within_fp32_reordering(geom):
+    w = small(lens=(1000, 1, 333), outliers=4, **geom)
+    pair = H.on_device(w)
+    qh = w.q[0].numpy().astype(np.float32)
+    s = q.estimate(pair.cache, w.q[0].cuda(), pair.ws).cpu().numpy()
+    H.assert_status_ok(pair.ws)
+    ref = oracle.score(pair.ref, qh)
+    H.assert_scores_close(s, ref, H.score_tolerance(pair.ref, qh))
+
+
+@pytest.mark.parametrize("K", [1, 7, 16, 64, 200])
+def test_topk_bit_exact_on_identical_scores(K):
+    """Given the oracle's own scores, the selection must be exactly the oracle's."""
+    w = small(lens=(16 * 150 - 3, 5, 16 * 40), budget=16 * K)
+    pair = H.on_device(w)
+    ref = oracle.score(pair.ref, w.q[0].numpy())
+    idx, cnt = q.topk(pair.cache, torch.from_numpy(ref).cuda(), K, pair.ws)
+    H.assert_status_ok(pair.ws)
+    ri, rc = oracle.topk(pair.ref, ref, K)
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    assert np.array_equal(gc, rc)
+    for b in range(w.batch):
+        for g in range(w.num_kv_heads):
+            assert gi[b, g, :gc[b, g]].tolist() == sorted(ri[b, g, :rc[b, g]].tolist())
+            assert np.all(gi[b, g, gc[b, g]:] == -1)
+
+
+def test_topk_exact_ties_go_to_lower_index():
+    w = small(lens=(16 * 500,), batch=1, hq=2, hkv=2)
+    pair = H.on_device(w)
+    rng = np.random.default_rng(1)
+    scores = np.full((1, 2, w.block_table.shape[1]), -np.inf, np.float32)
+    scores[0, 0, :500] = rng.integers(0, 5, 500).astype(np.float32)   # heavy ties
+    scores[0, 1, :500] = 1.5                                           # all tied
+    for K in (1, 37, 100, 499):
+        idx, cnt = q.topk(pair.cache, torch.from_numpy(scores).cuda(), K, pair.ws)
+        ri, rc = oracle.topk(pair.ref, scores, K)
+        for g in range(2):
+            assert idx[0, g, :K].cpu().tolist() == sorted(ri[0, g, :K].tolist())
+    H.assert_status_ok(pair.ws)
+
+
+def test_topk_at_max_pages():
+    """The largest supported row: 16384 pages."""
+    n = q.QUEST_MAX_PAGES
+    w = small(lens=(16 * n,), batch=1, hq=1, hkv=1, steps=0, budget=16 * 512)
+    pair = H.on_device(w, build_meta=False)
+    rng = np.random.default_rng(2)
+    scores = rng.standard_normal((1, 1, n)).astype(np.float32)
+    scores[0, 0, ::7] = scores[0, 0, 3]  # some exact ties
+    for K in (1, 512, n - 1, n):
+        idx, cnt = q.topk(pair.cache, torch.from_numpy(scores).cuda(), K, pair.ws)
+        ri, rc = oracle.topk(pair.ref, scores, K)
+        assert int(cnt[0, 0]) == rc[0, 0]
+        assert idx[0, 0, :K].cpu().tolist() == sorted(ri[0, 0, :K].tolist())
+    H.assert_status_ok(pair.ws)
+
+
+@pytest.mark.parametrize("geom", GEOMS, ids=lambda g: f"hq{g['hq']}_hkv{g['hkv']}_p{g['P']}")
+@pytest.mark.parametrize("pps", [0, 1, 5])
+def test_sparse_decode_on_oracle_selection(geom, pps):
+    w = small(lens=(900, 1, 333, 0), batch=4, **geom)
+    pair = H.on_device(w, opts=q.opts(pages_per_split=pps))
+    qh = w.q[0].numpy()
+    ref_s = oracle.score(pair.ref, qh)
+    ri, rc = oracle.topk(pair.ref, ref_s, w.top_k)
+    out, lse = q.sparse_decode(pair.cache, w.q[0].cuda(), torch.from_numpy(ri).cuda(),
+                               torch.from_numpy(rc).cuda(), w.top_k, pair.ws,
+                               q.opts(pages_per_split=pps))
+    H.assert_status_ok(pair.ws)
+    ro, rl = oracle.attend(pair.ref, qh, ri, rc)
+    H.assert_attention_close(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("geom", GEOMS, ids=lambda g: f"hq{g['hq']}_hkv{g['hkv']}_p{g['P']}")
+def test_dense_decode_matches_oracle(geom):
+    w = small(lens=(2000, 1, 333, 0), batch=4, **geom)
+    pair = H.on_device(w)
+    qh = w.q[0].numpy()
+    out, lse = q.dense_decode(pair.cache, w.q[0].cuda(), pair.ws)
+    H.assert_status_ok(pair.ws)
+    ro, rl = oracle.dense(pair.ref, qh)
+    H.assert_attention_close(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("geom", GEOMS, ids=lambda g: f"hq{g['hq']}_hkv{g['hkv']}_p{g['P']}")
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "chain"])
+def test_decode_steps_match_oracle(geom, fused):
+    w = small(lens=(1500, 1, 333, 0, 16 * 30), batch=5, steps=6, outliers=4, **geom)
+    pair = H.on_device(w)
+    for t in range(w.steps):
+        H.run_step_and_compare(pair, t, w.top_k, fused=fused)
+
+
+def test_tiny_config():
+    w = wl.tiny(seed=0)
+    pair = H.on_device(w)
+    H.run_step_and_compare(pair, 0, w.top_k)
+
+
+def test_fused_equals_chain_bitwise():
+    w = small(lens=(3000, 700), batch=2, hq=8, hkv=4, budget=256, outliers=4)
+    pair = H.on_device(w)
+    qd = w.q[0].cuda()
+    o1, l1 = q.decode(pair.cache, qd, w.top_k, pair.ws)
+    s = q.estimate(pair.cache, qd, pair.ws)
+    idx, cnt = q.topk(pair.cache, s, w.top_k, pair.ws)
+    o2, l2 = q.sparse_decode(pair.cache, qd, idx, cnt, w.top_k, pair.ws)
+    H.assert_status_ok(pair.ws)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_split_invariance_and_repeatability():
+    w = small(lens=(5000, 2100), batch=2, hq=8, hkv=2, budget=1024, outliers=4)
+    pair = H.on_device(w, top_k=w.top_k, opts=q.opts(pages_per_split=1))
+    qd = w.q[0].cuda()
+    base, base_lse = q.decode(pair.cache, qd, w.top_k, pair.ws)
+    again, again_lse = q.decode(pair.cache, qd, w.top_k, pair.ws)
+    assert torch.equal(base, again) and torch.equal(base_lse, again_lse)
+    for pps, stp in [(1, 16), (3, 64), (8, 128), (32, 1000), (64, 7)]:
+        o = q.opts(pages_per_split=pps, score_tile_pages=stp)
+        out, lse = q.decode(pair.cache, qd, w.top_k, pair.ws, o)
+        torch.testing.assert_close(out.float(), base.float(), atol=2e-3, rtol=0)
+        torch.testing.assert_close(lse, base_lse, atol=1e-4, rtol=0)
+    H.assert_status_ok(pair.ws)
+
+
+def test_workspace_reuse_many_calls():
+    w = small(lens=(4000, 100, 2500), budget=512)
+    pair = H.on_device(w)
+    qd = w.q[0].cuda()
+    first, _ = q.decode(pair.cache, qd, w.top_k, pair.ws)
+    for _ in range(50):
+        out, _ = q.decode(pair.cache, qd, w.top_k, pair.ws)
+    H.assert_status_ok(pair.ws)
+    assert torch.equal(first, out)
+    # the header counters are back to zero, the epoch counts the launches
+    hdr = pair.ws[:32].view(torch.int32).cpu().tolist()
+    assert hdr[4] == 0 and hdr[5] == 0 and hdr[6] == 51
+
+
+def test_planted_needles_selected_on_gpu():
+    w = wl.build("needles", batch=2, num_q_heads=8, num_kv_heads=8, page_size=16,
+                 prefill_lens=[8192, 5000], steps=4, budget=512, seed=3, outliers=4,
+                 needles_per_head=8, needle_mode="direction")
+    pair = H.on_device(w)
+    for t in range(w.steps):
+        H.run_step_and_compare(pair, t, w.top_k, check_needles=True)
+
+
+def test_empty_and_single_token_sequences():
+    w = small(lens=(0, 1, 0), steps=2)
+    pair = H.on_device(w)
+    qd = w.q[0].cuda()
+    out, lse = q.decode(pair.cache, qd, w.top_k, pair.ws)
+    H.assert_status_ok(pair.ws)
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    phys = int(w.block_table[1, 0])
+    ro, rl = oracle.dense(pair.ref, w.q[0].numpy())
+    H.assert_attention_close(out, lse, ro, rl)
+    for t in range(w.steps):
+        H.run_step_and_compare(pair, t, w.top_k)
+
+
+# ---------------------------------------------------------------- device-side faults
+# Every fault below is caught by the kernels' own bounds checks (they skip the access and
+# record a status); nothing here faults, traps or hangs the GPU.
+
+def test_bad_block_table_entry_is_reported():
+    w = small(lens=(300, 200), batch=2)
+    bt = w.block_table.clone()
+    bt[1, 3] = w.num_phys + 5          # out of the pool
+    w.block_table = bt
+    pair = H.on_device(w, build_meta=False)
+    q.build_meta(pair.cache, pair.ws)
+    rc, detail = q.read_status(pair.ws)
+    assert rc == q.QUEST_ERR_BAD_PAGE and detail[0] == 1 and detail[1] == 3
+    q.workspace_init(pair.ws)
+    q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws)
+    rc, detail = q.read_status(pair.ws)
+    assert rc == q.QUEST_ERR_BAD_PAGE
+
+
+def test_bad_lengths_are_reported():
+    w = small(lens=(300,), batch=1, steps=1)
+    pair = H.on_device(w)
+    cap = w.block_table.shape[1] * w.page_size
+    pair.cache.seq_lens.fill_(cap)                 # full row: append has no room
+    q.append(pair.cache, w.q[0, :, :4].contiguous().cuda(), w.q[0, :, :4].contiguous().cuda(),
+             pair.ws)
+    rc, _ = q.read_status(pair.ws)
+    assert rc == q.QUEST_ERR_BAD_LENGTH
+    assert int(pair.cache.seq_lens[0]) == cap      # untouched
+    pair.cache.seq_lens.fill_(cap + 1)             # beyond the row
+    q.workspace_init(pair.ws)
+    q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws)
+    rc, _ = q.read_status(pair.ws)
+    assert rc == q.QUEST_ERR_BAD_LENGTH
+
+
+def test_bad_selection_is_reported():
+    w = small(lens=(300,), batch=1)
+    pair = H.on_device(w)
+    idx = torch.full((1, 4, w.top_k), 2, dtype=torch.int32, device="cuda")
+    idx[0, 1, 0] = 1000                            # past the sequence's pages
+    cnt = torch.full((1, 4), 3, dtype=torch.int32, device="cuda")
+    q.sparse_decode(pair.cache, w.q[0].cuda(), idx, cnt, w.top_k, pair.ws)
+    rc, detail = q.read_status(pair.ws)
+    assert rc == q.QUEST_ERR_BAD_SELECTION and detail[1] == 1000
+    cnt.fill_(w.top_k + 1)                         # count above top_k
+    q.workspace_init(pair.ws)
+    q.sparse_decode(pair.cache, w.q[0].cuda(), idx, cnt, w.top_k, pair.ws)
+    rc, _ = q.read_status(pair.ws)
+    assert rc == q.QUEST_ERR_BAD_SELECTION
+
+
+def test_withheld_selection_times_out_and_context_survives():
+    """A flag that nothing sets: every decode item's bounded wait runs out (20 ms), the
+    call reports QUEST_ERR_TIMEOUT, and the next normal call works."""
+    w = small(lens=(3000, 2000), batch=2, budget=256)
+    pair = H.on_device(w)
+    o = q.opts(debug_flags=q.QUEST_DEBUG_WITHHOLD_SELECTION, wait_limit_ns=20_000_000)
+    q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws, o)
+    rc, detail = q.read_status(pair.ws)
+    assert rc == q.QUEST_ERR_TIMEOUT
+    q.workspace_init(pair.ws)
+    H.run_step_and_compare(pair, 0, w.top_k)
