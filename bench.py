@@ -36,7 +36,9 @@ def parse():
     ap.add_argument("--impl", default="quest", choices=["quest", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
+    ap.add_argument("--profile-decode", type=int, default=0, metavar="N",
+                    help="profiling run for ncu: set up, --warmup steps, then N quest_decode "
+                         "launches; no L2 flush buffer, no timing, no JSON line")
     return ap.parse_args()
 
 
@@ -228,7 +230,7 @@ def run_quest(args):
     build_meta_us = 1e3 * t0.elapsed_time(t1)
     meta0 = cache.meta.clone()
     len0 = w.seq_lens.clone()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = None if args.profile_decode else torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     out = torch.empty((1, w.num_q_heads, 128), dtype=torch.float16, device=dev)
     lse = torch.empty((1, w.num_q_heads), dtype=torch.float32, device=dev)
     idx = torch.empty((1, w.num_kv_heads, K), dtype=torch.int32, device=dev)
@@ -242,6 +244,18 @@ def run_quest(args):
     def step(t):
         q.append(cache, w.k_new[t], w.v_new[t], ws)
         q.decode(cache, w.q[t], K, ws, out=out, lse=lse, idx_out=idx, count_out=cnt)
+
+    if args.profile_decode:
+        rewind()
+        for i in range(args.warmup):
+            step(i % w.steps)
+        for i in range(args.profile_decode):
+            q.decode(cache, w.q[i % w.steps], K, ws, out=out, lse=lse, idx_out=idx, count_out=cnt)
+        torch.cuda.synchronize()
+        rc, detail = q.read_status(ws)
+        print(f"profile run: {args.warmup} steps + {args.profile_decode} quest_decode launches, "
+              f"status {rc}", flush=True)
+        return
 
     # warm-up
     rewind()
