@@ -195,6 +195,27 @@ int quest_dense_decode(const quest_cache_t* cache, const void* q, void* out, flo
                        quest_stream_t stream);
 
 /*
+ * quest_decode for callers that cannot allocate device memory.  The papers have no
+ * counterpart to this call; it exists for callers that are handed their tensors but may
+ * not obtain device memory themselves (an extension hosted by a runtime that owns the
+ * allocator, an engine that forbids allocation while serving, a binding with no device
+ * allocator), so they cannot pass quest_decode a workspace.  Same arguments and results as
+ * quest_decode without ws / ws_bytes / opts (defaults are used).  The scratch is a 16 MiB
+ * array in the library's own device memory (present on every GPU that loads the library,
+ * until the process exits); a cache / top_k whose quest_workspace_size() exceeds 16 MiB is
+ * rejected with QUEST_ERR_WORKSPACE.  Nothing is allocated.
+ * - The first call on each device looks up that array's device address (with the device
+ *   current); make that first call before any stream capture.
+ * - Every call, on every stream, shares the one array: calls that may overlap on the GPU
+ *   race and give wrong results.  Each call clears the part that must start at zero.
+ * - status_out (nullable, device int32[4]) receives the device status word and its three
+ *   detail words (see quest_read_status) once the call's work is done, in stream order.
+ */
+int quest_decode_static(const quest_cache_t* cache, const void* q, int32_t top_k, void* out,
+                        float* lse, int32_t* idx_out, int32_t* count_out, int32_t* status_out,
+                        quest_stream_t stream);
+
+/*
  * Synchronise `stream`, return the device status recorded in the workspace (QUEST_OK
  * or a QUEST_ERR_* code) and clear it.  detail (nullable, 3 ints) receives the first
  * fault's sequence, logical page and a kernel-specific code.

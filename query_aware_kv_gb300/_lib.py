@@ -37,7 +37,7 @@ HEAD_DIM = 128
 EXPORTS = (
     "quest_workspace_size", "quest_workspace_init", "quest_build_meta", "quest_append",
     "quest_estimate", "quest_topk", "quest_sparse_decode", "quest_decode",
-    "quest_dense_decode", "quest_read_status", "quest_last_error", "quest_status_string",
+    "quest_dense_decode", "quest_decode_static", "quest_read_status", "quest_last_error", "quest_status_string",
     "quest_version",
 )
 

@@ -159,6 +159,23 @@ int group_of(const quest_cache_t* c) { return c->num_q_heads / c->num_kv_heads; 
 
 }  // namespace
 
+namespace quest {
+
+int decode_workspace_requirement(const quest_cache_t* cache, int top_k, size_t* total,
+                                 size_t* zeroed) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if ((rc = check_topk(top_k))) return rc;
+  const WsLayout L = make_layout(cache, make_tiling(cache, top_k, nullptr));
+  *total = L.total;
+  *zeroed = L.scores;
+  return QUEST_OK;
+}
+
+int set_last_error(int code, const char* message) { return fail(code, "%s", message); }
+
+}  // namespace quest
+
 extern "C" {
 
 int quest_version(void) { return QUEST_VERSION; }

@@ -114,6 +114,14 @@ size_t decode_smem_bytes(int G, int P, int topk_keys, int score_tile_pages);
 // Raise a kernel's dynamic shared-memory cap (once per device and kernel).
 cudaError_t ensure_smem(const void* fn, size_t bytes);
 
+// Host-side checks of quest_decode's cache / top_k arguments (status code, error text
+// set), and the workspace bytes it needs: `total`, of which the first `zeroed` bytes
+// (status word, queue, counters, selection flags) must be zero when a call starts.
+int decode_workspace_requirement(const quest_cache_t* cache, int top_k, size_t* total,
+                                 size_t* zeroed);
+// Record a failure for quest_last_error(); returns `code`.
+int set_last_error(int code, const char* message);
+
 cudaError_t launch_build_meta(const Params& p, cudaStream_t s);
 cudaError_t launch_append(const Params& p, const __half* k_new, const __half* v_new,
                           cudaStream_t s);
