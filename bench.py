@@ -36,6 +36,10 @@ def parse():
     ap.add_argument("--impl", default="quest", choices=["quest", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--decode-lag", type=int, default=0)
+    ap.add_argument("--pages-per-split", type=int, default=0)
+    ap.add_argument("--score-tile-pages", type=int, default=0)
+    ap.add_argument("--trace", default="", help="write a fused-kernel timeline (npy) here")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="N",
                     help="profiling run for ncu: set up, --warmup steps, then N quest_decode "
                          "launches; no L2 flush buffer, no timing, no JSON line")
@@ -236,21 +240,24 @@ def run_quest(args):
     idx = torch.empty((1, w.num_kv_heads, K), dtype=torch.int32, device=dev)
     cnt = torch.empty((1, w.num_kv_heads), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
+    opts_main = q.opts(decode_lag=args.decode_lag, pages_per_split=args.pages_per_split,
+                       score_tile_pages=args.score_tile_pages)
 
     def rewind():
         cache.meta.copy_(meta0)
         cache.seq_lens.copy_(len0)
 
     def step(t):
-        q.append(cache, w.k_new[t], w.v_new[t], ws)
-        q.decode(cache, w.q[t], K, ws, out=out, lse=lse, idx_out=idx, count_out=cnt)
+        q.decode_step(cache, w.q[t], w.k_new[t], w.v_new[t], K, ws, opts_main, out=out, lse=lse,
+                      idx_out=idx, count_out=cnt)
 
     if args.profile_decode:
         rewind()
         for i in range(args.warmup):
             step(i % w.steps)
         for i in range(args.profile_decode):
-            q.decode(cache, w.q[i % w.steps], K, ws, out=out, lse=lse, idx_out=idx, count_out=cnt)
+            q.decode(cache, w.q[i % w.steps], K, ws, opts_main, out=out, lse=lse, idx_out=idx,
+                     count_out=cnt)
         torch.cuda.synchronize()
         rc, detail = q.read_status(ws)
         print(f"profile run: {args.warmup} steps + {args.profile_decode} quest_decode launches, "
@@ -307,10 +314,21 @@ def run_quest(args):
     for i in range(kn):
         flush.zero_()
         kev[i][0].record()
-        q.decode(cache, w.q[i % w.steps], K, ws, out=out, lse=lse, idx_out=idx, count_out=cnt)
+        q.decode(cache, w.q[i % w.steps], K, ws, opts_main, out=out, lse=lse, idx_out=idx,
+                 count_out=cnt)
         kev[i][1].record()
     torch.cuda.synchronize()
     dec_us = sum(1e3 * a.elapsed_time(b) for a, b in kev) / kn
+    if args.trace:
+        cap = 1 << 16
+        tr = torch.zeros(1 + 2 * cap, dtype=torch.int64, device=dev)
+        o_tr = q.opts(decode_lag=args.decode_lag, pages_per_split=args.pages_per_split,
+                      score_tile_pages=args.score_tile_pages, trace=tr)
+        flush.zero_()
+        q.decode(cache, w.q[0], K, ws, o_tr, out=out, lse=lse)
+        torch.cuda.synchronize()
+        n_rec = min(int(tr[0]), cap)
+        np.save(args.trace, tr[1:1 + 2 * n_rec].view(n_rec, 2).cpu().numpy())
     tok = selected_tokens(idx, cnt, L_fixed)
     dec_bytes = decode_bytes(L_fixed, tok, 1, w.num_q_heads, w.num_kv_heads)
 
@@ -362,8 +380,7 @@ def run_quest(args):
         dq.copy_(hq[t], non_blocking=True)
         dk.copy_(hk[t], non_blocking=True)
         dv.copy_(hv[t], non_blocking=True)
-        q.append(cache, dk, dv, ws)
-        q.decode(cache, dq, K, ws, out=out, lse=lse)
+        q.decode_step(cache, dq, dk, dv, K, ws, opts_main, out=out, lse=lse)
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
         eev[i][1].record()
@@ -399,7 +416,7 @@ def run_quest(args):
         "data": "synthetic (seeded N(0,1) fp16 K/V, 4 key channels x8, 8 planted needles/head)",
         "config": {**w.describe(), "storage": "fp16 K/V/q/out, fp32 arithmetic",
                    "l2": "flushed before every timed step (512 MiB write)",
-                   "step": "quest_append + quest_decode (fused score, top-K, split-K decode)",
+                   "step": "quest_decode_step: append + score + top-K + split-K decode, one launch",
                    "replicas": world},
         "gbs": round(world * step_bytes / (mean_step * 1e-6) / 1e9, 1),
         "roofline": {"bound": "hbm", "kernel": "quest_decode (fused)",
@@ -410,7 +427,7 @@ def run_quest(args):
                      "traffic": traffic},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * n,
+        "gpu_launches": n,
         "clocks": clk.summary(),
         "detail_us": {"step_mean": round(mean_step, 3), "step_p50": round(statistics.median(step_us), 3),
                       "quest_decode": round(dec_us, 3), "unfused_chain": round(chain_us, 3),

@@ -70,9 +70,12 @@ typedef void* quest_stream_t; /* cudaStream_t */
  *   k_pool, v_pool : fp16 [num_phys][num_kv_heads][page_size][128]; token t of sequence
  *                    b lives in physical page block_table[b][t / page_size], slot
  *                    t % page_size.  One (page, kv head) chunk is contiguous.
- *   meta           : fp16 [num_phys][num_kv_heads][2][128]: per (page, kv head) the
- *                    per-dimension key minimum (row 0) and maximum (row 1) over the
- *                    tokens present ([Guide] Solution step 1).
+ *   meta           : fp16 [batch][num_kv_heads][max_pages][2][128]: for logical page p of
+ *                    sequence b and kv head g, the per-dimension key minimum (row 0) and
+ *                    maximum (row 1) over the tokens present ([Guide] Solution step 1).
+ *                    Boxes are kept per sequence in logical page order (not per physical
+ *                    page) so that scoring streams them contiguously without the block
+ *                    table.
  *   block_table    : int32 [batch][max_pages], logical page -> physical page.  Entries at
  *                    or past ceil(seq_len / page_size) are never read.
  *   seq_lens       : int32 [batch], tokens present; only quest_append writes it.
@@ -100,6 +103,14 @@ typedef struct quest_opts {
     int32_t max_ctas;         /* fused kernel: cap on persistent CTAs (0 = all that fit)  */
     int32_t debug_flags;      /* QUEST_DEBUG_* (0 in normal use)                          */
     int64_t wait_limit_ns;    /* bound on any inter-CTA wait (default 1e9 ns)             */
+    int32_t decode_lag;       /* fused kernel: a (b, g)'s decode items are queued after the
+                                 scoring items of the next decode_lag (b, g) pairs
+                                 (<= 0: default 16)                                         */
+    int32_t trace_capacity;   /* fused kernel: records `trace` can hold                   */
+    uint64_t* trace;          /* fused kernel: optional device timeline, NULL = off.
+                                 trace[0] counts records (zero it before the call); record i
+                                 is trace[1 + 2i] = %globaltimer ns, trace[2 + 2i] =
+                                 smid << 48 | cta << 32 | event << 24 | item              */
 } quest_opts_t;
 
 /* quest_decode only: never publish the selection, so that every decode work item's
@@ -185,6 +196,19 @@ int quest_sparse_decode(const quest_cache_t* cache, const void* q, const int32_t
 int quest_decode(const quest_cache_t* cache, const void* q, int32_t top_k, void* out,
                  float* lse, int32_t* idx_out, int32_t* count_out, void* ws, size_t ws_bytes,
                  const quest_opts_t* opts, quest_stream_t stream);
+
+/*
+ * One whole decode step in one launch: the append of quest_append (k_new, v_new: fp16
+ * [batch][num_kv_heads][128], NULL for none) folded into quest_decode.  The scoring work
+ * item that holds the new token's page widens (or opens) that page's box, writes the
+ * token's K/V rows and scores the page with the updated box; selection and attention
+ * then cover seq_len + 1 tokens; seq_lens[b] becomes seq_len + 1 when the launch ends.
+ * Results equal quest_append followed by quest_decode.
+ */
+int quest_decode_step(const quest_cache_t* cache, const void* q, const void* k_new,
+                      const void* v_new, int32_t top_k, void* out, float* lse, int32_t* idx_out,
+                      int32_t* count_out, void* ws, size_t ws_bytes, const quest_opts_t* opts,
+                      quest_stream_t stream);
 
 /*
  * Full-context attention over every token (every page kept): the library's own dense

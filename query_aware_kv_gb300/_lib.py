@@ -37,8 +37,8 @@ HEAD_DIM = 128
 EXPORTS = (
     "quest_workspace_size", "quest_workspace_init", "quest_build_meta", "quest_append",
     "quest_estimate", "quest_topk", "quest_sparse_decode", "quest_decode",
-    "quest_dense_decode", "quest_decode_static", "quest_read_status", "quest_last_error", "quest_status_string",
-    "quest_version",
+    "quest_decode_step", "quest_dense_decode", "quest_decode_static", "quest_read_status",
+    "quest_last_error", "quest_status_string", "quest_version",
 )
 
 
@@ -63,7 +63,8 @@ class QuestOpts(ctypes.Structure):
     _fields_ = [
         ("pages_per_split", ctypes.c_int32), ("score_tile_pages", ctypes.c_int32),
         ("max_ctas", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
-        ("wait_limit_ns", ctypes.c_int64),
+        ("wait_limit_ns", ctypes.c_int64), ("decode_lag", ctypes.c_int32),
+        ("trace_capacity", ctypes.c_int32), ("trace", ctypes.c_void_p),
     ]
 
 
@@ -94,6 +95,7 @@ def load() -> ctypes.CDLL:
             "quest_topk": (ctypes.c_int, [C, V, I32, V, V, V, SZ, V]),
             "quest_sparse_decode": (ctypes.c_int, [C, V, V, V, I32, V, V, V, SZ, O, V]),
             "quest_decode": (ctypes.c_int, [C, V, I32, V, V, V, V, V, SZ, O, V]),
+            "quest_decode_step": (ctypes.c_int, [C, V, V, V, I32, V, V, V, V, V, SZ, O, V]),
             "quest_dense_decode": (ctypes.c_int, [C, V, V, V, V, SZ, O, V]),
             "quest_read_status": (ctypes.c_int, [V, SZ, V, ctypes.POINTER(I32)]),
             "quest_last_error": (ctypes.c_char_p, []),
@@ -137,8 +139,18 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
 
 
 def opts(pages_per_split: int = 0, score_tile_pages: int = 0, max_ctas: int = 0,
-         debug_flags: int = 0, wait_limit_ns: int = 0) -> QuestOpts:
-    return QuestOpts(pages_per_split, score_tile_pages, max_ctas, debug_flags, wait_limit_ns)
+         debug_flags: int = 0, wait_limit_ns: int = 0, decode_lag: int = 0,
+         trace: Optional[torch.Tensor] = None) -> QuestOpts:
+    """Launch tuning (0 = default).  ``trace``: int64 CUDA tensor of 1 + 2n elements whose
+    first element is zero; receives up to n timeline records of the fused kernel."""
+    cap, ptr = 0, None
+    if trace is not None:
+        _need(trace, "trace", torch.int64)
+        cap, ptr = (trace.numel() - 1) // 2, trace.data_ptr()
+    o = QuestOpts(pages_per_split, score_tile_pages, max_ctas, debug_flags, wait_limit_ns,
+                  decode_lag, cap, ptr)
+    o._trace_ref = trace  # keep the buffer alive with the options
+    return o
 
 
 def _opts_ref(o: Optional[QuestOpts]):
@@ -149,8 +161,9 @@ def _opts_ref(o: Optional[QuestOpts]):
 class PagedCache:
     """One layer's paged fp16 KV cache with per-page key min/max (device tensors).
 
-    k_pool, v_pool: [num_phys][Hkv][P][128] fp16; meta: [num_phys][Hkv][2][128] fp16;
-    block_table: [B][max_pages] int32; seq_lens: [B] int32 (advanced by ``append``).
+    k_pool, v_pool: [num_phys][Hkv][P][128] fp16; meta: [B][Hkv][max_pages][2][128] fp16
+    (boxes per sequence, logical page order); block_table: [B][max_pages] int32;
+    seq_lens: [B] int32 (advanced by ``append`` / ``decode_step``).
     """
     k_pool: torch.Tensor
     v_pool: torch.Tensor
@@ -164,7 +177,7 @@ class PagedCache:
         B, max_pages = self.block_table.shape
         _need(self.k_pool, "k_pool", torch.float16)
         _need(self.v_pool, "v_pool", torch.float16, self.k_pool.shape)
-        _need(self.meta, "meta", torch.float16, (num_phys, hkv, 2, d))
+        _need(self.meta, "meta", torch.float16, (B, hkv, max_pages, 2, d))
         _need(self.block_table, "block_table", torch.int32)
         _need(self.seq_lens, "seq_lens", torch.int32, (B,))
         self.desc = QuestCacheDesc(B, int(self.num_q_heads), hkv, d, P, max_pages, num_phys,
@@ -175,7 +188,8 @@ class PagedCache:
     @classmethod
     def allocate_meta(cls, k_pool, v_pool, block_table, seq_lens, num_q_heads):
         num_phys, hkv, P, d = k_pool.shape
-        meta = torch.zeros((num_phys, hkv, 2, d), dtype=torch.float16, device=k_pool.device)
+        B, max_pages = block_table.shape
+        meta = torch.zeros((B, hkv, max_pages, 2, d), dtype=torch.float16, device=k_pool.device)
         return cls(k_pool, v_pool, meta, block_table, seq_lens, num_q_heads)
 
     @property
@@ -290,6 +304,27 @@ def decode(cache: PagedCache, q: torch.Tensor, top_k: int, ws: torch.Tensor,
     _check(load().quest_decode(ctypes.byref(cache.desc), q.data_ptr(), int(top_k), out.data_ptr(),
                                _ptr(lse), _ptr(idx_out), _ptr(count_out), ws.data_ptr(),
                                ws.numel(), _opts_ref(o), _stream(stream)))
+    return out, lse
+
+
+def decode_step(cache: PagedCache, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                top_k: int, ws: torch.Tensor, o: Optional[QuestOpts] = None, out=None, lse=None,
+                want_lse: bool = True, idx_out: Optional[torch.Tensor] = None,
+                count_out: Optional[torch.Tensor] = None, stream=None):
+    """Append (k_new, v_new) and run the fused decode step, in one launch."""
+    _need(q, "q", torch.float16, (cache.batch, cache.desc.num_q_heads, HEAD_DIM))
+    shape = (cache.batch, cache.num_kv_heads, HEAD_DIM)
+    _need(k_new, "k_new", torch.float16, shape)
+    _need(v_new, "v_new", torch.float16, shape)
+    out, lse = _out(cache, q, out, lse, want_lse)
+    if idx_out is not None:
+        _need(idx_out, "idx_out", torch.int32, (cache.batch, cache.num_kv_heads, top_k))
+    if count_out is not None:
+        _need(count_out, "count_out", torch.int32, (cache.batch, cache.num_kv_heads))
+    _check(load().quest_decode_step(ctypes.byref(cache.desc), q.data_ptr(), k_new.data_ptr(),
+                                    v_new.data_ptr(), int(top_k), out.data_ptr(), _ptr(lse),
+                                    _ptr(idx_out), _ptr(count_out), ws.data_ptr(), ws.numel(),
+                                    _opts_ref(o), _stream(stream)))
     return out, lse
 
 

@@ -295,9 +295,10 @@ int quest_sparse_decode(const quest_cache_t* cache, const void* q, const int32_t
                   "quest_sparse_decode");
 }
 
-int quest_decode(const quest_cache_t* cache, const void* q, int32_t top_k, void* out, float* lse,
-                 int32_t* idx_out, int32_t* count_out, void* ws, size_t ws_bytes,
-                 const quest_opts_t* opts, quest_stream_t stream) {
+static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_new,
+                       const void* v_new, int32_t top_k, void* out, float* lse, int32_t* idx_out,
+                       int32_t* count_out, void* ws, size_t ws_bytes, const quest_opts_t* opts,
+                       quest_stream_t stream, const char* what) {
   int rc = check_cache(cache);
   if (rc) return rc;
   if ((rc = check_topk(top_k))) return rc;
@@ -305,6 +306,10 @@ int quest_decode(const quest_cache_t* cache, const void* q, int32_t top_k, void*
   if (!q || !out || !aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(idx_out, 4) || !aligned(count_out, 4))
     return fail(QUEST_ERR_INVALID_ARG, "q / out must be non-NULL and aligned");
+  if ((k_new == nullptr) != (v_new == nullptr) || !aligned(k_new, 16) || !aligned(v_new, 16))
+    return fail(QUEST_ERR_INVALID_ARG, "k_new and v_new must both be NULL or both 16-byte aligned");
+  if (opts && opts->trace && (opts->trace_capacity < 0 || !aligned(opts->trace, 8)))
+    return fail(QUEST_ERR_INVALID_ARG, "trace must be 8-byte aligned with trace_capacity >= 0");
   const Tiling t = make_tiling(cache, top_k, opts);
   const WsLayout L = make_layout(cache, t);
   if ((rc = check_ws(ws, ws_bytes, L.total))) return rc;
@@ -318,12 +323,34 @@ int quest_decode(const quest_cache_t* cache, const void* q, int32_t top_k, void*
   p.pps = t.pps_sparse;
   p.n_splits = t.n_splits_sparse;
   p.dense = 0;
+  p.k_new = static_cast<const __half*>(k_new);
+  p.v_new = static_cast<const __half*>(v_new);
+  p.decode_lag = (opts && opts->decode_lag > 0) ? opts->decode_lag : kDefaultDecodeLag;
+  p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
+  p.trace_capacity = opts ? opts->trace_capacity : 0;
   const long long items = (long long)cache->batch * cache->num_kv_heads *
                           ((long long)t.n_score_tiles + t.n_splits_sparse);
   if (items > 0x7fffffffLL) return fail(QUEST_ERR_UNSUPPORTED, "too many work items");
   return launched(launch_fused(p, group_of(cache), opts ? opts->max_ctas : 0,
                                static_cast<cudaStream_t>(stream)),
-                  "quest_decode");
+                  what);
+}
+
+int quest_decode(const quest_cache_t* cache, const void* q, int32_t top_k, void* out, float* lse,
+                 int32_t* idx_out, int32_t* count_out, void* ws, size_t ws_bytes,
+                 const quest_opts_t* opts, quest_stream_t stream) {
+  return decode_impl(cache, q, nullptr, nullptr, top_k, out, lse, idx_out, count_out, ws,
+                     ws_bytes, opts, stream, "quest_decode");
+}
+
+int quest_decode_step(const quest_cache_t* cache, const void* q, const void* k_new,
+                      const void* v_new, int32_t top_k, void* out, float* lse, int32_t* idx_out,
+                      int32_t* count_out, void* ws, size_t ws_bytes, const quest_opts_t* opts,
+                      quest_stream_t stream) {
+  if (!k_new || !v_new)
+    return fail(QUEST_ERR_INVALID_ARG, "quest_decode_step needs k_new and v_new");
+  return decode_impl(cache, q, k_new, v_new, top_k, out, lse, idx_out, count_out, ws, ws_bytes,
+                     opts, stream, "quest_decode_step");
 }
 
 int quest_dense_decode(const quest_cache_t* cache, const void* q, void* out, float* lse, void* ws,

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(256) build_meta_kernel(Params p) {
     mn[k] = __hmin2(mn[k], *reinterpret_cast<const __half2*>(&a));
     mx[k] = __hmax2(mx[k], *reinterpret_cast<const __half2*>(&z));
   }
-  __half2* dst = reinterpret_cast<__half2*>(p.meta + ((size_t)phys * p.Hkv + g) * 2 * kHeadDim +
+  __half2* dst = reinterpret_cast<__half2*>(p.meta + box_offset(p, b, g, pg) +
                                             (hw ? kHeadDim : 0) + 8 * c);
   const __half2* v = hw ? mx : mn;
   uint4 o;
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(256) append_kernel(Params p, const __half* k_n
     const uint4 mine = upper ? *reinterpret_cast<const uint4*>(v_new + row) : kk;
     const size_t kv_off = (((size_t)phys * p.Hkv + g) * P + slot) * kHeadDim + 8 * c;
     *reinterpret_cast<uint4*>((upper ? p.v_pool : p.k_pool) + kv_off) = mine;
-    uint4* box = reinterpret_cast<uint4*>(p.meta + ((size_t)phys * p.Hkv + g) * 2 * kHeadDim +
+    uint4* box = reinterpret_cast<uint4*>(p.meta + box_offset(p, b, g, L / P) +
                                           (upper ? kHeadDim : 0) + 8 * c);
     uint4 res = kk;
     if (slot != 0) {

@@ -91,14 +91,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// The waiting thread may be suspended until the phase completes (at most ~100 us per
+// call), so waiting warps do not take issue slots from working ones.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
       : "memory");
   return ok != 0;
 }
@@ -131,6 +133,12 @@ __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// Offset (in halves) of the box record of logical page `page` of (sequence b, kv head g):
+// boxes are kept per sequence in logical page order, [B][Hkv][max_pages][2][128].
+__device__ __forceinline__ size_t box_offset(const Params& p, int b, int g, int page) {
+  return (((size_t)b * p.Hkv + g) * p.max_pages + page) * 2 * kHeadDim;
 }
 
 __device__ __forceinline__ uint2 lds_u2(const void* p) { return *reinterpret_cast<const uint2*>(p); }
@@ -200,16 +208,31 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Inclusive prefix sum over the block (blockDim.x a multiple of 32).  scratch >= 32 ints.
+// Barrier over the NT threads that run a block-wide step: the whole CTA (__syncthreads)
+// or, inside the fused kernel, the consumer warps only (named barrier 1), so that the
+// producer warp keeps running ahead.
+template <int NT, bool kNamed>
+__device__ __forceinline__ void bsync() {
+  if constexpr (kNamed) {
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+  } else {
+    __syncthreads();
+  }
+}
+
+// Inclusive prefix sum over the NT participating threads (NT a multiple of 32, threads
+// 0..NT-1).  scratch >= 32 ints.
+template <int NT, bool kNamed>
 __device__ __forceinline__ int block_incl_scan(int v, int* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  constexpr int nw = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int n = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += n;
   }
   if (lane == 31) scratch[warp] = v;
-  __syncthreads();
+  bsync<NT, kNamed>();
   if (warp == 0) {
     int t = lane < nw ? scratch[lane] : 0;
 #pragma unroll
@@ -219,22 +242,25 @@ __device__ __forceinline__ int block_incl_scan(int v, int* scratch) {
     }
     if (lane < nw) scratch[lane] = t;
   }
-  __syncthreads();
+  bsync<NT, kNamed>();
   const int add = warp > 0 ? scratch[warp - 1] : 0;
-  __syncthreads();
+  bsync<NT, kNamed>();
   return v + add;
 }
 
 // Arrival on a per-(b, g) counter; true in the one CTA that arrives last.  The last CTA
 // sees every write the others made before arriving.
+template <int NT, bool kNamed>
 __device__ __forceinline__ bool arrive_last(unsigned* counter, unsigned target, int* s_flag) {
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) *s_flag = (atomicAdd(counter, 1u) == target - 1u) ? 1 : 0;
-  __syncthreads();
+  bsync<NT, kNamed>();  // every thread's writes happen before thread 0's release
+  if (threadIdx.x == 0) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+    *s_flag = (old == target - 1u) ? 1 : 0;
+  }
+  bsync<NT, kNamed>();  // ... and the last one's acquire happens before every thread's reads
   const bool last = *s_flag != 0;
-  if (last) __threadfence();
-  __syncthreads();
+  bsync<NT, kNamed>();
   return last;
 }
 
@@ -284,41 +310,28 @@ __device__ __forceinline__ float corner_dot(const QueryFrag<G>& f, int j, const 
   return s;
 }
 
-// Scores pages [p0, p0 + n_live) of (b, g) into dst[0 .. n_live).  Half-warp per page,
-// 16 B of the min row and 16 B of the max row per lane, 4 pages in flight per half-warp.
-// bt_s: shared scratch of >= n_live ints.  Called by the whole block.
+// Scores pages [p0, p0 + n_live) of (b, g) into dst[0 .. n_live).  The boxes of those pages
+// are contiguous (logical page order).  Half-warp per page, 16 B of the min row and 16 B of
+// the max row per lane, 4 pages in flight per half-warp.  Called by the whole block.
 template <int G>
-__device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, float* dst,
-                           int* bt_s) {
+__device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, float* dst) {
   const int tid = threadIdx.x, nthr = blockDim.x;
-  const int* bt_row = p.block_table + (size_t)b * p.max_pages + p0;
-  for (int i = tid; i < n_live; i += nthr) bt_s[i] = bt_row[i];
   const int hw = tid >> 4, c = tid & 15, nhw = nthr >> 4;
   QueryFrag<G> f;
   load_query_frag<G>(p, b, g, c, f);
-  __syncthreads();
-  const __half* meta_g = p.meta + (size_t)g * 2 * kHeadDim + 8 * c;
-  const size_t page_stride = (size_t)p.Hkv * 2 * kHeadDim;
+  const __half* box0 = p.meta + box_offset(p, b, g, p0) + 8 * c;
   constexpr int U = 4;
   for (int base = 0; base < n_live; base += U * nhw) {
     uint4 mn[U], mx[U];
-    bool ok[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int r = base + u * nhw + hw;
-      ok[u] = false;
       mn[u] = make_uint4(0, 0, 0, 0);
       mx[u] = make_uint4(0, 0, 0, 0);
       if (r < n_live) {
-        const int phys = bt_s[r];
-        if (phys >= 0 && phys < p.num_phys) {
-          const __half* src = meta_g + (size_t)phys * page_stride;
-          mn[u] = ld_stream_v4(src);
-          mx[u] = ld_stream_v4(src + kHeadDim);
-          ok[u] = true;
-        } else if (c == 0) {
-          report(p, QUEST_ERR_BAD_PAGE, b, p0 + r, kSiteScore);
-        }
+        const __half* src = box0 + (size_t)r * 2 * kHeadDim;
+        mn[u] = ld_stream_v4(src);
+        mx[u] = ld_stream_v4(src + kHeadDim);
       }
     }
 #pragma unroll
@@ -334,61 +347,90 @@ __device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, fl
         best = fmaxf(best, s);
       }
       const int r = base + u * nhw + hw;
-      if (c == 0 && r < n_live) dst[r] = ok[u] ? best : -CUDART_INF_F;
+      if (c == 0 && r < n_live) dst[r] = best;
     }
   }
 }
 
 // ------------------------------------------------------------------------------------
 // top-K: "Guide to Quest", Solution step 3.  Scores become order-preserving unsigned keys
-// (sign flip); an MSB-first radix select (8-bit digits, shared-memory histogram, block
-// scan) finds the K-th largest key; a block scan then compacts, in ascending page order,
-// every key above the threshold and the lowest-indexed keys equal to it.
+// (sign flip).  The keys' actual range [lo, hi] is cut into 2048 equal bins (an 11-bit
+// histogram of (key - lo) >> shift, warp-aggregated shared-memory atomics), a block scan
+// from the top bin finds the bin holding the K-th largest key, and the few keys of that
+// bin are ranked exactly (larger key first, then lower page).  A bin with more than 256
+// keys (many near-equal scores) falls back to an MSB-first radix select on the full keys.
+// A block scan then writes the kept pages in ascending page order.
 // ------------------------------------------------------------------------------------
+constexpr int kTopkBins = 2048;
+constexpr int kTopkCand = 256;
+
 __device__ __forceinline__ uint32_t score_key(float s) {
   const uint32_t u = __float_as_uint(s + 0.0f);  // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// row: N scores (global, may have been written by other CTAs of this grid); writes K
-// entries of idx_out and *count_out.  keys: shared >= N uint32.  Called by the whole block.
-static __device__ void topk_select(const float* row, int N, int K, int* idx_out, int* count_out,
-                            uint32_t* keys, int* hist, int* scratch) {
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  if (N <= K) {
-    for (int r = tid; r < K; r += nthr) idx_out[r] = r < N ? r : -1;
-    if (tid == 0) *count_out = N;
-    return;
-  }
-  for (int i = tid; i < N; i += nthr) keys[i] = score_key(__ldcg(row + i));
+// Shared memory of one selection over a row of up to max_pages scores.
+struct TopkSmem {
+  uint32_t* keys;      // [max_pages]
+  int* hist;           // [kTopkBins]
+  uint32_t* cand_key;  // [kTopkCand]
+  int* cand_idx;       // [kTopkCand]
+  uint32_t* kept;      // [ceil(max_pages / 32)] bitmap of kept keys of the threshold bin
+};
+
+__host__ __device__ inline size_t topk_smem_bytes(int max_pages) {
+  return align_up((size_t)max_pages * 4, 16) + (size_t)kTopkBins * 4 + (size_t)kTopkCand * 8 +
+         align_up((size_t)((max_pages + 31) / 32) * 4, 16);
+}
+
+__device__ inline TopkSmem topk_smem_at(unsigned char* base, int max_pages) {
+  TopkSmem t;
+  t.keys = reinterpret_cast<uint32_t*>(base);
+  base += align_up((size_t)max_pages * 4, 16);
+  t.hist = reinterpret_cast<int*>(base);
+  base += (size_t)kTopkBins * 4;
+  t.cand_key = reinterpret_cast<uint32_t*>(base);
+  base += (size_t)kTopkCand * 4;
+  t.cand_idx = reinterpret_cast<int*>(base);
+  base += (size_t)kTopkCand * 4;
+  t.kept = reinterpret_cast<uint32_t*>(base);
+  return t;
+}
+
+// Exact selection on keys[0..N) by MSB-first radix select (8-bit digits); used when the
+// threshold bin of the fast path holds too many keys.
+template <int NT, bool kNamed>
+__device__ void topk_radix_keys(const uint32_t* keys, int N, int K, int* idx_out, int* count_out,
+                                int* hist, int* scratch) {
+  const int tid = threadIdx.x;
   uint32_t prefix = 0, mask = 0;
   int need = K;
   int* sel = scratch + 40;  // digit, keys above, keys in the digit's bucket
 #pragma unroll 1
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += nthr) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < N; i += nthr) {
+    for (int i = tid; i < 256; i += NT) hist[i] = 0;
+    bsync<NT, kNamed>();
+    for (int i = tid; i < N; i += NT) {
       const uint32_t k = keys[i];
       if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
     }
-    __syncthreads();
+    bsync<NT, kNamed>();
     const int cnt = tid < 256 ? hist[255 - tid] : 0;
-    const int incl = block_incl_scan(cnt, scratch);
+    const int incl = block_incl_scan<NT, kNamed>(cnt, scratch);
     if (tid < 256 && incl >= need && incl - cnt < need) {
       sel[0] = 255 - tid;
       sel[1] = incl - cnt;
       sel[2] = cnt;
     }
-    __syncthreads();
+    bsync<NT, kNamed>();
     const int digit = sel[0], above = sel[1], bucket = sel[2];
     need -= above;
     prefix |= (uint32_t)digit << shift;
     mask |= 0xFFu << shift;
-    __syncthreads();
+    bsync<NT, kNamed>();
     if (bucket == need) break;  // the whole bucket is kept: threshold found
   }
-  const int chunk = (N + nthr - 1) / nthr;
+  const int chunk = (N + NT - 1) / NT;
   const int lo = min(N, tid * chunk), hi = min(N, lo + chunk);
   int ngt = 0, neq = 0;
   for (int i = lo; i < hi; ++i) {
@@ -397,7 +439,7 @@ static __device__ void topk_select(const float* row, int N, int K, int* idx_out,
     neq += m == prefix;
   }
   const int packed = (ngt << 16) | neq;
-  const int excl = block_incl_scan(packed, scratch) - packed;
+  const int excl = block_incl_scan<NT, kNamed>(packed, scratch) - packed;
   int eq_before = excl & 0xFFFF;
   int pos = (excl >> 16) + min(eq_before, need);
   for (int i = lo; i < hi; ++i) {
@@ -408,6 +450,198 @@ static __device__ void topk_select(const float* row, int N, int K, int* idx_out,
       if (eq_before < need) idx_out[pos++] = i;
       ++eq_before;
     }
+  }
+  if (tid == 0) *count_out = K;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Inclusive / exclusive sum over NT threads with warp shuffles and one barrier; tot: shared
+// [NW] ints of the caller's choosing.
+template <int NT, bool kNamed>
+__device__ __forceinline__ int block_excl_sum(int v, int* tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) tot[warp] = x;
+  bsync<NT, kNamed>();
+  int pre = lane < warp ? tot[lane] : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) pre += __shfl_xor_sync(0xffffffffu, pre, o);
+  return pre + x - v;
+}
+
+// row: N scores (global, may have been written by other CTAs of this grid), N <= 64 * NT;
+// writes K entries of idx_out and *count_out.  scratch >= 64 ints.  Called by threads
+// 0..NT-1.  Thread tid owns the contiguous keys [tid * cpt, tid * cpt + cpt).
+template <int NT, bool kNamed>
+__device__ void topk_select(const float* row, int N, int K, int* idx_out, int* count_out,
+                            const TopkSmem& t, int* scratch) {
+  static_assert(NT % 32 == 0 && NT <= 256 && kTopkBins % (4 * NT) == 0, "up to 8 whole warps");
+  constexpr int NW = NT / 32;  // scratch: [0,8) lo, [8,16) hi, [16,24) / [24,32) sums,
+                               // [40,44) threshold
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (N <= K) {
+    for (int r = tid; r < K; r += NT) idx_out[r] = r < N ? r : -1;
+    if (tid == 0) *count_out = N;
+    return;
+  }
+  // 1. keys (coalesced loads, 16 in flight per thread) and their range
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  const int rounds = (N + NT - 1) / NT;
+  for (int r0 = 0; r0 < rounds; r0 += 16) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = (r0 + u) * NT + tid;
+      v[u] = i < N ? __ldcg(row + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = (r0 + u) * NT + tid;
+      if (i < N) {
+        const uint32_t k = score_key(v[u]);
+        t.keys[i] = k;
+        lo = min(lo, k);
+        hi = max(hi, k);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  for (int i = tid; i < kTopkBins / 4; i += NT) reinterpret_cast<int4*>(t.hist)[i] = make_int4(0, 0, 0, 0);
+  for (int i = tid; i < (N + 31) / 32; i += NT) t.kept[i] = 0u;
+  if (lane == 0) {
+    scratch[warp] = (int)lo;
+    scratch[8 + warp] = (int)hi;
+  }
+  if (tid == 0) scratch[43] = 0;
+  bsync<NT, kNamed>();
+  lo = lane < NW ? (uint32_t)scratch[lane] : 0xffffffffu;
+  hi = lane < NW ? (uint32_t)scratch[8 + lane] : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  const uint32_t span = hi - lo;
+  const int shift = span >= (uint32_t)kTopkBins ? (32 - __clz(span)) - 11 : 0;
+  // my contiguous block of keys, 4 at a time
+  const int cpt = (rounds + 3) & ~3;
+  const int i0 = tid * cpt;
+  auto load4 = [&](int i, uint32_t (&k)[4]) {
+    if (i + 3 < N) {
+      const uint4 q = *reinterpret_cast<const uint4*>(t.keys + i);
+      k[0] = q.x; k[1] = q.y; k[2] = q.z; k[3] = q.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) k[u] = i + u < N ? t.keys[i + u] : 0u;
+    }
+  };
+  // 2. histogram of (key - lo) >> shift over 2048 bins
+  for (int j = 0; j < cpt; j += 4) {
+    if (i0 + j >= N) break;
+    uint32_t k[4];
+    load4(i0 + j, k);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + j + u < N) atomicAdd(&t.hist[(k[u] - lo) >> shift], 1);
+  }
+  bsync<NT, kNamed>();
+  // 3. from the top bin down, the bin where the count reaches K; thread tid owns the 8 bins
+  //    [2040 - 8 tid, 2047 - 8 tid]
+  constexpr int kBPT = kTopkBins / NT;
+  const int low = kTopkBins - kBPT * (tid + 1);
+  int h[kBPT];
+#pragma unroll
+  for (int q = 0; q < kBPT / 4; ++q) {
+    const int4 v = reinterpret_cast<const int4*>(t.hist + low)[q];
+    h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
+  }
+  int local = 0;
+#pragma unroll
+  for (int j = 0; j < kBPT; ++j) local += h[j];
+  const int excl = block_excl_sum<NT, kNamed>(local, scratch + 16);
+  if (excl < K && K <= excl + local) {
+    int acc = excl;
+#pragma unroll
+    for (int j = kBPT - 1; j >= 0; --j) {
+      if (acc < K && acc + h[j] >= K) {
+        scratch[40] = low + j;
+        scratch[41] = acc;
+        scratch[42] = h[j];
+      }
+      acc += h[j];
+    }
+  }
+  bsync<NT, kNamed>();
+  const int bstar = scratch[40], above = scratch[41], bucket = scratch[42];
+  const int need = K - above;  // 1 .. bucket
+  if (bucket != need && bucket > kTopkCand) {
+    topk_radix_keys<NT, kNamed>(t.keys, N, K, idx_out, count_out, t.hist, scratch);
+    return;
+  }
+  const bool whole = bucket == need;
+  if (!whole) {
+    // 4. rank the threshold bin's keys exactly: larger key first, then lower page
+    for (int j = 0; j < cpt; j += 4) {
+      if (i0 + j >= N) break;
+      uint32_t k[4];
+      load4(i0 + j, k);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (i0 + j + u < N && (int)((k[u] - lo) >> shift) == bstar) {
+          const int pos = atomicAdd(&scratch[43], 1);
+          t.cand_key[pos] = k[u];
+          t.cand_idx[pos] = i0 + j + u;
+        }
+      }
+    }
+    bsync<NT, kNamed>();
+    for (int j = tid; j < bucket; j += NT) {
+      const uint32_t kj = t.cand_key[j];
+      const int ij = t.cand_idx[j];
+      int r = 0;
+      for (int m = 0; m < bucket; ++m) {
+        const uint32_t km = t.cand_key[m];
+        r += (km > kj) || (km == kj && t.cand_idx[m] < ij);
+      }
+      if (r < need) atomicOr(&t.kept[ij >> 5], 1u << (ij & 31));
+    }
+    bsync<NT, kNamed>();
+  }
+  // 5. compaction in ascending page order: count my kept keys, one block scan, write
+  unsigned long long mine = 0ull;
+  int nsel = 0;
+  for (int j = 0; j < cpt; j += 4) {
+    if (i0 + j >= N) break;
+    uint32_t k[4];
+    load4(i0 + j, k);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + j + u;
+      const int bin = (int)((k[u] - lo) >> shift);
+      const bool sel = i < N && (bin > bstar || (bin == bstar && (whole || ((t.kept[i >> 5] >> (i & 31)) & 1u))));
+      mine |= (unsigned long long)sel << (j + u);
+      nsel += sel;
+    }
+  }
+  int pos = block_excl_sum<NT, kNamed>(nsel, scratch + 24);
+  while (mine) {
+    const int j = __ffsll((long long)mine) - 1;
+    idx_out[pos++] = i0 + j;
+    mine &= mine - 1ull;
   }
   if (tid == 0) *count_out = K;
 }
@@ -680,10 +914,9 @@ __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap&
 }
 
 // Log-sum-exp merge of the first n_live partials of every head of (b, g) into out / lse.
-template <int G>
-__device__ void merge_splits(const Params& p, unsigned char* smem, const SmemMap& m, int b,
-                             int g, int n_live) {
-  float* msc = reinterpret_cast<float*>(smem + m.mscale);  // [G][kMaxSplits + 2]
+// msc: shared [G][kMaxSplits + 2] floats.  Called by threads 0..NT-1.
+template <int G, int NT, bool kNamed>
+__device__ void merge_splits(const Params& p, float* msc, int b, int g, int n_live) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp < G) {
     const int h = g * G + warp;
@@ -705,15 +938,23 @@ __device__ void merge_splits(const Params& p, unsigned char* smem, const SmemMap
       row[kMaxSplits + 1] = Ls;
     }
   }
-  __syncthreads();
-  for (int o = tid; o < G * kHeadDim; o += blockDim.x) {
+  bsync<NT, kNamed>();
+  for (int o = tid; o < G * kHeadDim; o += NT) {
     const int j = o / kHeadDim, i = o % kHeadDim;
     const int h = g * G + j;
     const float* row = msc + j * (kMaxSplits + 2);
     const float Ls = row[kMaxSplits + 1];
     const float* accp = p.part_acc + (size_t)(b * p.Hq + h) * p.n_splits * kHeadDim + i;
     float A = 0.f;
-    for (int s = 0; s < n_live; ++s) {
+    int s = 0;
+    for (; s + 8 <= n_live; s += 8) {  // 8 independent loads in flight
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = row[s + u] != 0.f ? __ldcg(accp + (size_t)(s + u) * kHeadDim) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) A = fmaf(v[u], row[s + u], A);
+    }
+    for (; s < n_live; ++s) {
       const float f = row[s];
       if (f != 0.f) A = fmaf(__ldcg(accp + (size_t)s * kHeadDim), f, A);
     }
@@ -722,7 +963,7 @@ __device__ void merge_splits(const Params& p, unsigned char* smem, const SmemMap
       p.lse[b * p.Hq + h] =
           Ls > 0.f ? (row[kMaxSplits] + log2f(Ls)) * 0.69314718055994531f : -CUDART_INF_F;
   }
-  __syncthreads();
+  bsync<NT, kNamed>();
 }
 
 // Shared prologue of the decode-capable kernels: ring barriers.

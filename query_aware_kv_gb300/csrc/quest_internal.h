@@ -20,6 +20,7 @@ constexpr int kMaxSplits = 256;             // split-K partials per (sequence, q
 constexpr int kDefaultPagesPerSplit = 8;
 constexpr int kDefaultScoreTilePages = 128;
 constexpr long long kDefaultWaitNs = 1000000000LL;
+constexpr int kDefaultDecodeLag = 16;
 
 // Places in the code that record a device fault (third detail word).
 enum FaultSite : int {
@@ -89,6 +90,12 @@ struct Params {
   long long wait_limit_ns;
   int debug_flags;
   float qscale;          // log2(e) / sqrt(128)
+
+  const __half* k_new;   // fused step: token appended per (b, g) before scoring, or null
+  const __half* v_new;
+  int decode_lag;        // fused: (b, g)'s decode items follow the scoring of pair bg + lag
+  unsigned long long* trace;  // fused: optional timeline, trace[0] = records written
+  int trace_capacity;
 };
 
 // Launch with programmatic dependent launch allowed: the kernel may start while the
@@ -111,6 +118,7 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
 
 // Dynamic shared memory of the decode-capable kernels (bytes), see quest_device.cuh.
 size_t decode_smem_bytes(int G, int P, int topk_keys, int score_tile_pages);
+size_t fused_smem_bytes(int G, int P, int max_pages);
 // Raise a kernel's dynamic shared-memory cap (once per device and kernel).
 cudaError_t ensure_smem(const void* fn, size_t bytes);
 

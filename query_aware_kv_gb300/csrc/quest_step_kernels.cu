@@ -28,10 +28,9 @@ cudaError_t ensure_smem(const void* fn, size_t bytes) {
 }
 
 // ---------------------------------------------------------------- scoring
-// grid (n_score_tiles, B*Hkv), 256 threads; dynamic smem: the tile's block-table slice.
+// grid (n_score_tiles, B*Hkv), 256 threads.
 template <int G>
 __global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
-  extern __shared__ __align__(16) int bt_s[];
   pdl_wait();
   const int tile = blockIdx.x, bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
@@ -42,7 +41,7 @@ __global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
   const int n_live = max(0, min(N - p0, np));
   float* row = p.scores + (size_t)bg * p.max_pages + p0;
   for (int i = n_live + (int)threadIdx.x; i < np; i += blockDim.x) row[i] = -CUDART_INF_F;
-  if (n_live > 0) score_tile<G>(p, b, g, p0, n_live, row, bt_s);
+  if (n_live > 0) score_tile<G>(p, b, g, p0, n_live, row);
 }
 
 // ---------------------------------------------------------------- top-K
@@ -53,11 +52,10 @@ __global__ void __launch_bounds__(kConsumerThreads) topk_kernel(Params p) {
   const int bg = blockIdx.x, b = bg / p.Hkv;
   const int L = load_len(p, b, kSiteTopk);
   const int N = (L + p.P - 1) / p.P;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(sm);
-  int* hist = reinterpret_cast<int*>(sm + align_up((size_t)p.max_pages * 4, 16));
-  int* scratch = hist + 256;
-  topk_select(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
-              p.sel_idx + (size_t)bg * p.top_k, p.sel_count + bg, keys, hist, scratch);
+  int* scratch = reinterpret_cast<int*>(sm + topk_smem_bytes(p.max_pages));
+  topk_select<kConsumerThreads, false>(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
+                                       p.sel_idx + (size_t)bg * p.top_k, p.sel_count + bg,
+                                       topk_smem_at(sm, p.max_pages), scratch);
 }
 
 // ---------------------------------------------------------------- decode
@@ -89,8 +87,9 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Params p) {
   const int n_tile = max(0, min(count - r0, p.pps));
   if (n_tile > 0) decode_tile<G, P>(p, smem, m, b, g, split, r0, n_tile, L, N, sel_row, 0u);
   int* misc = reinterpret_cast<int*>(smem + m.misc);
-  if (arrive_last(&p.decode_arrive[bg], (unsigned)p.n_splits, misc)) {
-    merge_splits<G>(p, smem, m, b, g, (count + p.pps - 1) / p.pps);
+  if (arrive_last<kDecodeThreads, false>(&p.decode_arrive[bg], (unsigned)p.n_splits, misc)) {
+    merge_splits<G, kDecodeThreads, false>(p, reinterpret_cast<float*>(smem + m.mscale), b, g,
+                                           (count + p.pps - 1) / p.pps);
     if (threadIdx.x == 0) p.decode_arrive[bg] = 0u;
   }
 }
@@ -129,9 +128,7 @@ static const void* pick_decode(int G, int P) {
 
 cudaError_t launch_estimate(const Params& p, int G, cudaStream_t s) {
   const void* fn = pick_estimate(G);
-  const size_t smem = align_up((size_t)p.score_tile_pages * 4, 16);
-  cudaError_t e = ensure_smem(fn, smem);
-  if (e != cudaSuccess) return e;
+  const size_t smem = 0;
   Params pp = p;
   void* args[] = {&pp};
   return launch_pdl(fn, dim3(p.n_score_tiles, p.B * p.Hkv), dim3(kConsumerThreads), smem, s,
@@ -140,7 +137,7 @@ cudaError_t launch_estimate(const Params& p, int G, cudaStream_t s) {
 
 cudaError_t launch_topk(const Params& p, cudaStream_t s) {
   const void* fn = (const void*)topk_kernel;
-  const size_t smem = align_up((size_t)p.max_pages * 4, 16) + (256 + 64) * 4;
+  const size_t smem = topk_smem_bytes(p.max_pages) + 64 * 4;
   cudaError_t e = ensure_smem(fn, smem);
   if (e != cudaSuccess) return e;
   Params pp = p;

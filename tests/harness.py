@@ -69,10 +69,13 @@ def valid_pages(ref: oracle.Cache):
 
 
 def assert_meta_equal(pair: Pair) -> None:
+    """GPU machines [B][Hkv][max_pages][2][d] (logical order) vs the oracle's boxes
+    [num_phys][Hkv][2][d] (physical order), bit-exact for every existing page."""
     gpu = pair.cache.meta.cpu().numpy()
     ref16 = pair.ref.meta.astype(np.float16)
-    phys = sorted({ph for _, _, ph in valid_pages(pair.ref)})
-    np.testing.assert_array_equal(gpu[phys].view(np.uint16), ref16[phys].view(np.uint16))
+    for b, p, ph in valid_pages(pair.ref):
+        np.testing.assert_array_equal(gpu[b, :, p].view(np.uint16), ref16[ph].view(np.uint16),
+                                      err_msg=f"box of sequence {b} page {p}")
 
 
 def score_tolerance(ref: oracle.Cache, qh: np.ndarray) -> np.ndarray:
@@ -139,19 +142,28 @@ def oracle_selection_arrays(gpu_idx: np.ndarray, gpu_cnt: np.ndarray):
 
 
 def run_step_and_compare(pair: Pair, step: int, top_k: int, opts=None, fused: bool = True,
-                         check_needles: bool = False) -> int:
+                         check_needles: bool = False, one_launch: bool = False,
+                         check_cache: bool = False) -> int:
     """One decode step on both sides (append + score + select + attend); compares
-    boxes of the touched page, scores (unfused only), selection and attention."""
+    scores (unfused only), selection and attention; with check_cache also the boxes,
+    pools and lengths.  one_launch: quest_decode_step (append folded into the fused
+    kernel) instead of quest_append + quest_decode."""
     w = pair.w
     qd = w.q[step].to("cuda").contiguous()
     kn = w.k_new[step].to("cuda").contiguous()
     vn = w.v_new[step].to("cuda").contiguous()
-    q.append(pair.cache, kn, vn, pair.ws)
+    if not one_launch:
+        q.append(pair.cache, kn, vn, pair.ws)
     oracle.append(pair.ref, w.k_new[step].cpu().numpy(), w.v_new[step].cpu().numpy())
     qh = w.q[step].cpu().numpy().astype(np.float32)
     ref_scores = oracle.score(pair.ref, qh)
     ref_idx, ref_cnt = oracle.topk(pair.ref, ref_scores, top_k)
-    if fused:
+    if one_launch:
+        idx = torch.empty((w.batch, w.num_kv_heads, top_k), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((w.batch, w.num_kv_heads), dtype=torch.int32, device="cuda")
+        out, lse = q.decode_step(pair.cache, qd, kn, vn, top_k, pair.ws, opts, idx_out=idx,
+                                 count_out=cnt)
+    elif fused:
         idx = torch.empty((w.batch, w.num_kv_heads, top_k), dtype=torch.int32, device="cuda")
         cnt = torch.empty((w.batch, w.num_kv_heads), dtype=torch.int32, device="cuda")
         out, lse = q.decode(pair.cache, qd, top_k, pair.ws, opts, idx_out=idx, count_out=cnt)
@@ -169,4 +181,13 @@ def run_step_and_compare(pair: Pair, step: int, top_k: int, opts=None, fused: bo
     if check_needles:
         for (b, g, p, slot) in w.needles:
             assert p in gi[b, g, :gc[b, g]].tolist(), ("needle page not selected", b, g, p)
+    if check_cache:
+        assert_meta_equal(pair)
+        kp = pair.cache.k_pool.cpu().numpy()
+        vp = pair.cache.v_pool.cpu().numpy()
+        P = w.page_size
+        for b, p, ph in valid_pages(pair.ref):
+            n = min(P, int(pair.ref.seq_lens[b]) - p * P)
+            np.testing.assert_array_equal(kp[ph, :, :n].astype(np.float32), pair.ref.k_pool[ph, :, :n])
+            np.testing.assert_array_equal(vp[ph, :, :n].astype(np.float32), pair.ref.v_pool[ph, :, :n])
     return swapped

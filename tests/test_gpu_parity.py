@@ -152,10 +152,59 @@ def test_decode_steps_match_oracle(geom, fused):
         H.run_step_and_compare(pair, t, w.top_k, fused=fused)
 
 
+@pytest.mark.parametrize("geom", GEOMS, ids=lambda g: f"hq{g['hq']}_hkv{g['hkv']}_p{g['P']}")
+def test_one_launch_step_matches_oracle(geom):
+    """quest_decode_step: append folded into the fused kernel; boxes, pools, lengths,
+    selection and attention all match the oracle step after step (pages open and fill)."""
+    w = small(lens=(1500, 1, 333, 0, 16 * 30 - 2), batch=5, steps=20, outliers=4, **geom)
+    pair = H.on_device(w)
+    for t in range(w.steps):
+        H.run_step_and_compare(pair, t, w.top_k, one_launch=True, check_cache=(t % 5 == 4))
+
+
 def test_tiny_config():
     w = wl.tiny(seed=0)
     pair = H.on_device(w)
-    H.run_step_and_compare(pair, 0, w.top_k)
+    H.run_step_and_compare(pair, 0, w.top_k, one_launch=True, check_cache=True)
+
+
+def test_fused_queue_orders_agree():
+    """Any decode_lag (queue interleaving) and CTA count gives the same selection and the
+    same outputs up to split-merge rounding."""
+    w = small(lens=(4000, 2100, 5000), batch=3, hq=8, hkv=4, budget=512, outliers=4)
+    pair = H.on_device(w)
+    qd = w.q[0].cuda()
+    idx0 = torch.empty((3, 4, w.top_k), dtype=torch.int32, device="cuda")
+    cnt0 = torch.empty((3, 4), dtype=torch.int32, device="cuda")
+    base, base_lse = q.decode(pair.cache, qd, w.top_k, pair.ws, idx_out=idx0, count_out=cnt0)
+    for lag, ctas in [(1, 0), (2, 1), (3, 7), (100, 0), (5, 300)]:
+        idx = torch.empty_like(idx0)
+        cnt = torch.empty_like(cnt0)
+        out, lse = q.decode(pair.cache, qd, w.top_k, pair.ws, q.opts(decode_lag=lag, max_ctas=ctas),
+                            idx_out=idx, count_out=cnt)
+        assert torch.equal(idx, idx0) and torch.equal(cnt, cnt0)
+        assert torch.equal(out, base) and torch.equal(lse, base_lse)
+    H.assert_status_ok(pair.ws)
+
+
+def test_trace_records_a_timeline():
+    w = small(lens=(3000, 700), batch=2, budget=256)
+    pair = H.on_device(w)
+    cap = 4096
+    tr = torch.zeros(1 + 2 * cap, dtype=torch.int64, device="cuda")
+    q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws, q.opts(trace=tr))
+    H.assert_status_ok(pair.ws)
+    n = int(tr[0])
+    assert 0 < n <= cap
+    rec = tr[1:1 + 2 * n].view(n, 2).cpu().numpy()
+    t, info = rec[:, 0], rec[:, 1].astype(np.uint64)
+    ev = (info >> np.uint64(24)) & np.uint64(0xff)
+    kinds = set(int(e) for e in ev)
+    assert {1, 2, 3, 6, 7, 8, 9, 10, 11} <= kinds
+    # one top-K and one merge per (b, g)
+    assert int((ev == 9).sum()) == w.batch * w.num_kv_heads
+    assert int((ev == 11).sum()) == w.batch * w.num_kv_heads
+    assert (t.max() - t.min()) < 1e9
 
 
 def test_fused_equals_chain_bitwise():
@@ -197,6 +246,11 @@ def test_workspace_reuse_many_calls():
     # the header counters are back to zero, the epoch counts the launches
     hdr = pair.ws[:32].view(torch.int32).cpu().tolist()
     assert hdr[4] == 0 and hdr[5] == 0 and hdr[6] == 51
+    # so does the one-launch step
+    for t in range(w.steps):
+        H.run_step_and_compare(pair, t, w.top_k, one_launch=True)
+    hdr = pair.ws[:32].view(torch.int32).cpu().tolist()
+    assert hdr[4] == 0 and hdr[5] == 0 and hdr[6] == 51 + w.steps
 
 
 def test_planted_needles_selected_on_gpu():
@@ -227,7 +281,8 @@ def test_empty_and_single_token_sequences():
 # record a status); nothing here faults, traps or hangs the GPU.
 
 def test_bad_block_table_entry_is_reported():
-    w = small(lens=(300, 200), batch=2)
+    # sequence 1 has 7 pages and top-K keeps 8, so every page (and the bad entry) is read
+    w = small(lens=(300, 100), batch=2)
     bt = w.block_table.clone()
     bt[1, 3] = w.num_phys + 5          # out of the pool
     w.block_table = bt
