@@ -107,16 +107,26 @@ typedef struct quest_opts {
                                  scoring items of the next decode_lag (b, g) pairs
                                  (<= 0: default 16)                                         */
     int32_t trace_capacity;   /* fused kernel: records `trace` can hold                   */
-    uint64_t* trace;          /* fused kernel: optional device timeline, NULL = off.
-                                 trace[0] counts records (zero it before the call); record i
-                                 is trace[1 + 2i] = %globaltimer ns, trace[2 + 2i] =
-                                 smid << 48 | cta << 32 | event << 24 | item              */
+    uint64_t* trace;          /* fused kernel: optional device timeline, NULL = off; zero
+                                 it before the call.  Record i is trace[1 + 2i] =
+                                 %globaltimer ns, trace[2 + 2i] = smid << 48 | cta << 32 |
+                                 event << 24 | item; unused records stay 0.  The cluster
+                                 kernel gives CTA c records [64c, 64c + 64); the queue
+                                 kernel appends and counts them in trace[0].              */
+    int32_t cluster_size;     /* fused kernel: CTAs per (sequence, kv head) cluster, 1..16;
+                                 0: the largest size at which every pair's cluster is
+                                 resident at once (1 when there are more pairs than SMs can
+                                 hold)                                                      */
+    int32_t pad_;
 } quest_opts_t;
 
 /* quest_decode only: never publish the selection, so that every decode work item's
  * bounded wait runs out and the call reports QUEST_ERR_TIMEOUT.  For testing the
  * timeout path; outputs are then unspecified. */
 #define QUEST_DEBUG_WITHHOLD_SELECTION 1
+/* quest_decode / quest_decode_step: run the work-queue variant of the fused kernel
+ * (one persistent grid, global arrival counters) instead of the cluster variant. */
+#define QUEST_DEBUG_QUEUE_KERNEL 2
 
 /* Bytes of workspace the calls below need for this cache, top_k and opts; 0 if the
  * arguments are invalid (see quest_last_error). */

@@ -31,6 +31,7 @@ QUEST_ERR_BAD_LENGTH = 7
 QUEST_ERR_BAD_SELECTION = 8
 QUEST_MAX_PAGES = 16384
 QUEST_DEBUG_WITHHOLD_SELECTION = 1
+QUEST_DEBUG_QUEUE_KERNEL = 2
 HEAD_DIM = 128
 
 # Every symbol include/quest.h declares.
@@ -65,6 +66,7 @@ class QuestOpts(ctypes.Structure):
         ("max_ctas", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
         ("wait_limit_ns", ctypes.c_int64), ("decode_lag", ctypes.c_int32),
         ("trace_capacity", ctypes.c_int32), ("trace", ctypes.c_void_p),
+        ("cluster_size", ctypes.c_int32), ("pad_", ctypes.c_int32),
     ]
 
 
@@ -140,7 +142,7 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
 
 def opts(pages_per_split: int = 0, score_tile_pages: int = 0, max_ctas: int = 0,
          debug_flags: int = 0, wait_limit_ns: int = 0, decode_lag: int = 0,
-         trace: Optional[torch.Tensor] = None) -> QuestOpts:
+         trace: Optional[torch.Tensor] = None, cluster_size: int = 0) -> QuestOpts:
     """Launch tuning (0 = default).  ``trace``: int64 CUDA tensor of 1 + 2n elements whose
     first element is zero; receives up to n timeline records of the fused kernel."""
     cap, ptr = 0, None
@@ -148,7 +150,7 @@ def opts(pages_per_split: int = 0, score_tile_pages: int = 0, max_ctas: int = 0,
         _need(trace, "trace", torch.int64)
         cap, ptr = (trace.numel() - 1) // 2, trace.data_ptr()
     o = QuestOpts(pages_per_split, score_tile_pages, max_ctas, debug_flags, wait_limit_ns,
-                  decode_lag, cap, ptr)
+                  decode_lag, cap, ptr, cluster_size, 0)
     o._trace_ref = trace  # keep the buffer alive with the options
     return o
 

@@ -328,11 +328,31 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   p.decode_lag = (opts && opts->decode_lag > 0) ? opts->decode_lag : kDefaultDecodeLag;
   p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
   p.trace_capacity = opts ? opts->trace_capacity : 0;
-  const long long items = (long long)cache->batch * cache->num_kv_heads *
-                          ((long long)t.n_score_tiles + t.n_splits_sparse);
-  if (items > 0x7fffffffLL) return fail(QUEST_ERR_UNSUPPORTED, "too many work items");
-  return launched(launch_fused(p, group_of(cache), opts ? opts->max_ctas : 0,
-                               static_cast<cudaStream_t>(stream)),
+  if (opts && (opts->debug_flags & QUEST_DEBUG_QUEUE_KERNEL)) {
+    const long long items = (long long)cache->batch * cache->num_kv_heads *
+                            ((long long)t.n_score_tiles + t.n_splits_sparse);
+    if (items > 0x7fffffffLL) return fail(QUEST_ERR_UNSUPPORTED, "too many work items");
+    return launched(launch_fused(p, group_of(cache), opts ? opts->max_ctas : 0,
+                                 static_cast<cudaStream_t>(stream)),
+                    what);
+  }
+  const int cs = opts ? opts->cluster_size : 0;  // 0: the library picks
+  if (cs < 0 || cs > kMaxClusterSize)
+    return fail(QUEST_ERR_INVALID_ARG, "cluster_size %d: use 0 (automatic) or 1..%d", cs,
+                kMaxClusterSize);
+  if (cluster_smem_bytes(group_of(cache), cache->page_size, cache->max_pages, cs > 0 ? cs : 1,
+                         top_k) > 227 * 1024)
+    return fail(QUEST_ERR_UNSUPPORTED, "max_pages %d needs more shared memory than a CTA has",
+                cache->max_pages);
+  if (cs > 0 &&
+      cluster_smem_bytes(group_of(cache), cache->page_size, cache->max_pages, cs, top_k) >
+          227 * 1024)
+    return fail(QUEST_ERR_UNSUPPORTED, "cluster_size %d needs more shared memory than a CTA has",
+                cs);
+  p.sel_idx = idx_out;     // the cluster kernel writes the selection only when asked
+  p.sel_count = count_out;
+  return launched(launch_cluster(p, group_of(cache), cs, opts ? opts->max_ctas : 0,
+                                 static_cast<cudaStream_t>(stream)),
                   what);
 }
 

@@ -479,42 +479,18 @@ __device__ __forceinline__ int block_excl_sum(int v, int* tot) {
   return pre + x - v;
 }
 
-// row: N scores (global, may have been written by other CTAs of this grid), N <= 64 * NT;
-// writes K entries of idx_out and *count_out.  scratch >= 64 ints.  Called by threads
-// 0..NT-1.  Thread tid owns the contiguous keys [tid * cpt, tid * cpt + cpt).
+// Selection over keys already in t.keys[0..N) (N > K, N <= 64 * NT); lo / hi: this
+// thread's min / max over the keys it stored.  Writes K entries of idx_out (ascending) and
+// *count_out.  scratch >= 64 ints.  Called by threads 0..NT-1.  After the range is known,
+// thread tid owns the contiguous keys [tid * cpt, tid * cpt + cpt).
 template <int NT, bool kNamed>
-__device__ void topk_select(const float* row, int N, int K, int* idx_out, int* count_out,
-                            const TopkSmem& t, int* scratch) {
+__device__ void topk_core(int N, int K, int* idx_out, int* count_out, const TopkSmem& t,
+                          int* scratch, uint32_t lo, uint32_t hi) {
   static_assert(NT % 32 == 0 && NT <= 256 && kTopkBins % (4 * NT) == 0, "up to 8 whole warps");
   constexpr int NW = NT / 32;  // scratch: [0,8) lo, [8,16) hi, [16,24) / [24,32) sums,
                                // [40,44) threshold
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (N <= K) {
-    for (int r = tid; r < K; r += NT) idx_out[r] = r < N ? r : -1;
-    if (tid == 0) *count_out = N;
-    return;
-  }
-  // 1. keys (coalesced loads, 16 in flight per thread) and their range
-  uint32_t lo = 0xffffffffu, hi = 0u;
   const int rounds = (N + NT - 1) / NT;
-  for (int r0 = 0; r0 < rounds; r0 += 16) {
-    float v[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int i = (r0 + u) * NT + tid;
-      v[u] = i < N ? __ldcg(row + i) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int i = (r0 + u) * NT + tid;
-      if (i < N) {
-        const uint32_t k = score_key(v[u]);
-        t.keys[i] = k;
-        lo = min(lo, k);
-        hi = max(hi, k);
-      }
-    }
-  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
@@ -644,6 +620,40 @@ __device__ void topk_select(const float* row, int N, int K, int* idx_out, int* c
     mine &= mine - 1ull;
   }
   if (tid == 0) *count_out = K;
+}
+
+// row: N scores in global memory (possibly written by other CTAs of this grid), N <= 64 NT.
+template <int NT, bool kNamed>
+__device__ void topk_select(const float* row, int N, int K, int* idx_out, int* count_out,
+                            const TopkSmem& t, int* scratch) {
+  const int tid = threadIdx.x;
+  if (N <= K) {
+    for (int r = tid; r < K; r += NT) idx_out[r] = r < N ? r : -1;
+    if (tid == 0) *count_out = N;
+    return;
+  }
+  // keys (coalesced loads, 16 in flight per thread) and this thread's range
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  const int rounds = (N + NT - 1) / NT;
+  for (int r0 = 0; r0 < rounds; r0 += 16) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = (r0 + u) * NT + tid;
+      v[u] = i < N ? __ldcg(row + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = (r0 + u) * NT + tid;
+      if (i < N) {
+        const uint32_t k = score_key(v[u]);
+        t.keys[i] = k;
+        lo = min(lo, k);
+        hi = max(hi, k);
+      }
+    }
+  }
+  topk_core<NT, kNamed>(N, K, idx_out, count_out, t, scratch, lo, hi);
 }
 
 // ------------------------------------------------------------------------------------
