@@ -114,9 +114,9 @@ typedef struct quest_opts {
                                  kernel gives CTA c records [64c, 64c + 64); the queue
                                  kernel appends and counts them in trace[0].              */
     int32_t cluster_size;     /* fused kernel: CTAs per (sequence, kv head) cluster, 1..16;
-                                 0: the largest size at which every pair's cluster is
-                                 resident at once (1 when there are more pairs than SMs can
-                                 hold)                                                      */
+                                 0: the largest size up to 8 at which every pair's cluster
+                                 is resident at once (1 when there are more pairs than SMs
+                                 can hold)                                                  */
     int32_t pad_;
 } quest_opts_t;
 

@@ -340,13 +340,12 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   if (cs < 0 || cs > kMaxClusterSize)
     return fail(QUEST_ERR_INVALID_ARG, "cluster_size %d: use 0 (automatic) or 1..%d", cs,
                 kMaxClusterSize);
-  if (cluster_smem_bytes(group_of(cache), cache->page_size, cache->max_pages, cs > 0 ? cs : 1,
-                         top_k) > 227 * 1024)
+  if (!cluster_any_fits(group_of(cache), cache->page_size, cache->max_pages, top_k))
     return fail(QUEST_ERR_UNSUPPORTED, "max_pages %d needs more shared memory than a CTA has",
                 cache->max_pages);
   if (cs > 0 &&
       cluster_smem_bytes(group_of(cache), cache->page_size, cache->max_pages, cs, top_k) >
-          227 * 1024)
+          kMaxSmem)
     return fail(QUEST_ERR_UNSUPPORTED, "cluster_size %d needs more shared memory than a CTA has",
                 cs);
   p.sel_idx = idx_out;     // the cluster kernel writes the selection only when asked

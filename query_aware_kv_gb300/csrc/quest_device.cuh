@@ -372,14 +372,14 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 // Shared memory of one selection over a row of up to max_pages scores.
 struct TopkSmem {
   uint32_t* keys;      // [max_pages]
-  int* hist;           // [kTopkBins]
+  int* hist;           // [2 * kTopkBins]
   uint32_t* cand_key;  // [kTopkCand]
   int* cand_idx;       // [kTopkCand]
   uint32_t* kept;      // [ceil(max_pages / 32)] bitmap of kept keys of the threshold bin
 };
 
 __host__ __device__ inline size_t topk_smem_bytes(int max_pages) {
-  return align_up((size_t)max_pages * 4, 16) + (size_t)kTopkBins * 4 + (size_t)kTopkCand * 8 +
+  return align_up((size_t)max_pages * 4, 16) + (size_t)2 * kTopkBins * 4 + (size_t)kTopkCand * 8 +
          align_up((size_t)((max_pages + 31) / 32) * 4, 16);
 }
 
@@ -388,7 +388,7 @@ __device__ inline TopkSmem topk_smem_at(unsigned char* base, int max_pages) {
   t.keys = reinterpret_cast<uint32_t*>(base);
   base += align_up((size_t)max_pages * 4, 16);
   t.hist = reinterpret_cast<int*>(base);
-  base += (size_t)kTopkBins * 4;
+  base += (size_t)2 * kTopkBins * 4;
   t.cand_key = reinterpret_cast<uint32_t*>(base);
   base += (size_t)kTopkCand * 4;
   t.cand_idx = reinterpret_cast<int*>(base);
@@ -622,6 +622,218 @@ __device__ void topk_core(int N, int K, int* idx_out, int* count_out, const Topk
   if (tid == 0) *count_out = K;
 }
 
+// ------------------------------------------------------------------------------------
+// Register-resident selection for N <= KPT * NT keys (thread tid holds keys tid + r * NT,
+// r < KPT; key 0 marks "no key").  The same steps as topk_core, arranged as short
+// independent phases: one pass of shared-memory reductions into a 2048-bin histogram of
+// (key - lo) >> shift, a block scan for the threshold bin, a second 2048-bin histogram
+// inside that bin when it is not decided, then the kept keys are written in ascending
+// index order from warp ballots and one scan of the per-(round, warp) counts.  Keys equal
+// to the threshold key keep the lowest indices.  When the second level still leaves
+// distinct keys in one sub-bin (spans above 2^22 with near-equal keys), the keys go to
+// `spill` and the radix select decides.
+// hist: 2 * kTopkBins ints, zero on entry (left dirty); scratch >= 64 + KPT * NT / 32 ints;
+// spill: N words of shared memory (used only by the radix fallback).
+// ------------------------------------------------------------------------------------
+template <int NT, bool kNamed>
+__device__ __forceinline__ void topk_find_bin(const int* hist, int need, int* out3, int* sums) {
+  constexpr int kBPT = kTopkBins / NT;
+  const int tid = threadIdx.x;
+  const int low = kTopkBins - kBPT * (tid + 1);
+  int h[kBPT];
+#pragma unroll
+  for (int q = 0; q < kBPT / 4; ++q) {
+    const int4 v = reinterpret_cast<const int4*>(hist + low)[q];
+    h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
+  }
+  int local = 0;
+#pragma unroll
+  for (int j = 0; j < kBPT; ++j) local += h[j];
+  const int excl = block_excl_sum<NT, kNamed>(local, sums);
+  if (excl < need && need <= excl + local) {
+    int acc = excl;
+#pragma unroll
+    for (int j = kBPT - 1; j >= 0; --j) {
+      if (acc < need && acc + h[j] >= need) {
+        out3[0] = low + j;
+        out3[1] = acc;
+        out3[2] = h[j];
+      }
+      acc += h[j];
+    }
+  }
+  bsync<NT, kNamed>();
+}
+
+template <int NT, int KPT, bool kNamed>
+__device__ void topk_regs(const uint32_t (&k)[KPT], int N, int K, uint32_t lo, uint32_t hi,
+                          int* idx_out, int* count_out, int* hist, int* scratch,
+                          uint32_t* spill) {
+  static_assert(NT % 32 == 0 && NT <= 256 && kTopkBins % (4 * NT) == 0, "up to 8 whole warps");
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* hist2 = hist + kTopkBins;
+  int* cnt = scratch + 64;  // [KPT][NW] packed (definite << 16 | tie) counts, then prefixes
+  const uint32_t span = hi - lo;
+  const int shift1 = span >= (uint32_t)kTopkBins ? (32 - __clz(span)) - 11 : 0;
+  // 1. level-1 histogram
+#pragma unroll
+  for (int r = 0; r < KPT; ++r)
+    if (r * NT + tid < N) atomicAdd(&hist[(k[r] - lo) >> shift1], 1);
+  bsync<NT, kNamed>();
+  topk_find_bin<NT, kNamed>(hist, K, scratch + 40, scratch + 16);
+  const int bstar = scratch[40], above = scratch[41], bucket = scratch[42];
+  const int need = K - above;  // 1 .. bucket
+  const bool whole1 = bucket == need;
+  const bool exact1 = shift1 == 0;
+  // 2. inside the threshold bin, if it is not decided
+  const int shift2 = shift1 > 11 ? shift1 - 11 : 0;
+  const uint32_t mask1 = shift1 >= 32 ? 0xffffffffu : ((1u << shift1) - 1u);
+  int b2star = 0, need_t = need;
+  bool whole2 = true;
+  if (!whole1 && !exact1) {
+#pragma unroll
+    for (int r = 0; r < KPT; ++r) {
+      const uint32_t d = k[r] - lo;
+      if (r * NT + tid < N && (int)(d >> shift1) == bstar)
+        atomicAdd(&hist2[(d & mask1) >> shift2], 1);
+    }
+    bsync<NT, kNamed>();
+    topk_find_bin<NT, kNamed>(hist2, need, scratch + 44, scratch + 24);
+    b2star = scratch[44];
+    need_t = need - scratch[45];
+    whole2 = scratch[46] == need_t;
+    if (!whole2 && shift2 != 0) {
+      // distinct keys share the deciding sub-bin: exact radix select over all keys
+#pragma unroll
+      for (int r = 0; r < KPT; ++r)
+        if (r * NT + tid < N) spill[r * NT + tid] = k[r];
+      bsync<NT, kNamed>();
+      topk_radix_keys<NT, kNamed>(spill, N, K, idx_out, count_out, hist, scratch);
+      return;
+    }
+  }
+  // 3. classify: definite keep, or a key equal to the threshold key (keep the lowest
+  //    indices); predicates first, then the ballots, then one count store per lane
+  bool def[KPT], tie[KPT];
+#pragma unroll
+  for (int r = 0; r < KPT; ++r) {
+    const uint32_t d = k[r] - lo;
+    const int b1 = (int)(d >> shift1);
+    const int b2 = (int)((d & mask1) >> shift2);
+    const bool valid = r * NT + tid < N;
+    const bool in_bin = valid && b1 == bstar;
+    const bool refine = !whole1 && !exact1;
+    def[r] = valid && (b1 > bstar || (in_bin && (whole1 || (refine && (b2 > b2star || (b2 == b2star && whole2))))));
+    tie[r] = in_bin && !whole1 && (exact1 || (b2 == b2star && !whole2));
+  }
+  unsigned bd[KPT], bt[KPT];
+#pragma unroll
+  for (int r = 0; r < KPT; ++r) bd[r] = __ballot_sync(0xffffffffu, def[r]);
+#pragma unroll
+  for (int r = 0; r < KPT; ++r) bt[r] = __ballot_sync(0xffffffffu, tie[r]);
+  int mine = 0;
+#pragma unroll
+  for (int r = 0; r < KPT; ++r)
+    if (lane == r) mine = (__popc(bd[r]) << 16) | __popc(bt[r]);
+  if (lane < KPT) cnt[lane * NW + warp] = mine;
+  bsync<NT, kNamed>();
+  // 4. exclusive prefix of the (round, warp) counts in index order, by warp 0
+  if (warp == 0) {
+    constexpr int E = KPT * NW;
+    constexpr int EPL = (E + 31) / 32;
+    int v[EPL];
+    int run = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const int i = lane * EPL + e;
+      v[e] = i < E ? cnt[i] : 0;
+      run += v[e];
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int pre = incl - run;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const int i = lane * EPL + e;
+      if (i < E) cnt[i] = pre;
+      pre += v[e];
+    }
+  }
+  bsync<NT, kNamed>();
+  // 5. write the kept indices in ascending order (every count read before any write)
+  const unsigned lt = lanemask_lt();
+  int pre[KPT];
+#pragma unroll
+  for (int r = 0; r < KPT; ++r) pre[r] = cnt[r * NW + warp];
+#pragma unroll
+  for (int r = 0; r < KPT; ++r) {
+    const int d_before = (pre[r] >> 16) + __popc(bd[r] & lt);
+    const int t_before = (pre[r] & 0xffff) + __popc(bt[r] & lt);
+    const int i = r * NT + tid;
+    if ((bd[r] >> lane) & 1u)
+      idx_out[d_before + min(t_before, need_t)] = i;
+    else if (((bt[r] >> lane) & 1u) && t_before < need_t)
+      idx_out[d_before + t_before] = i;
+  }
+  if (tid == 0) *count_out = K;
+}
+
+// One score row in global memory, N <= KPT * NT: keys straight into registers, then
+// topk_regs.  scratch >= 64 + KPT * NT / 32 ints.
+template <int NT, int KPT, bool kNamed>
+__device__ void topk_row_regs(const float* row, int N, int K, int* idx_out, int* count_out,
+                              const TopkSmem& t, int* scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = NT / 32;
+  uint32_t k[KPT];
+  float v[KPT];
+#pragma unroll
+  for (int r = 0; r < KPT; ++r) {
+    const int i = r * NT + tid;
+    v[r] = i < N ? __ldcg(row + i) : 0.f;
+  }
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+  for (int r = 0; r < KPT; ++r) {
+    k[r] = score_key(v[r]);
+    if (r * NT + tid < N) {
+      lo = min(lo, k[r]);
+      hi = max(hi, k[r]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) {
+    scratch[warp] = (int)lo;
+    scratch[8 + warp] = (int)hi;
+  }
+  for (int i = tid; i < 2 * kTopkBins / 4; i += NT)
+    reinterpret_cast<int4*>(t.hist)[i] = make_int4(0, 0, 0, 0);
+  bsync<NT, kNamed>();
+  lo = 0xffffffffu;
+  hi = 0u;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    lo = min(lo, (uint32_t)scratch[w]);
+    hi = max(hi, (uint32_t)scratch[8 + w]);
+  }
+  topk_regs<NT, KPT, kNamed>(k, N, K, lo, hi, idx_out, count_out, t.hist, scratch, t.keys);
+}
+
+// One score row in global memory: register-resident selection up to 16 * NT keys, the
+// shared-memory one above.
+template <int NT, bool kNamed>
+__device__ void topk_row(const float* row, int N, int K, int* idx_out, int* count_out,
+                         const TopkSmem& t, int* scratch);
+
 // row: N scores in global memory (possibly written by other CTAs of this grid), N <= 64 NT.
 template <int NT, bool kNamed>
 __device__ void topk_select(const float* row, int N, int K, int* idx_out, int* count_out,
@@ -654,6 +866,25 @@ __device__ void topk_select(const float* row, int N, int K, int* idx_out, int* c
     }
   }
   topk_core<NT, kNamed>(N, K, idx_out, count_out, t, scratch, lo, hi);
+}
+
+template <int NT, bool kNamed>
+__device__ void topk_row(const float* row, int N, int K, int* idx_out, int* count_out,
+                         const TopkSmem& t, int* scratch) {
+  const int tid = threadIdx.x;
+  if (N <= K) {
+    for (int r = tid; r < K; r += NT) idx_out[r] = r < N ? r : -1;
+    if (tid == 0) *count_out = N;
+    return;
+  }
+  if (N <= 4 * NT)
+    topk_row_regs<NT, 4, kNamed>(row, N, K, idx_out, count_out, t, scratch);
+  else if (N <= 8 * NT)
+    topk_row_regs<NT, 8, kNamed>(row, N, K, idx_out, count_out, t, scratch);
+  else if (N <= 16 * NT)
+    topk_row_regs<NT, 16, kNamed>(row, N, K, idx_out, count_out, t, scratch);
+  else
+    topk_select<NT, kNamed>(row, N, K, idx_out, count_out, t, scratch);
 }
 
 // ------------------------------------------------------------------------------------

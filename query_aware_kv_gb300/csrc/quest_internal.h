@@ -138,7 +138,9 @@ cudaError_t launch_topk(const Params& p, cudaStream_t s);
 cudaError_t launch_decode(const Params& p, int G, cudaStream_t s);
 cudaError_t launch_fused(const Params& p, int G, int max_ctas, cudaStream_t s);
 size_t cluster_smem_bytes(int G, int P, int max_pages, int cs, int top_k);
+bool cluster_any_fits(int G, int P, int max_pages, int top_k);
 cudaError_t launch_cluster(const Params& p, int G, int cs, int max_clusters, cudaStream_t s);
 constexpr int kMaxClusterSize = 16;
+constexpr size_t kMaxSmem = 227 * 1024;  // dynamic shared memory of one CTA
 
 }  // namespace quest

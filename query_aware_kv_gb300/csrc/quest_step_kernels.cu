@@ -53,9 +53,9 @@ __global__ void __launch_bounds__(kConsumerThreads) topk_kernel(Params p) {
   const int L = load_len(p, b, kSiteTopk);
   const int N = (L + p.P - 1) / p.P;
   int* scratch = reinterpret_cast<int*>(sm + topk_smem_bytes(p.max_pages));
-  topk_select<kConsumerThreads, false>(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
-                                       p.sel_idx + (size_t)bg * p.top_k, p.sel_count + bg,
-                                       topk_smem_at(sm, p.max_pages), scratch);
+  topk_row<kConsumerThreads, false>(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
+                                    p.sel_idx + (size_t)bg * p.top_k, p.sel_count + bg,
+                                    topk_smem_at(sm, p.max_pages), scratch);
 }
 
 // ---------------------------------------------------------------- decode
@@ -137,7 +137,7 @@ cudaError_t launch_estimate(const Params& p, int G, cudaStream_t s) {
 
 cudaError_t launch_topk(const Params& p, cudaStream_t s) {
   const void* fn = (const void*)topk_kernel;
-  const size_t smem = topk_smem_bytes(p.max_pages) + 64 * 4;
+  const size_t smem = topk_smem_bytes(p.max_pages) + 256 * 4;
   cudaError_t e = ensure_smem(fn, smem);
   if (e != cudaSuccess) return e;
   Params pp = p;

@@ -100,6 +100,46 @@ def test_topk_exact_ties_go_to_lower_index():
     H.assert_status_ok(pair.ws)
 
 
+@pytest.mark.parametrize("n", [1024, 1025, 2048, 2049, 3000, 4096, 4097])
+def test_topk_row_sizes(n):
+    """Rows around the register-resident selection's size classes (4, 8 and 16 keys per
+    thread, then the shared-memory path), with outliers and exact ties."""
+    w = small(lens=(16 * n,), batch=1, hq=2, hkv=2, steps=0, budget=16 * 128)
+    pair = H.on_device(w, build_meta=False)
+    rng = np.random.default_rng(n)
+    scores = np.full((1, 2, w.block_table.shape[1]), -np.inf, np.float32)
+    scores[0, 0, :n] = rng.normal(200.0, 30.0, n).astype(np.float32)
+    scores[0, 0, rng.integers(0, n, 4)] = [5e3, 6e3, -7e3, 1e6]
+    scores[0, 1, :n] = rng.integers(0, 9, n).astype(np.float32) * 0.5  # heavy ties
+    for K in (1, 128, n // 2, n - 1):
+        idx, cnt = q.topk(pair.cache, torch.from_numpy(scores).cuda(), K, pair.ws)
+        ri, rc = oracle.topk(pair.ref, scores, K)
+        for g in range(2):
+            assert int(cnt[0, g]) == rc[0, g]
+            assert idx[0, g, :K].cpu().tolist() == sorted(ri[0, g, :K].tolist()), (K, g)
+    H.assert_status_ok(pair.ws)
+
+
+def test_topk_near_ties_over_a_wide_range():
+    """Distinct keys a few ulps apart at the threshold, in a row whose range spans the
+    whole float line: the two histogram levels cannot separate them, the radix select
+    must."""
+    n = 2000
+    w = small(lens=(16 * n,), batch=1, hq=1, hkv=1, steps=0, budget=16 * 100)
+    pair = H.on_device(w, build_meta=False)
+    scores = np.full((1, 1, w.block_table.shape[1]), -np.inf, np.float32)
+    base = np.float32(1.0)
+    near = np.nextafter(base, np.float32(2.0)) - base
+    scores[0, 0, :n] = np.float32(-3.0e38)
+    scores[0, 0, 1] = np.float32(3.0e38)
+    scores[0, 0, 10:310] = base + near * np.arange(300, dtype=np.float32)[::-1]
+    for K in (50, 100, 200):
+        idx, cnt = q.topk(pair.cache, torch.from_numpy(scores).cuda(), K, pair.ws)
+        ri, rc = oracle.topk(pair.ref, scores, K)
+        assert idx[0, 0, :K].cpu().tolist() == sorted(ri[0, 0, :K].tolist()), K
+    H.assert_status_ok(pair.ws)
+
+
 def test_topk_at_max_pages():
     """The largest supported row: 16384 pages."""
     n = q.QUEST_MAX_PAGES
@@ -214,6 +254,18 @@ def test_queue_variant_matches_cluster_variant():
     assert torch.equal(idx, idx0) and torch.equal(cnt, cnt0)
     torch.testing.assert_close(out.float(), base.float(), atol=2e-3, rtol=0)
     torch.testing.assert_close(lse, base_lse, atol=1e-4, rtol=0)
+
+
+@pytest.mark.parametrize("cs", [0, 1, 3, 16])
+def test_fused_step_long_rows(cs):
+    """Rows of 1.2K-3.2K pages (the register-resident selection's larger size classes) in
+    the fused step, two decode steps."""
+    w = small(lens=(33000, 20000, 51000), batch=3, hq=8, hkv=4, steps=2, budget=2048,
+              outliers=4, needles_per_head=2)
+    pair = H.on_device(w)
+    for t in range(w.steps):
+        H.run_step_and_compare(pair, t, w.top_k, opts=q.opts(cluster_size=cs), one_launch=True,
+                               check_needles=True)
 
 
 def test_trace_records_a_timeline():
