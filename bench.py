@@ -206,9 +206,10 @@ def run_quest(args):
     from query_aware_kv_gb300 import build as cuda_build
     from query_aware_kv_gb300 import workloads as wl
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from query_aware_kv_gb300 import replicas
+
+    ri = replicas.rank_info()
+    world, rank, local = ri.world, ri.rank, ri.local
     if world > 1:
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
@@ -220,7 +221,7 @@ def run_quest(args):
     q.load()
 
     # each rank decodes its own independent sequence (weak scaling, no collective)
-    w = wl.longchat_32k(seed=rank, device=dev)
+    w = wl.longchat_32k(seed=replicas.workload_seed(rank), device=dev)
     cache = q.PagedCache.allocate_meta(w.k_pool, w.v_pool, w.block_table, w.seq_lens.clone(),
                                        w.num_q_heads)
     K = w.top_k
@@ -399,11 +400,7 @@ def run_quest(args):
 
     # ---- max over ranks
     def rmax(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return replicas.max_over_ranks(x, world, dev)
 
     mean_step = rmax(mean_step)
     dec_us = rmax(dec_us)
@@ -426,7 +423,7 @@ def run_quest(args):
                    "l2": "flushed before every timed step (512 MiB write, then 256 MiB read)",
                    "step": "quest_decode_step: append + score + top-K + split-K decode, one launch",
                    "replicas": world},
-        "gbs": round(world * step_bytes / (mean_step * 1e-6) / 1e9, 1),
+        "gbs": round(replicas.job_bytes_per_second(step_bytes, world, mean_step * 1e-6) / 1e9, 1),
         "roofline": {"bound": "hbm", "kernel": "quest_decode (fused)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,

@@ -1,0 +1,56 @@
+"""Parity of the fused decode step at the full sizes of the five workloads, in the launch
+configuration the benchmark uses (automatic cluster size, quest_decode_step), against the
+CPU oracle on the same seeded inputs.  Acceptance rules as in tests/harness.py:
+
+* selection: exactly K_b distinct valid pages; swaps only inside the oracle's 1e-5
+  relative tie window around its K_b-th score;
+* attention: |gpu - oracle| <= 2e-3 + 1e-2 |oracle| against the oracle's attention over
+  the GPU's selected pages;
+* lengths, appended rows and boxes: bit-exact (checked on the last step);
+* planted needle pages are selected.
+"""
+import pytest
+import torch
+
+from query_aware_kv_gb300 import workloads as wl
+
+import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, steps, check_needles=True):
+    pair = H.on_device(w)
+    for t in range(steps):
+        H.run_step_and_compare(pair, t, w.top_k, one_launch=True, check_needles=check_needles,
+                               check_cache=(t == steps - 1))
+
+
+def test_longchat_32k_every_step():
+    """The benchmark workload: 32768 prefilled tokens, then all 64 decode steps (each
+    appends a token: 2049 -> 2052 pages), 32 MHA heads, budget 2048."""
+    w = wl.longchat_32k(seed=0, device="cuda")
+    _run(w, w.steps)
+
+
+@pytest.mark.parametrize("budget", [256, 512, 1024, 2048, 4096])
+def test_batched_ragged(budget):
+    """8 sequences of 8K-32K tokens, 32 heads, the five budgets; four decode steps."""
+    w = wl.batched_ragged(seed=0, device="cuda", budget=budget, steps=4)
+    _run(w, w.steps, check_needles=False)
+
+
+@pytest.mark.parametrize("layer,budget", [(0, 1024), (13, 2048), (31, 2048)])
+def test_yarn_128k_layers(layer, budget):
+    """Single layers of the 128K-context model (8192 pages per head); each head's needle
+    page must be kept."""
+    w = wl.yarn_128k_layer(layer, seed=0, device="cuda", budget=budget)
+    _run(w, 1)
+
+
+@pytest.mark.parametrize("page_size", [16, 32])
+def test_gqa_llama31(page_size):
+    """4 sequences of 64K tokens, 32 query / 8 kv heads, budget 4096, page 16 and 32."""
+    w = wl.gqa_llama31(seed=0, device="cuda", page_size=page_size)
+    _run(w, 1, check_needles=False)
+    torch.cuda.empty_cache()
