@@ -120,6 +120,11 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
+// Start pulling [p, p + bytes) into L2 (no destination in the CTA).  p and bytes: multiples
+// of 16.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -163,10 +168,9 @@ struct CSmem {
   uint32_t* ranges;        // [2][CS][2] key range of each CTA's share
   int* sel;                // [2][kcap] kept pages, ascending
   float* parts;            // [2][CS][G * (128 + 2)] partials M[G], L[G], A[G][128]
-  int* hist;               // [kTopkBins]
-  uint32_t* cand_key;      // [kTopkCand]   (large-N selection)
-  int* cand_idx;           // [kTopkCand]
-  uint32_t* kept;          // [ceil(max_pages / 32)]
+  int* hist;               // [2][kTopkBins], at the start of the ring: rank 0's ring is idle
+                           // while it selects
+  uint32_t* kept;          // [2][ceil(max_pages / 32)] selection bitmaps
 };
 
 constexpr int kLenCache = 1024;
@@ -195,6 +199,8 @@ __host__ __device__ inline size_t cluster_smem_layout(int G, int P, int max_page
   // streaming region
   size_t a = o;
   const size_t ring = a;     a = align_up(a + (size_t)kStages * 2 * P * kHeadDim * 2, 16);
+  static_assert((size_t)kStages * 2 * 16 * kHeadDim * 2 >= (size_t)2 * kTopkBins * 4,
+                "the ring holds the selection's histograms");
   const size_t sdesc = a;    a = align_up(a + kStages * sizeof(StageInfo), 16);
   const size_t wsc = a;      a = align_up(a + (size_t)kConsumerWarps * G * P * 4, 16);
   const size_t st = a;       a = align_up(a + (size_t)kConsumerWarps * G * 3 * 4, 16);
@@ -206,10 +212,7 @@ __host__ __device__ inline size_t cluster_smem_layout(int G, int P, int max_page
   const size_t ranges = b;   b = align_up(b + (size_t)2 * S * 2 * 4, 16);
   const size_t sel = b;      b = align_up(b + (size_t)2 * kcap * 4, 16);
   const size_t parts = b;    b = align_up(b + (size_t)2 * S * part_floats * 4, 16);
-  const size_t hist = b;     b = align_up(b + (size_t)kTopkBins * 4, 16);
-  const size_t ck = b;       b += (size_t)kTopkCand * 4;
-  const size_t ci = b;       b += (size_t)kTopkCand * 4;
-  const size_t kept = b;     b = align_up(b + (size_t)((max_pages + 31) / 32) * 4, 16);
+  const size_t kept = b;     b = align_up(b + (size_t)2 * ((max_pages + 31) / 32) * 4, 16);
   const size_t total = b;
   if (s) {
     s->full = reinterpret_cast<uint64_t*>(base + full);
@@ -231,9 +234,7 @@ __host__ __device__ inline size_t cluster_smem_layout(int G, int P, int max_page
     s->ranges = reinterpret_cast<uint32_t*>(base + ranges);
     s->sel = reinterpret_cast<int*>(base + sel);
     s->parts = reinterpret_cast<float*>(base + parts);
-    s->hist = reinterpret_cast<int*>(base + hist);
-    s->cand_key = reinterpret_cast<uint32_t*>(base + ck);
-    s->cand_idx = reinterpret_cast<int*>(base + ci);
+    s->hist = reinterpret_cast<int*>(base + ring);
     s->kept = reinterpret_cast<uint32_t*>(base + kept);
   }
   return total;
@@ -344,6 +345,14 @@ __device__ void c_produce_decode(const Params& p, const CSmem& s, const Pair& q,
   const int lane = threadIdx.x & 31;
   const int n_dec = q.q_hi - q.q_lo;
   bool ok = true;
+  if (lane == 0 && q.N > 0) {
+    // while the selection is being made: the pair's block-table row into L2, so that the
+    // page lookups after it hit L2 (whole 16-byte units inside the row only)
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p.block_table + (size_t)q.b * p.max_pages);
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(p.block_table + (size_t)q.b * p.max_pages + q.N);
+    const uintptr_t lo16 = (a0 + 15) & ~(uintptr_t)15, hi16 = a1 & ~(uintptr_t)15;
+    if (hi16 > lo16) prefetch_l2(reinterpret_cast<const void*>(lo16), (uint32_t)(hi16 - lo16));
+  }
   if (lane == 0) {
     ok = wait_cluster_bounded(p, &s.bar_sel[q.buf], (uint32_t)(j >> 1) & 1u, kSiteWaitSelection);
     mbar_arrive(&s.prod_ok[q.buf]);
@@ -572,9 +581,7 @@ __device__ void c_score_share(const Params& p, const CSmem& s, const Role& r, co
   }
 }
 
-// Selector: the top-K of pair q's N keys (in s.keys[buf]) into s.sel[buf], ascending.  One
-// shared-memory selection for every row length keeps the kernel's code small (its
-// instruction cache is shared by the selector and the streamer that share an SM).
+// Rank 0: the top-K of pair q's N keys (in s.keys[buf]) into s.sel[buf], ascending.
 __device__ void c_select(const Params& p, const CSmem& s, const Role& r, const Pair& q) {
   const int tid = threadIdx.x;
   const int kcap = min(p.top_k, p.max_pages);
@@ -591,13 +598,14 @@ __device__ void c_select(const Params& p, const CSmem& s, const Role& r, const P
     lo = min(lo, rg[2 * i]);
     hi = max(hi, rg[2 * i + 1]);
   }
-  TopkSmem t;
-  t.keys = s.keys + (size_t)q.buf * keys_stride(p.max_pages);
-  t.hist = s.hist;
-  t.cand_key = s.cand_key;
-  t.cand_idx = s.cand_idx;
-  t.kept = s.kept;
-  topk_core<kConsumerThreads, true>(q.N, q.count, sel, cnt_slot, t, s.scratch, lo, hi);
+  // the histograms live in the ring, which bulk copies wrote last: clear them first
+  for (int i = tid; i < 2 * kTopkBins / 4; i += kConsumerThreads)
+    reinterpret_cast<int4*>(s.hist)[i] = make_int4(0, 0, 0, 0);
+  bsync<kConsumerThreads, true>();
+  topk_keys<kConsumerThreads, true>(s.keys + (size_t)q.buf * keys_stride(p.max_pages), q.N,
+                                    q.count, lo, hi, sel, cnt_slot, s.hist, s.kept, s.scratch);
+  // the ring goes back to bulk copies (async proxy) after these generic writes
+  fence_proxy_async_smem();
 }
 
 // Selector: the selection, for the caller, if asked for (after it was released).

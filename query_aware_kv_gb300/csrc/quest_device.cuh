@@ -2,8 +2,8 @@
 //
 //   score_tile    : criticality bound of a run of pages for one (sequence, kv head)
 //                   ("Guide to Quest", Solution step 2).
-//   topk_select   : exact top-K of a score row, ties to the lower page index
-//                   ("Guide to Quest", Solution step 3).
+//   topk_keys     : exact top-K of a row of score keys, ties to the lower page index
+//   topk_row        ("Guide to Quest", Solution step 3); topk_row loads the row first.
 //   decode_tile   : flash-decode over a run of kept pages, staged into shared memory by
 //                   1-D bulk copies (TMA) with an mbarrier ring; writes one split-K partial
 //                   (Tang 2024 summary: exact attention over the Top-K pages).
@@ -355,15 +355,9 @@ __device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, fl
 
 // ------------------------------------------------------------------------------------
 // top-K: "Guide to Quest", Solution step 3.  Scores become order-preserving unsigned keys
-// (sign flip).  The keys' actual range [lo, hi] is cut into 2048 equal bins (an 11-bit
-// histogram of (key - lo) >> shift, warp-aggregated shared-memory atomics), a block scan
-// from the top bin finds the bin holding the K-th largest key, and the few keys of that
-// bin are ranked exactly (larger key first, then lower page).  A bin with more than 256
-// keys (many near-equal scores) falls back to an MSB-first radix select on the full keys.
-// A block scan then writes the kept pages in ascending page order.
+// (sign flip), so the K largest scores are the K largest keys; see topk_keys below.
 // ------------------------------------------------------------------------------------
 constexpr int kTopkBins = 2048;
-constexpr int kTopkCand = 256;
 
 __device__ __forceinline__ uint32_t score_key(float s) {
   const uint32_t u = __float_as_uint(s + 0.0f);  // -0 -> +0
@@ -374,14 +368,12 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 struct TopkSmem {
   uint32_t* keys;      // [max_pages]
   int* hist;           // [2 * kTopkBins]
-  uint32_t* cand_key;  // [kTopkCand]
-  int* cand_idx;       // [kTopkCand]
-  uint32_t* kept;      // [ceil(max_pages / 32)] bitmap of kept keys of the threshold bin
+  uint32_t* kept;      // [2][ceil(max_pages / 32)] bitmaps (kept keys; keys tied at the threshold)
 };
 
 __host__ __device__ inline size_t topk_smem_bytes(int max_pages) {
-  return align_up((size_t)max_pages * 4, 16) + (size_t)2 * kTopkBins * 4 + (size_t)kTopkCand * 8 +
-         align_up((size_t)((max_pages + 31) / 32) * 4, 16);
+  return align_up((size_t)max_pages * 4, 16) + (size_t)2 * kTopkBins * 4 +
+         align_up((size_t)2 * ((max_pages + 31) / 32) * 4, 16);
 }
 
 __device__ inline TopkSmem topk_smem_at(unsigned char* base, int max_pages) {
@@ -390,10 +382,6 @@ __device__ inline TopkSmem topk_smem_at(unsigned char* base, int max_pages) {
   base += align_up((size_t)max_pages * 4, 16);
   t.hist = reinterpret_cast<int*>(base);
   base += (size_t)2 * kTopkBins * 4;
-  t.cand_key = reinterpret_cast<uint32_t*>(base);
-  base += (size_t)kTopkCand * 4;
-  t.cand_idx = reinterpret_cast<int*>(base);
-  base += (size_t)kTopkCand * 4;
   t.kept = reinterpret_cast<uint32_t*>(base);
   return t;
 }
@@ -480,161 +468,21 @@ __device__ __forceinline__ int block_excl_sum(int v, int* tot) {
   return pre + x - v;
 }
 
-// Selection over keys already in t.keys[0..N) (N > K, N <= 64 * NT); lo / hi: this
-// thread's min / max over the keys it stored.  Writes K entries of idx_out (ascending) and
-// *count_out.  scratch >= 64 ints.  Called by threads 0..NT-1.  After the range is known,
-// thread tid owns the contiguous keys [tid * cpt, tid * cpt + cpt).
-template <int NT, bool kNamed>
-__device__ void topk_core(int N, int K, int* idx_out, int* count_out, const TopkSmem& t,
-                          int* scratch, uint32_t lo, uint32_t hi) {
-  static_assert(NT % 32 == 0 && NT <= 256 && kTopkBins % (4 * NT) == 0, "up to 8 whole warps");
-  constexpr int NW = NT / 32;  // scratch: [0,8) lo, [8,16) hi, [16,24) / [24,32) sums,
-                               // [40,44) threshold
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rounds = (N + NT - 1) / NT;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-  }
-  for (int i = tid; i < kTopkBins / 4; i += NT) reinterpret_cast<int4*>(t.hist)[i] = make_int4(0, 0, 0, 0);
-  for (int i = tid; i < (N + 31) / 32; i += NT) t.kept[i] = 0u;
-  if (lane == 0) {
-    scratch[warp] = (int)lo;
-    scratch[8 + warp] = (int)hi;
-  }
-  if (tid == 0) scratch[43] = 0;
-  bsync<NT, kNamed>();
-  lo = lane < NW ? (uint32_t)scratch[lane] : 0xffffffffu;
-  hi = lane < NW ? (uint32_t)scratch[8 + lane] : 0u;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-  }
-  const uint32_t span = hi - lo;
-  const int shift = span >= (uint32_t)kTopkBins ? (32 - __clz(span)) - 11 : 0;
-  // my contiguous block of keys, 4 at a time
-  const int cpt = (rounds + 3) & ~3;
-  const int i0 = tid * cpt;
-  auto load4 = [&](int i, uint32_t (&k)[4]) {
-    if (i + 3 < N) {
-      const uint4 q = *reinterpret_cast<const uint4*>(t.keys + i);
-      k[0] = q.x; k[1] = q.y; k[2] = q.z; k[3] = q.w;
-    } else {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) k[u] = i + u < N ? t.keys[i + u] : 0u;
-    }
-  };
-  // 2. histogram of (key - lo) >> shift over 2048 bins
-  for (int j = 0; j < cpt; j += 4) {
-    if (i0 + j >= N) break;
-    uint32_t k[4];
-    load4(i0 + j, k);
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (i0 + j + u < N) atomicAdd(&t.hist[(k[u] - lo) >> shift], 1);
-  }
-  bsync<NT, kNamed>();
-  // 3. from the top bin down, the bin where the count reaches K; thread tid owns the 8 bins
-  //    [2040 - 8 tid, 2047 - 8 tid]
-  constexpr int kBPT = kTopkBins / NT;
-  const int low = kTopkBins - kBPT * (tid + 1);
-  int h[kBPT];
-#pragma unroll
-  for (int q = 0; q < kBPT / 4; ++q) {
-    const int4 v = reinterpret_cast<const int4*>(t.hist + low)[q];
-    h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
-  }
-  int local = 0;
-#pragma unroll
-  for (int j = 0; j < kBPT; ++j) local += h[j];
-  const int excl = block_excl_sum<NT, kNamed>(local, scratch + 16);
-  if (excl < K && K <= excl + local) {
-    int acc = excl;
-#pragma unroll
-    for (int j = kBPT - 1; j >= 0; --j) {
-      if (acc < K && acc + h[j] >= K) {
-        scratch[40] = low + j;
-        scratch[41] = acc;
-        scratch[42] = h[j];
-      }
-      acc += h[j];
-    }
-  }
-  bsync<NT, kNamed>();
-  const int bstar = scratch[40], above = scratch[41], bucket = scratch[42];
-  const int need = K - above;  // 1 .. bucket
-  if (bucket != need && bucket > kTopkCand) {
-    topk_radix_keys<NT, kNamed>(t.keys, N, K, idx_out, count_out, t.hist, scratch);
-    return;
-  }
-  const bool whole = bucket == need;
-  if (!whole) {
-    // 4. rank the threshold bin's keys exactly: larger key first, then lower page
-    for (int j = 0; j < cpt; j += 4) {
-      if (i0 + j >= N) break;
-      uint32_t k[4];
-      load4(i0 + j, k);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (i0 + j + u < N && (int)((k[u] - lo) >> shift) == bstar) {
-          const int pos = atomicAdd(&scratch[43], 1);
-          t.cand_key[pos] = k[u];
-          t.cand_idx[pos] = i0 + j + u;
-        }
-      }
-    }
-    bsync<NT, kNamed>();
-    for (int j = tid; j < bucket; j += NT) {
-      const uint32_t kj = t.cand_key[j];
-      const int ij = t.cand_idx[j];
-      int r = 0;
-      for (int m = 0; m < bucket; ++m) {
-        const uint32_t km = t.cand_key[m];
-        r += (km > kj) || (km == kj && t.cand_idx[m] < ij);
-      }
-      if (r < need) atomicOr(&t.kept[ij >> 5], 1u << (ij & 31));
-    }
-    bsync<NT, kNamed>();
-  }
-  // 5. compaction in ascending page order: count my kept keys, one block scan, write
-  unsigned long long mine = 0ull;
-  int nsel = 0;
-  for (int j = 0; j < cpt; j += 4) {
-    if (i0 + j >= N) break;
-    uint32_t k[4];
-    load4(i0 + j, k);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + j + u;
-      const int bin = (int)((k[u] - lo) >> shift);
-      const bool sel = i < N && (bin > bstar || (bin == bstar && (whole || ((t.kept[i >> 5] >> (i & 31)) & 1u))));
-      mine |= (unsigned long long)sel << (j + u);
-      nsel += sel;
-    }
-  }
-  int pos = block_excl_sum<NT, kNamed>(nsel, scratch + 24);
-  while (mine) {
-    const int j = __ffsll((long long)mine) - 1;
-    idx_out[pos++] = i0 + j;
-    mine &= mine - 1ull;
-  }
-  if (tid == 0) *count_out = K;
-}
 
 // ------------------------------------------------------------------------------------
-// Register-resident selection for N <= KPT * NT keys (thread tid holds keys tid + r * NT,
-// r < KPT; key 0 marks "no key").  The same steps as topk_core, arranged as short
-// independent phases: one pass of shared-memory reductions into a 2048-bin histogram of
-// (key - lo) >> shift, a block scan for the threshold bin, a second 2048-bin histogram
-// inside that bin when it is not decided, then the kept keys are written in ascending
-// index order from warp ballots and one scan of the per-(round, warp) counts.  Keys equal
-// to the threshold key keep the lowest indices.  When the second level still leaves
-// distinct keys in one sub-bin (spans above 2^22 with near-equal keys), the keys go to
-// `spill` and the radix select decides.
-// hist: 2 * kTopkBins ints, zero on entry (left dirty); scratch >= 64 + KPT * NT / 32 ints;
-// spill: N words of shared memory (used only by the radix fallback).
+// Exact selection over N <= 64 * NT keys in shared memory.  With d = key - lo (lo, hi: the
+// keys' range), the bits of d are resolved 11 at a time from the top, like a radix select
+// whose digits start at the span's leading bit: each level histograms the digit of the
+// keys still tied with the threshold (2048 bins), a block scan finds the bin holding the
+// K-th largest key, and the level ends when that bin is taken whole or d is exhausted
+// (at most 3 levels).  A last pass over the keys (the same loop, in marking mode) sets
+// two bitmaps: keys above the threshold, and keys equal to it (the lowest indices of those
+// are kept); one block scan of the per-thread counts then places the kept indices in
+// ascending order.  Running every
+// level and the marking pass through one loop keeps the code small: this routine runs once
+// per launch and its first pass waits for instruction fetches.
+// hist: 2 * kTopkBins ints, zero on entry (left zero); bits: 2 * ceil(N / 32) words;
+// scratch: 64 ints.  Called by threads 0..NT-1.
 // ------------------------------------------------------------------------------------
 template <int NT, bool kNamed>
 __device__ __forceinline__ void topk_find_bin(const int* hist, int need, int* out3, int* sums) {
@@ -666,145 +514,119 @@ __device__ __forceinline__ void topk_find_bin(const int* hist, int need, int* ou
   bsync<NT, kNamed>();
 }
 
-template <int NT, int KPT, bool kNamed>
-__device__ void topk_regs(const uint32_t (&k)[KPT], int N, int K, uint32_t lo, uint32_t hi,
-                          int* idx_out, int* count_out, int* hist, int* scratch,
-                          uint32_t* spill) {
+template <int NT, bool kNamed>
+__device__ void topk_keys(const uint32_t* keys, int N, int K, uint32_t lo, uint32_t hi,
+                          int* idx_out, int* count_out, int* hist, uint32_t* bits,
+                          int* scratch) {
   static_assert(NT % 32 == 0 && NT <= 256 && kTopkBins % (4 * NT) == 0, "up to 8 whole warps");
-  constexpr int NW = NT / 32;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int* hist2 = hist + kTopkBins;
-  int* cnt = scratch + 64;  // [KPT][NW] packed (definite << 16 | tie) counts, then prefixes
+  const int tid = threadIdx.x;
+  const int nw = (N + 31) >> 5;
+  uint32_t* dbits = bits;
+  uint32_t* tbits = bits + nw;
+  for (int i = tid; i < 2 * nw; i += NT) bits[i] = 0u;
+  // level: the keys with (d >> top) == prefix are still tied with the threshold; this
+  // level resolves bits [sh, top) of d (at most 11)
   const uint32_t span = hi - lo;
-  const int shift1 = span >= (uint32_t)kTopkBins ? (32 - __clz(span)) - 11 : 0;
-  // 1. level-1 histogram
-#pragma unroll
-  for (int r = 0; r < KPT; ++r)
-    if (r * NT + tid < N) atomicAdd(&hist[(k[r] - lo) >> shift1], 1);
-  bsync<NT, kNamed>();
-  topk_find_bin<NT, kNamed>(hist, K, scratch + 40, scratch + 16);
-  const int bstar = scratch[40], above = scratch[41], bucket = scratch[42];
-  const int need = K - above;  // 1 .. bucket
-  const bool whole1 = bucket == need;
-  const bool exact1 = shift1 == 0;
-  // 2. inside the threshold bin, if it is not decided
-  const int shift2 = shift1 > 11 ? shift1 - 11 : 0;
-  const uint32_t mask1 = shift1 >= 32 ? 0xffffffffu : ((1u << shift1) - 1u);
-  int b2star = 0, need_t = need;
-  bool whole2 = true;
-  if (!whole1 && !exact1) {
-#pragma unroll
-    for (int r = 0; r < KPT; ++r) {
-      const uint32_t d = k[r] - lo;
-      if (r * NT + tid < N && (int)(d >> shift1) == bstar)
-        atomicAdd(&hist2[(d & mask1) >> shift2], 1);
+  int sh = span >= (uint32_t)kTopkBins ? (32 - __clz(span)) - 11 : 0;
+  int top = sh + 11;
+  uint64_t prefix = 0;
+  int need = K;  // keys still to take among the tied ones
+  bool mark = false, whole = false;
+  for (int level = 0;; ++level) {
+    int* h = hist + (level & 1) * kTopkBins;
+#pragma unroll 4
+    for (int i = tid; i < N; i += NT) {
+      const uint64_t d = keys[i] - lo;
+      if (!mark) {
+        if ((d >> top) == prefix) atomicAdd(&h[(int)((d >> sh) & (kTopkBins - 1))], 1);
+      } else {
+        // marking pass: above the threshold, or equal to it (only once d is exhausted,
+        // or when the whole threshold bin is taken)
+        const uint64_t v = d >> top;
+        if (v > prefix || (v == prefix && whole))
+          atomicOr(&dbits[i >> 5], 1u << (i & 31));
+        else if (v == prefix)
+          atomicOr(&tbits[i >> 5], 1u << (i & 31));
+      }
     }
+    if (mark) break;
     bsync<NT, kNamed>();
-    topk_find_bin<NT, kNamed>(hist2, need, scratch + 44, scratch + 24);
-    b2star = scratch[44];
-    need_t = need - scratch[45];
-    whole2 = scratch[46] == need_t;
-    if (!whole2 && shift2 != 0) {
-      // distinct keys share the deciding sub-bin: exact radix select over all keys
-#pragma unroll
-      for (int r = 0; r < KPT; ++r)
-        if (r * NT + tid < N) spill[r * NT + tid] = k[r];
-      bsync<NT, kNamed>();
-      topk_radix_keys<NT, kNamed>(spill, N, K, idx_out, count_out, hist, scratch);
-      return;
-    }
-  }
-  // 3. classify: definite keep, or a key equal to the threshold key (keep the lowest
-  //    indices); predicates first, then the ballots, then one count store per lane
-  bool def[KPT], tie[KPT];
-#pragma unroll
-  for (int r = 0; r < KPT; ++r) {
-    const uint32_t d = k[r] - lo;
-    const int b1 = (int)(d >> shift1);
-    const int b2 = (int)((d & mask1) >> shift2);
-    const bool valid = r * NT + tid < N;
-    const bool in_bin = valid && b1 == bstar;
-    const bool refine = !whole1 && !exact1;
-    def[r] = valid && (b1 > bstar || (in_bin && (whole1 || (refine && (b2 > b2star || (b2 == b2star && whole2))))));
-    tie[r] = in_bin && !whole1 && (exact1 || (b2 == b2star && !whole2));
-  }
-  unsigned bd[KPT], bt[KPT];
-#pragma unroll
-  for (int r = 0; r < KPT; ++r) bd[r] = __ballot_sync(0xffffffffu, def[r]);
-#pragma unroll
-  for (int r = 0; r < KPT; ++r) bt[r] = __ballot_sync(0xffffffffu, tie[r]);
-  int mine = 0;
-#pragma unroll
-  for (int r = 0; r < KPT; ++r)
-    if (lane == r) mine = (__popc(bd[r]) << 16) | __popc(bt[r]);
-  if (lane < KPT) cnt[lane * NW + warp] = mine;
-  bsync<NT, kNamed>();
-  // 4. exclusive prefix of the (round, warp) counts in index order, by warp 0
-  if (warp == 0) {
-    constexpr int E = KPT * NW;
-    constexpr int EPL = (E + 31) / 32;
-    int v[EPL];
-    int run = 0;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const int i = lane * EPL + e;
-      v[e] = i < E ? cnt[i] : 0;
-      run += v[e];
-    }
-    int incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    int pre = incl - run;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const int i = lane * EPL + e;
-      if (i < E) cnt[i] = pre;
-      pre += v[e];
+    int* f = scratch + 40 + 4 * (level & 1);
+    topk_find_bin<NT, kNamed>(h, need, f, scratch + 16 + 8 * (level & 1));
+    const int bstar = f[0], above = f[1], bucket = f[2];
+    // clear this level's histogram for the level after next (the next one uses the other)
+    for (int i = tid; i < kTopkBins / 4; i += NT) reinterpret_cast<int4*>(h)[i] = make_int4(0, 0, 0, 0);
+    need -= above;
+    prefix = (prefix << (top - sh)) | (uint64_t)bstar;
+    top = sh;
+    whole = bucket == need;
+    if (whole || sh == 0) {
+      mark = true;  // next pass marks the kept keys
+    } else {
+      sh = sh > 11 ? sh - 11 : 0;
     }
   }
   bsync<NT, kNamed>();
-  // 5. write the kept indices in ascending order (every count read before any write)
-  const unsigned lt = lanemask_lt();
-  int pre[KPT];
-#pragma unroll
-  for (int r = 0; r < KPT; ++r) pre[r] = cnt[r * NW + warp];
-#pragma unroll
-  for (int r = 0; r < KPT; ++r) {
-    const int d_before = (pre[r] >> 16) + __popc(bd[r] & lt);
-    const int t_before = (pre[r] & 0xffff) + __popc(bt[r] & lt);
-    const int i = r * NT + tid;
-    if ((bd[r] >> lane) & 1u)
-      idx_out[d_before + min(t_before, need_t)] = i;
-    else if (((bt[r] >> lane) & 1u) && t_before < need_t)
-      idx_out[d_before + t_before] = i;
+  // every thread writes the kept indices of its words, at offsets from one block scan of
+  // the (kept, tied) counts (packed in one int: both are below 2^16)
+  const int wpt = (nw + NT - 1) / NT;
+  const int w0 = min(nw, tid * wpt), w1 = min(nw, w0 + wpt);
+  int nd = 0, nt = 0;
+  for (int w = w0; w < w1; ++w) {
+    nd += __popc(dbits[w]);
+    nt += __popc(tbits[w]);
+  }
+  const int before = block_excl_sum<NT, kNamed>((nd << 16) | nt, scratch + 32);
+  int dcnt = before >> 16, tcnt = before & 0xffff;
+  for (int w = w0; w < w1; ++w) {
+    const uint32_t D = dbits[w], T = tbits[w];
+    uint32_t A = D | T;
+    while (A) {
+      const int b = __ffs(A) - 1;
+      A &= A - 1u;
+      const int i = w * 32 + b;
+      if ((D >> b) & 1u) {
+        idx_out[dcnt + min(tcnt, need)] = i;
+        ++dcnt;
+      } else {
+        if (tcnt < need) idx_out[dcnt + tcnt] = i;
+        ++tcnt;
+      }
+    }
   }
   if (tid == 0) *count_out = K;
 }
 
-// One score row in global memory, N <= KPT * NT: keys straight into registers, then
-// topk_regs.  scratch >= 64 + KPT * NT / 32 ints.
-template <int NT, int KPT, bool kNamed>
-__device__ void topk_row_regs(const float* row, int N, int K, int* idx_out, int* count_out,
-                              const TopkSmem& t, int* scratch) {
+// One row of N scores in global memory (possibly written by another CTA): keys into shared
+// memory with their range, then topk_keys.  N <= 64 * NT.
+template <int NT, bool kNamed>
+__device__ void topk_row(const float* row, int N, int K, int* idx_out, int* count_out,
+                         const TopkSmem& t, int* scratch) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = NT / 32;
-  uint32_t k[KPT];
-  float v[KPT];
-#pragma unroll
-  for (int r = 0; r < KPT; ++r) {
-    const int i = r * NT + tid;
-    v[r] = i < N ? __ldcg(row + i) : 0.f;
+  if (N <= K) {
+    for (int r = tid; r < K; r += NT) idx_out[r] = r < N ? r : -1;
+    if (tid == 0) *count_out = N;
+    return;
   }
   uint32_t lo = 0xffffffffu, hi = 0u;
+  const int rounds = (N + NT - 1) / NT;
+  for (int r0 = 0; r0 < rounds; r0 += 16) {
+    float v[16];
 #pragma unroll
-  for (int r = 0; r < KPT; ++r) {
-    k[r] = score_key(v[r]);
-    if (r * NT + tid < N) {
-      lo = min(lo, k[r]);
-      hi = max(hi, k[r]);
+    for (int u = 0; u < 16; ++u) {
+      const int i = (r0 + u) * NT + tid;
+      v[u] = i < N ? __ldcg(row + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = (r0 + u) * NT + tid;
+      if (i < N) {
+        const uint32_t k = score_key(v[u]);
+        t.keys[i] = k;
+        lo = min(lo, k);
+        hi = max(hi, k);
+      }
     }
   }
 #pragma unroll
@@ -826,67 +648,10 @@ __device__ void topk_row_regs(const float* row, int N, int K, int* idx_out, int*
     lo = min(lo, (uint32_t)scratch[w]);
     hi = max(hi, (uint32_t)scratch[8 + w]);
   }
-  topk_regs<NT, KPT, kNamed>(k, N, K, lo, hi, idx_out, count_out, t.hist, scratch, t.keys);
+  topk_keys<NT, kNamed>(t.keys, N, K, lo, hi, idx_out, count_out, t.hist, t.kept, scratch);
 }
 
-// One score row in global memory: register-resident selection up to 16 * NT keys, the
-// shared-memory one above.
-template <int NT, bool kNamed>
-__device__ void topk_row(const float* row, int N, int K, int* idx_out, int* count_out,
-                         const TopkSmem& t, int* scratch);
 
-// row: N scores in global memory (possibly written by other CTAs of this grid), N <= 64 NT.
-template <int NT, bool kNamed>
-__device__ void topk_select(const float* row, int N, int K, int* idx_out, int* count_out,
-                            const TopkSmem& t, int* scratch) {
-  const int tid = threadIdx.x;
-  if (N <= K) {
-    for (int r = tid; r < K; r += NT) idx_out[r] = r < N ? r : -1;
-    if (tid == 0) *count_out = N;
-    return;
-  }
-  // keys (coalesced loads, 16 in flight per thread) and this thread's range
-  uint32_t lo = 0xffffffffu, hi = 0u;
-  const int rounds = (N + NT - 1) / NT;
-  for (int r0 = 0; r0 < rounds; r0 += 16) {
-    float v[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int i = (r0 + u) * NT + tid;
-      v[u] = i < N ? __ldcg(row + i) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int i = (r0 + u) * NT + tid;
-      if (i < N) {
-        const uint32_t k = score_key(v[u]);
-        t.keys[i] = k;
-        lo = min(lo, k);
-        hi = max(hi, k);
-      }
-    }
-  }
-  topk_core<NT, kNamed>(N, K, idx_out, count_out, t, scratch, lo, hi);
-}
-
-template <int NT, bool kNamed>
-__device__ void topk_row(const float* row, int N, int K, int* idx_out, int* count_out,
-                         const TopkSmem& t, int* scratch) {
-  const int tid = threadIdx.x;
-  if (N <= K) {
-    for (int r = tid; r < K; r += NT) idx_out[r] = r < N ? r : -1;
-    if (tid == 0) *count_out = N;
-    return;
-  }
-  if (N <= 4 * NT)
-    topk_row_regs<NT, 4, kNamed>(row, N, K, idx_out, count_out, t, scratch);
-  else if (N <= 8 * NT)
-    topk_row_regs<NT, 8, kNamed>(row, N, K, idx_out, count_out, t, scratch);
-  else if (N <= 16 * NT)
-    topk_row_regs<NT, 16, kNamed>(row, N, K, idx_out, count_out, t, scratch);
-  else
-    topk_select<NT, kNamed>(row, N, K, idx_out, count_out, t, scratch);
-}
 
 // ------------------------------------------------------------------------------------
 // decode: one page of one kv head against the G query heads of its group, in one warp.
