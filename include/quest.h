@@ -117,6 +117,14 @@ typedef struct quest_opts {
                                  0: the largest size up to 8 at which every pair's cluster
                                  is resident at once (1 when there are more pairs than SMs
                                  can hold)                                                  */
+    int32_t sink_pages;       /* quest_topk / quest_decode*: the first sink_pages pages of   */
+    int32_t local_pages;      /* a sequence longer than top_k pages, and its last
+                                 local_pages pages, are always kept; the other
+                                 top_k - sink_pages - local_pages slots go to the best of
+                                 the rest ([Guide] Solution step 3, third bullet;
+                                 Implementation step 2).  0 and 0 (the default): plain
+                                 top-K.  Needs sink_pages, local_pages >= 0 and
+                                 sink_pages + local_pages <= top_k (QUEST_ERR_INVALID_ARG) */
     int32_t pad_;
 } quest_opts_t;
 
@@ -176,9 +184,11 @@ int quest_estimate(const quest_cache_t* cache, const void* q, float* scores, voi
  * N_b <= top_k every page is kept.  idx: int32 [batch][num_kv_heads][top_k], the kept
  * logical pages in ASCENDING page order, -1 after the first K_b; count: int32
  * [batch][num_kv_heads] = K_b.  Selection is an exact radix select on the fp32 scores.
+ * opts (may be NULL): sink_pages / local_pages force the first and last pages in.
  */
 int quest_topk(const quest_cache_t* cache, const float* scores, int32_t top_k, int32_t* idx,
-               int32_t* count, void* ws, size_t ws_bytes, quest_stream_t stream);
+               int32_t* count, void* ws, size_t ws_bytes, const quest_opts_t* opts,
+               quest_stream_t stream);
 
 /*
  * Attention over the kept pages.  [Summary] Summary: exact attention is computed only

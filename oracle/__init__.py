@@ -60,7 +60,7 @@ def _load():
             lib.oq_build_meta.argtypes = [D, P, P, P, P]
             lib.oq_append.argtypes = [D, P, P, P, P, P, P, P]
             lib.oq_score.argtypes = [D, P, P, P, P, P]
-            lib.oq_topk.argtypes = [D, P, P, ctypes.c_int, P, P]
+            lib.oq_topk.argtypes = [D, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
             lib.oq_attend.argtypes = [D, P, P, P, P, P, P, P, ctypes.c_int, P, P]
             for f in (lib.oq_build_meta, lib.oq_append, lib.oq_score, lib.oq_topk,
                       lib.oq_attend):
@@ -144,16 +144,18 @@ def score(c: Cache, q) -> np.ndarray:
     return out
 
 
-def topk(c: Cache, scores, K: int) -> Tuple[np.ndarray, np.ndarray]:
-    """Kept pages in rank order [B][Hkv][K] (-1 padded) and counts [B][Hkv]."""
+def topk(c: Cache, scores, K: int, sink: int = 0, local: int = 0) -> Tuple[np.ndarray, np.ndarray]:
+    """Kept pages [B][Hkv][K] (-1 padded) and counts [B][Hkv]: with sink = local = 0 in
+    rank order; otherwise the first `sink` and last `local` pages of every sequence longer
+    than K pages, then the best of the others in rank order."""
     dims = c.dims()
     sc = _f32(scores)
     idx = np.empty((dims.batch, dims.num_kv_heads, K), np.int32)
     cnt = np.empty((dims.batch, dims.num_kv_heads), np.int32)
-    rc = _load().oq_topk(ctypes.byref(dims), _ptr(sc), _ptr(c.seq_lens), int(K), _ptr(idx),
-                         _ptr(cnt))
+    rc = _load().oq_topk(ctypes.byref(dims), _ptr(sc), _ptr(c.seq_lens), int(K), int(sink),
+                         int(local), _ptr(idx), _ptr(cnt))
     if rc:
-        raise OracleError("topk: bad K or length")
+        raise OracleError("topk: bad K, window or length")
     return idx, cnt
 
 
@@ -193,12 +195,12 @@ def dense(c: Cache, q) -> Tuple[np.ndarray, np.ndarray]:
     return attend(c, q, idx, cnt)
 
 
-def decode_step(c: Cache, q, K: int, k_new=None, v_new=None):
+def decode_step(c: Cache, q, K: int, k_new=None, v_new=None, sink: int = 0, local: int = 0):
     """One decode step: optional append, then score, select and attend.
     Returns (scores, idx, count, out, lse)."""
     if k_new is not None:
         append(c, k_new, v_new)
     s = score(c, q)
-    idx, cnt = topk(c, s, K)
+    idx, cnt = topk(c, s, K, sink, local)
     out, lse = attend(c, q, idx, cnt)
     return s, idx, cnt, out, lse

@@ -199,8 +199,17 @@ int oq_score(const oq_dims* s, const float* q, const float* meta, const int32_t*
  * ([Summary]: "Top-K highest-scoring pages").  Pages are ordered by score, larger
  * first, and equal scores by page index, lower first; the first K_b = min(K, N_b) are
  * kept.  When the sequence has no more than K pages every page is kept ([Guide],
- * Implementation step 2, the short-sequence case).  idx receives the kept pages in that
- * rank order; entries past count are set to -1.
+ * Implementation step 2, the short-sequence case).
+ *
+ * Mandatory pages ([Guide] Solution step 3, third bullet, and Implementation step 2):
+ * the first `sink` pages and the last `local` pages of a sequence longer than K pages are
+ * kept unconditionally, and only the remaining K - sink - local slots are competed for,
+ * by the pages between them, in the order above.  sink = local = 0 is the plain top-K;
+ * local = 0 keeps no trailing page.  Requires sink, local >= 0 and sink + local <= K.
+ *
+ * idx receives the kept pages: for a short sequence all pages in rank order, otherwise the
+ * sinks, then the local pages, then the competitive pages in rank order; entries past
+ * count are set to -1.
  * --------------------------------------------------------------------------------- */
 typedef struct {
     float score;
@@ -215,9 +224,9 @@ static int oq_rank_cmp(const void* x, const void* y) {
     return (a->page < b->page) ? -1 : (a->page > b->page) ? 1 : 0;
 }
 
-int oq_topk(const oq_dims* s, const float* scores, const int32_t* seq_lens, int K,
-            int32_t* idx, int32_t* count) {
-    if (K < 1) return -1;
+int oq_topk(const oq_dims* s, const float* scores, const int32_t* seq_lens, int K, int sink,
+            int local, int32_t* idx, int32_t* count) {
+    if (K < 1 || sink < 0 || local < 0 || sink + local > K) return -1;
     oq_ranked* tmp = (oq_ranked*)malloc(sizeof(oq_ranked) * (size_t)(s->max_pages > 0 ? s->max_pages : 1));
     if (!tmp) return -1;
     for (int b = 0; b < s->batch; ++b) {
@@ -227,14 +236,28 @@ int oq_topk(const oq_dims* s, const float* scores, const int32_t* seq_lens, int 
         for (int g = 0; g < s->num_kv_heads; ++g) {
             const float* row = scores + ((size_t)b * s->num_kv_heads + g) * s->max_pages;
             int32_t* out = idx + ((size_t)b * s->num_kv_heads + g) * K;
-            for (int p = 0; p < n_pages; ++p) {
-                tmp[p].score = row[p];
-                tmp[p].page = p;
+            int n_out = 0;
+            if (n_pages <= K) {
+                for (int p = 0; p < n_pages; ++p) {
+                    tmp[p].score = row[p];
+                    tmp[p].page = p;
+                }
+                qsort(tmp, (size_t)n_pages, sizeof(oq_ranked), oq_rank_cmp);
+                for (int r = 0; r < n_pages; ++r) out[n_out++] = tmp[r].page;
+            } else {
+                for (int p = 0; p < sink; ++p) out[n_out++] = p;
+                for (int p = n_pages - local; p < n_pages; ++p) out[n_out++] = p;
+                int n_cand = 0;
+                for (int p = sink; p < n_pages - local; ++p) {
+                    tmp[n_cand].score = row[p];
+                    tmp[n_cand].page = p;
+                    ++n_cand;
+                }
+                qsort(tmp, (size_t)n_cand, sizeof(oq_ranked), oq_rank_cmp);
+                for (int r = 0; r < K - sink - local; ++r) out[n_out++] = tmp[r].page;
             }
-            qsort(tmp, (size_t)n_pages, sizeof(oq_ranked), oq_rank_cmp);
-            const int kb = n_pages < K ? n_pages : K;
-            for (int r = 0; r < K; ++r) out[r] = (r < kb) ? tmp[r].page : -1;
-            count[(size_t)b * s->num_kv_heads + g] = kb;
+            for (int r = n_out; r < K; ++r) out[r] = -1;
+            count[(size_t)b * s->num_kv_heads + g] = n_out;
         }
     }
     free(tmp);

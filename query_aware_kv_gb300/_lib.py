@@ -66,7 +66,8 @@ class QuestOpts(ctypes.Structure):
         ("max_ctas", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
         ("wait_limit_ns", ctypes.c_int64), ("decode_lag", ctypes.c_int32),
         ("trace_capacity", ctypes.c_int32), ("trace", ctypes.c_void_p),
-        ("cluster_size", ctypes.c_int32), ("pad_", ctypes.c_int32),
+        ("cluster_size", ctypes.c_int32), ("sink_pages", ctypes.c_int32),
+        ("local_pages", ctypes.c_int32), ("pad_", ctypes.c_int32),
     ]
 
 
@@ -94,7 +95,7 @@ def load() -> ctypes.CDLL:
             "quest_build_meta": (ctypes.c_int, [C, V, SZ, V]),
             "quest_append": (ctypes.c_int, [C, V, V, V, SZ, V]),
             "quest_estimate": (ctypes.c_int, [C, V, V, V, SZ, V]),
-            "quest_topk": (ctypes.c_int, [C, V, I32, V, V, V, SZ, V]),
+            "quest_topk": (ctypes.c_int, [C, V, I32, V, V, V, SZ, O, V]),
             "quest_sparse_decode": (ctypes.c_int, [C, V, V, V, I32, V, V, V, SZ, O, V]),
             "quest_decode": (ctypes.c_int, [C, V, I32, V, V, V, V, V, SZ, O, V]),
             "quest_decode_step": (ctypes.c_int, [C, V, V, V, I32, V, V, V, V, V, SZ, O, V]),
@@ -142,15 +143,18 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
 
 def opts(pages_per_split: int = 0, score_tile_pages: int = 0, max_ctas: int = 0,
          debug_flags: int = 0, wait_limit_ns: int = 0, decode_lag: int = 0,
-         trace: Optional[torch.Tensor] = None, cluster_size: int = 0) -> QuestOpts:
+         trace: Optional[torch.Tensor] = None, cluster_size: int = 0, sink_pages: int = 0,
+         local_pages: int = 0) -> QuestOpts:
     """Launch tuning (0 = default).  ``trace``: int64 CUDA tensor of 1 + 2n elements whose
-    first element is zero; receives up to n timeline records of the fused kernel."""
+    first element is zero; receives up to n timeline records of the fused kernel.
+    ``sink_pages`` / ``local_pages``: pages always kept at the start / end of a sequence
+    longer than top_k pages."""
     cap, ptr = 0, None
     if trace is not None:
         _need(trace, "trace", torch.int64)
         cap, ptr = (trace.numel() - 1) // 2, trace.data_ptr()
     o = QuestOpts(pages_per_split, score_tile_pages, max_ctas, debug_flags, wait_limit_ns,
-                  decode_lag, cap, ptr, cluster_size, 0)
+                  decode_lag, cap, ptr, cluster_size, sink_pages, local_pages, 0)
     o._trace_ref = trace  # keep the buffer alive with the options
     return o
 
@@ -256,14 +260,14 @@ def estimate(cache: PagedCache, q: torch.Tensor, ws: torch.Tensor,
 
 
 def topk(cache: PagedCache, scores: torch.Tensor, top_k: int, ws: torch.Tensor,
-         stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+         o: Optional[QuestOpts] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     _need(scores, "scores", torch.float32, (cache.batch, cache.num_kv_heads, cache.max_pages))
     idx = torch.empty((cache.batch, cache.num_kv_heads, top_k), dtype=torch.int32,
                       device=scores.device)
     cnt = torch.empty((cache.batch, cache.num_kv_heads), dtype=torch.int32, device=scores.device)
     _check(load().quest_topk(ctypes.byref(cache.desc), scores.data_ptr(), int(top_k),
                              idx.data_ptr(), cnt.data_ptr(), ws.data_ptr(), ws.numel(),
-                             _stream(stream)))
+                             _opts_ref(o), _stream(stream)))
     return idx, cnt
 
 

@@ -70,6 +70,16 @@ int check_topk(int top_k) {
   return QUEST_OK;
 }
 
+int check_window(const quest_opts_t* o, int top_k) {
+  if (!o) return QUEST_OK;
+  if (o->sink_pages < 0 || o->local_pages < 0 ||
+      (long long)o->sink_pages + o->local_pages > (long long)top_k)
+    return fail(QUEST_ERR_INVALID_ARG,
+                "sink_pages %d and local_pages %d must be >= 0 with a sum <= top_k %d",
+                o->sink_pages, o->local_pages, top_k);
+  return QUEST_OK;
+}
+
 Tiling make_tiling(const quest_cache_t* c, int top_k, const quest_opts_t* o) {
   Tiling t{};
   t.topk_cap = top_k;
@@ -137,6 +147,8 @@ Params make_params(const quest_cache_t* c, void* ws, const WsLayout& L, const Ti
   p.n_score_tiles = t.n_score_tiles;
   p.wait_limit_ns = (o && o->wait_limit_ns > 0) ? o->wait_limit_ns : kDefaultWaitNs;
   p.debug_flags = o ? o->debug_flags : 0;
+  p.sink_pages = o ? o->sink_pages : 0;
+  p.local_pages = o ? o->local_pages : 0;
   p.qscale = (float)(1.4426950408889634 / std::sqrt((double)kHeadDim));
   return p;
 }
@@ -251,16 +263,18 @@ int quest_estimate(const quest_cache_t* cache, const void* q, float* scores, voi
 }
 
 int quest_topk(const quest_cache_t* cache, const float* scores, int32_t top_k, int32_t* idx,
-               int32_t* count, void* ws, size_t ws_bytes, quest_stream_t stream) {
+               int32_t* count, void* ws, size_t ws_bytes, const quest_opts_t* opts,
+               quest_stream_t stream) {
   int rc = check_cache(cache);
   if (rc) return rc;
   if ((rc = check_topk(top_k))) return rc;
+  if ((rc = check_window(opts, top_k))) return rc;
   if (cache->batch == 0) return QUEST_OK;
   if (!scores || !idx || !count || !aligned(scores, 4) || !aligned(idx, 4) || !aligned(count, 4))
     return fail(QUEST_ERR_INVALID_ARG, "scores / idx / count must be non-NULL and 4-byte aligned");
   if ((rc = check_ws(ws, ws_bytes, sizeof(WsHeader)))) return rc;
   const Tiling t = make_tiling(cache, top_k, nullptr);
-  Params p = make_params(cache, ws, make_layout(cache, t), t, nullptr);
+  Params p = make_params(cache, ws, make_layout(cache, t), t, opts);
   p.scores = const_cast<float*>(scores);
   p.sel_idx = idx;
   p.sel_count = count;
@@ -302,6 +316,7 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   int rc = check_cache(cache);
   if (rc) return rc;
   if ((rc = check_topk(top_k))) return rc;
+  if ((rc = check_window(opts, top_k))) return rc;
   if (cache->batch == 0) return QUEST_OK;
   if (!q || !out || !aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(idx_out, 4) || !aligned(count_out, 4))

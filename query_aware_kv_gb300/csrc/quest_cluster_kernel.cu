@@ -545,7 +545,10 @@ __device__ void c_score_share(const Params& p, const CSmem& s, const Role& r, co
         best = fmaxf(best, sc);
       }
       if (c == 0 && page < q.p_hi) {
-        const uint32_t key = score_key(have ? best : -CUDART_INF_F);
+        // pages of the sink / local window of a long sequence get the largest key
+        const bool forced =
+            q.N > q.count && (page < p.sink_pages || page >= q.N - p.local_pages);
+        const uint32_t key = forced ? 0xffffffffu : score_key(have ? best : -CUDART_INF_F);
         kout[page - q.p_lo] = key;
         lo = min(lo, key);
         hi = max(hi, key);

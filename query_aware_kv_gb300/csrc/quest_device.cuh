@@ -598,10 +598,11 @@ __device__ void topk_keys(const uint32_t* keys, int N, int K, uint32_t lo, uint3
 }
 
 // One row of N scores in global memory (possibly written by another CTA): keys into shared
-// memory with their range, then topk_keys.  N <= 64 * NT.
+// memory with their range, then topk_keys.  N <= 64 * NT.  In a row longer than K, the
+// first `sink` and last `local` pages get the largest key, so they are always kept.
 template <int NT, bool kNamed>
-__device__ void topk_row(const float* row, int N, int K, int* idx_out, int* count_out,
-                         const TopkSmem& t, int* scratch) {
+__device__ void topk_row(const float* row, int N, int K, int sink, int local, int* idx_out,
+                         int* count_out, const TopkSmem& t, int* scratch) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = NT / 32;
   if (N <= K) {
@@ -622,7 +623,8 @@ __device__ void topk_row(const float* row, int N, int K, int* idx_out, int* coun
     for (int u = 0; u < 16; ++u) {
       const int i = (r0 + u) * NT + tid;
       if (i < N) {
-        const uint32_t k = score_key(v[u]);
+        const bool forced = N > K && (i < sink || i >= N - local);
+        const uint32_t k = forced ? 0xffffffffu : score_key(v[u]);
         t.keys[i] = k;
         lo = min(lo, k);
         hi = max(hi, k);

@@ -443,7 +443,8 @@ __device__ void consume_score(const Params& p, const FusedSmem& s, const ItemDes
   if (tid == 0) trace(p, kEvArrived, d.bg);
   if (last) {
     if (tid == 0) trace(p, kEvTopkBegin, d.bg);
-    topk_row<kConsumerThreads, true>(row, d.N, p.top_k, p.sel_idx + (size_t)d.bg * p.top_k,
+    topk_row<kConsumerThreads, true>(row, d.N, p.top_k, p.sink_pages, p.local_pages,
+                                     p.sel_idx + (size_t)d.bg * p.top_k,
                                         p.sel_count + d.bg, topk_smem_at(s.topk, p.max_pages),
                                         s.scratch);
     bsync<kConsumerThreads, true>();  // every thread's selection writes precede the release

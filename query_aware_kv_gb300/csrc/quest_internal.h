@@ -72,6 +72,7 @@ struct Params {
   int* sel_idx;          // [B][Hkv][top_k]
   int* sel_count;        // [B][Hkv]
   int top_k;             // row length of sel_idx (= requested K, capped at max_pages)
+  int sink_pages, local_pages;  // pages always kept at the start / end of a long sequence
 
   int score_tile_pages, n_score_tiles;
   int pps, n_splits;     // decode work-item size and count per (b, g)

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kConsumerThreads) topk_kernel(Params p) {
   const int N = (L + p.P - 1) / p.P;
   int* scratch = reinterpret_cast<int*>(sm + topk_smem_bytes(p.max_pages));
   topk_row<kConsumerThreads, false>(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
-                                    p.sel_idx + (size_t)bg * p.top_k, p.sel_count + bg,
+                                    p.sink_pages, p.local_pages, p.sel_idx + (size_t)bg * p.top_k, p.sel_count + bg,
                                     topk_smem_at(sm, p.max_pages), scratch);
 }
 

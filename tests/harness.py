@@ -143,7 +143,7 @@ def oracle_selection_arrays(gpu_idx: np.ndarray, gpu_cnt: np.ndarray):
 
 def run_step_and_compare(pair: Pair, step: int, top_k: int, opts=None, fused: bool = True,
                          check_needles: bool = False, one_launch: bool = False,
-                         check_cache: bool = False) -> int:
+                         check_cache: bool = False, sink: int = 0, local: int = 0) -> int:
     """One decode step on both sides (append + score + select + attend); compares
     scores (unfused only), selection and attention; with check_cache also the boxes,
     pools and lengths.  one_launch: quest_decode_step (append folded into the fused
@@ -157,7 +157,7 @@ def run_step_and_compare(pair: Pair, step: int, top_k: int, opts=None, fused: bo
     oracle.append(pair.ref, w.k_new[step].cpu().numpy(), w.v_new[step].cpu().numpy())
     qh = w.q[step].cpu().numpy().astype(np.float32)
     ref_scores = oracle.score(pair.ref, qh)
-    ref_idx, ref_cnt = oracle.topk(pair.ref, ref_scores, top_k)
+    ref_idx, ref_cnt = oracle.topk(pair.ref, ref_scores, top_k, sink, local)
     if one_launch:
         idx = torch.empty((w.batch, w.num_kv_heads, top_k), dtype=torch.int32, device="cuda")
         cnt = torch.empty((w.batch, w.num_kv_heads), dtype=torch.int32, device="cuda")
@@ -170,7 +170,7 @@ def run_step_and_compare(pair: Pair, step: int, top_k: int, opts=None, fused: bo
     else:
         scores = q.estimate(pair.cache, qd, pair.ws)
         assert_scores_close(scores.cpu().numpy(), ref_scores, score_tolerance(pair.ref, qh))
-        idx, cnt = q.topk(pair.cache, scores, top_k, pair.ws)
+        idx, cnt = q.topk(pair.cache, scores, top_k, pair.ws, opts)
         out, lse = q.sparse_decode(pair.cache, qd, idx, cnt, top_k, pair.ws, opts)
     assert_status_ok(pair.ws)
     assert pair.cache.seq_lens.cpu().numpy().tolist() == pair.ref.seq_lens.tolist()

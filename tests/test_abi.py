@@ -86,8 +86,16 @@ def test_calls_reject_bad_arguments_without_launching(lib):
     assert lib.quest_estimate(ctypes.byref(d), 18, 16, 256, 1 << 20, None) == \
         q.QUEST_ERR_INVALID_ARG
     # top_k out of range
-    assert lib.quest_topk(ctypes.byref(d), 16, 0, 16, 16, 256, 1 << 20, None) == \
+    assert lib.quest_topk(ctypes.byref(d), 16, 0, 16, 16, 256, 1 << 20, None, None) == \
         q.QUEST_ERR_INVALID_ARG
+    # a sink / local window larger than the budget, or negative
+    for sink, local in ((3, 2), (-1, 0), (0, -2)):
+        o = q.opts(sink_pages=sink, local_pages=local)
+        assert lib.quest_topk(ctypes.byref(d), 16, 4, 16, 16, 256, 1 << 20, ctypes.byref(o),
+                              None) == q.QUEST_ERR_INVALID_ARG
+        assert lib.quest_decode(ctypes.byref(d), 16, 4, 16, None, None, None, 256, 1 << 20,
+                                ctypes.byref(o), None) == q.QUEST_ERR_INVALID_ARG
+        assert "sink_pages" in lib.quest_last_error().decode()
     # unsupported geometry
     d2 = desc(page_size=64)
     assert lib.quest_build_meta(ctypes.byref(d2), 256, 1 << 20, None) == q.QUEST_ERR_UNSUPPORTED

@@ -140,6 +140,43 @@ def test_topk_near_ties_over_a_wide_range():
     H.assert_status_ok(pair.ws)
 
 
+@pytest.mark.parametrize("sink,local", [(2, 2), (0, 3), (4, 0), (8, 8)])
+def test_topk_sink_and_local_pages(sink, local):
+    """[Guide] Solution step 3 / Implementation step 2: the first `sink` and last `local`
+    pages of a long sequence are always kept, the rest of the budget goes to the best of
+    the others; short sequences keep everything."""
+    w = small(lens=(16 * 300 - 7, 16 * 12, 16 * 64), batch=3, hq=4, hkv=2)
+    pair = H.on_device(w, build_meta=False)
+    rng = np.random.default_rng(sink * 10 + local)
+    scores = np.full((3, 2, w.block_table.shape[1]), -np.inf, np.float32)
+    for b, L in enumerate((16 * 300 - 7, 16 * 12, 16 * 64)):
+        n = wl.pages_for(L, 16)
+        scores[b, :, :n] = rng.standard_normal((2, n)).astype(np.float32)
+        scores[b, 1, :n] = np.round(scores[b, 1, :n])          # exact ties
+        scores[b, 0, n - 1] = -50.0                              # a weak last page
+    for K in (16, 40):
+        o = q.opts(sink_pages=sink, local_pages=local)
+        idx, cnt = q.topk(pair.cache, torch.from_numpy(scores).cuda(), K, pair.ws, o)
+        ri, rc = oracle.topk(pair.ref, scores, K, sink, local)
+        gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+        assert np.array_equal(gc, rc)
+        for b in range(3):
+            for g in range(2):
+                assert gi[b, g, :gc[b, g]].tolist() == sorted(ri[b, g, :rc[b, g]].tolist())
+    H.assert_status_ok(pair.ws)
+
+
+@pytest.mark.parametrize("cs", [0, 1, 8])
+def test_fused_step_with_sink_and_local_pages(cs):
+    w = small(lens=(2500, 1, 700, 16 * 9), batch=4, steps=2, hq=8, hkv=4, budget=256,
+              outliers=4)
+    pair = H.on_device(w)
+    o = q.opts(cluster_size=cs, sink_pages=2, local_pages=2)
+    for t in range(w.steps):
+        H.run_step_and_compare(pair, t, w.top_k, opts=o, one_launch=True, sink=2, local=2,
+                               check_cache=(t == w.steps - 1))
+
+
 def test_topk_at_max_pages():
     """The largest supported row: 16384 pages."""
     n = q.QUEST_MAX_PAGES

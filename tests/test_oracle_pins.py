@@ -273,6 +273,50 @@ def test_topk_keeps_everything_when_short():
     assert idx[0, 0, :3].tolist() == [0, 1, 2] and np.all(idx[0, 0, 3:] == -1)
 
 
+def test_topk_window_keeps_sinks_and_local_pages():
+    """[Guide] Solution step 3 / Implementation step 2: the first `sink` and last `local`
+    pages are always kept; the other K - sink - local pages are the best of the rest, by
+    brute force; a sequence of at most K pages keeps everything."""
+    rng = np.random.default_rng(9)
+    w, c = make(lens=(16 * 60, 16 * 7, 16 * 30 - 5), batch=3)
+    n = [wl.pages_for(int(L), 16) for L in c.seq_lens]
+    scores = np.full((3, 4, c.block_table.shape[1]), -np.inf, np.float32)
+    for b in range(3):
+        scores[b, :, :n[b]] = rng.standard_normal((4, n[b])).astype(np.float32)
+        scores[b, 0, :n[b]] = np.round(scores[b, 0, :n[b]])  # ties
+    scores[0, 1, :2] = 100.0  # a sink that would win anyway
+    for K, sink, local in [(16, 2, 2), (16, 0, 3), (16, 4, 0), (10, 5, 5), (9, 0, 0)]:
+        idx, cnt = oracle.topk(c, scores, K, sink, local)
+        for b in range(3):
+            for g in range(4):
+                got = idx[b, g, :cnt[b, g]].tolist()
+                if n[b] <= K:
+                    assert sorted(got) == list(range(n[b]))
+                    continue
+                mand = list(range(sink)) + list(range(n[b] - local, n[b]))
+                rest = sorted(range(sink, n[b] - local), key=lambda p: (-float(scores[b, g, p]), p))
+                assert got == mand + rest[:K - sink - local]
+                assert cnt[b, g] == K and len(set(got)) == K
+                assert np.all(idx[b, g, K:] == -1)
+
+
+def test_topk_window_zero_is_plain_topk_and_local_zero_keeps_no_tail():
+    rng = np.random.default_rng(10)
+    w, c = make(lens=(16 * 50,), batch=1)
+    scores = np.full((1, 4, c.block_table.shape[1]), -np.inf, np.float32)
+    scores[0, :, :50] = rng.standard_normal((4, 50)).astype(np.float32)
+    scores[0, :, 49] = 1e6  # the last page: kept on merit only
+    a, _ = oracle.topk(c, scores, 8)
+    b, _ = oracle.topk(c, scores, 8, 0, 0)
+    assert np.array_equal(a, b)
+    idx, cnt = oracle.topk(c, scores, 8, 3, 0)
+    for g in range(4):
+        got = idx[0, g, :8].tolist()
+        assert got[:3] == [0, 1, 2] and 49 in got  # no page is masked by local = 0
+    with pytest.raises(oracle.OracleError):
+        oracle.topk(c, scores, 4, 3, 2)  # the window does not fit the budget
+
+
 def test_planted_needles_are_selected():
     """[Guide] Evaluation: a page holding a key aligned with the query gets an elevated
     bound and is kept by the top-K."""
