@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--pages-per-split", type=int, default=0)
     ap.add_argument("--score-tile-pages", type=int, default=0)
     ap.add_argument("--trace", default="", help="write a fused-kernel timeline (npy) here")
+    ap.add_argument("--sweep", action="store_true",
+                    help="measure every workload (one JSON line each) instead of the step")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="N",
                     help="profiling run for ncu: set up, --warmup steps, then N quest_decode "
                          "launches; no L2 flush buffer, no timing, no JSON line")
@@ -60,8 +62,8 @@ def peaks():
 # algorithmic bytes (what the step must move): metadata of every page of every head,
 # the K and V rows of every valid token of every selected page, q in, out + lse out.
 # ------------------------------------------------------------------------------------
-def decode_bytes(seq_lens, counts_tokens, B, Hq, Hkv, d=128):
-    meta = sum(math.ceil(L / PAGE) for L in seq_lens) * Hkv * 2 * d * 2
+def decode_bytes(seq_lens, counts_tokens, B, Hq, Hkv, d=128, page=PAGE):
+    meta = sum(math.ceil(L / page) for L in seq_lens) * Hkv * 2 * d * 2
     kv = counts_tokens * 2 * d * 2
     qo = B * Hq * d * 2 * 2 + B * Hq * 4
     return meta + kv + qo
@@ -72,7 +74,7 @@ def append_bytes(B, Hkv, d=128):
     return B * Hkv * d * 2 * (2 + 2 + 4)
 
 
-def selected_tokens(idx, cnt, seq_lens):
+def selected_tokens(idx, cnt, seq_lens, page=PAGE):
     import numpy as np
     idx = idx.cpu().numpy()
     cnt = cnt.cpu().numpy()
@@ -81,7 +83,7 @@ def selected_tokens(idx, cnt, seq_lens):
         L = int(seq_lens[b])
         for g in range(idx.shape[1]):
             for p in idx[b, g, :cnt[b, g]]:
-                total += min(PAGE, L - int(p) * PAGE)
+                total += min(page, L - int(p) * page)
     return total
 
 
@@ -448,6 +450,103 @@ def run_quest(args):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """quest_decode (fused, kernel only), the unfused estimate + top-K + sparse-decode chain,
+    quest_append and quest_dense_decode on every workload, L2 flushed before each timed
+    launch; one JSON line per workload (not the benchmark's contract line)."""
+    import torch
+
+    import query_aware_kv_gb300 as q
+    from query_aware_kv_gb300 import build as cuda_build
+    from query_aware_kv_gb300 import workloads as wl
+
+    cuda_build.build()
+    q.load()
+    dev = torch.device("cuda")
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sum = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush_buf.zero_()
+        torch.sum(flush_buf[: FLUSH_BYTES // 2].view(torch.int64), dim=0, out=flush_sum)
+
+    def timed(fn, reps):
+        es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for _ in range(3):
+            fn()
+        for a, b in es:
+            flush_l2()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(1e3 * a.elapsed_time(b) for a, b in es) / reps
+
+    peak, _ = peaks()
+    cases = [("tiny", lambda: wl.tiny(seed=0, device=dev))]
+    cases.append(("longchat_32k", lambda: wl.longchat_32k(seed=0, device=dev, steps=4)))
+    for budget in (256, 512, 1024, 2048, 4096):
+        cases.append((f"batched_ragged_budget{budget}",
+                      lambda budget=budget: wl.batched_ragged(seed=0, device=dev, budget=budget,
+                                                              steps=1)))
+    for budget in (1024, 2048):
+        cases.append((f"yarn_128k_layer0_budget{budget}",
+                      lambda budget=budget: wl.yarn_128k_layer(0, seed=0, device=dev,
+                                                               budget=budget)))
+    for page in (16, 32):
+        cases.append((f"gqa_llama31_p{page}",
+                      lambda page=page: wl.gqa_llama31(seed=0, device=dev, page_size=page)))
+    for name, make in cases:
+        w = make()
+        cache = q.PagedCache.allocate_meta(w.k_pool, w.v_pool, w.block_table, w.seq_lens.clone(),
+                                           w.num_q_heads)
+        K = w.top_k
+        ws = q.workspace(cache, K)
+        q.build_meta(cache, ws)
+        B, Hq, Hkv, P = w.batch, w.num_q_heads, w.num_kv_heads, w.page_size
+        out = torch.empty((B, Hq, 128), dtype=torch.float16, device=dev)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        idx = torch.empty((B, Hkv, K), dtype=torch.int32, device=dev)
+        cnt = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
+        qv = w.q[0]
+        reps = 64 if name != "tiny" else 256
+        fused = timed(lambda: q.decode(cache, qv, K, ws, out=out, lse=lse, idx_out=idx,
+                                       count_out=cnt), reps)
+        L = [int(x) for x in cache.seq_lens.cpu().tolist()]
+        tok = selected_tokens(idx, cnt, L, P)
+        nbytes = decode_bytes(L, tok, B, Hq, Hkv, page=P)
+        scores = torch.empty((B, Hkv, cache.max_pages), dtype=torch.float32, device=dev)
+
+        def chain():
+            q.estimate(cache, qv, ws, scores=scores)
+            i2, c2 = q.topk(cache, scores, K, ws)
+            q.sparse_decode(cache, qv, i2, c2, K, ws, out=out, lse=lse)
+
+        chain_us = timed(chain, reps)
+        dense_us = timed(lambda: q.dense_decode(cache, qv, ws, out=out, lse=lse), max(8, reps // 4))
+        snap_meta, snap_len = cache.meta.clone(), cache.seq_lens.clone()
+
+        def append_once():
+            q.append(cache, w.k_new[0], w.v_new[0], ws)
+            cache.seq_lens.copy_(snap_len)
+
+        append_us = timed(append_once, reps)
+        cache.meta.copy_(snap_meta)
+        rc, detail = q.read_status(ws)
+        gbs = nbytes / (fused * 1e-6) / 1e9
+        print(json.dumps({
+            "workload": name, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv,
+            "page_size": P, "top_k_pages": K, "seq_lens_mean": round(sum(L) / len(L), 1),
+            "quest_decode_us": round(fused, 2), "algorithmic_bytes": nbytes,
+            "gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+            "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
+            "unfused_chain_us": round(chain_us, 2), "append_plus_len_reset_us": round(append_us, 2),
+            "dense_decode_us": round(dense_us, 2), "status": rc}), flush=True)
+        del w, cache, ws, scores
+        torch.cuda.empty_cache()
+
+
 def profiled_traffic():
     """DRAM bytes per quest_decode launch from the committed ncu summary, if it was taken
     on the current kernel sources (else null)."""
@@ -471,6 +570,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_quest(args)
 
