@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--pages-per-split", type=int, default=0)
     ap.add_argument("--score-tile-pages", type=int, default=0)
     ap.add_argument("--trace", default="", help="write a fused-kernel timeline (npy) here")
+    ap.add_argument("--layers", action="store_true",
+                    help="time the 32-layer 128K step in one launch against one launch per layer")
     ap.add_argument("--sweep", action="store_true",
                     help="measure every workload (one JSON line each) instead of the step")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="N",
@@ -547,6 +549,74 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_layers(args):
+    """All 32 layers of the 128K-context model in one quest_decode_layers launch against 32
+    quest_decode launches, L2 flushed before each timed step; one JSON line."""
+    import torch
+
+    import query_aware_kv_gb300 as q
+    from query_aware_kv_gb300 import build as cuda_build
+    from query_aware_kv_gb300 import workloads as wl
+
+    cuda_build.build()
+    q.load()
+    dev = torch.device("cuda")
+    n_layers = 32
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sum = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush_buf.zero_()
+        torch.sum(flush_buf[: FLUSH_BYTES // 2].view(torch.int64), dim=0, out=flush_sum)
+
+    ws_ = [wl.yarn_128k_layer(i, seed=0, device=dev, budget=2048) for i in range(n_layers)]
+    w0 = ws_[0]
+    K = w0.top_k
+    base = q.PagedCache.allocate_meta(w0.k_pool, w0.v_pool, w0.block_table, w0.seq_lens.clone(),
+                                      w0.num_q_heads)
+    layers = [base] + [q.PagedCache.allocate_meta(w.k_pool, w.v_pool, base.block_table,
+                                                   base.seq_lens, w.num_q_heads) for w in ws_[1:]]
+    ws = q.workspace(base, K)
+    for lay in layers:
+        q.build_meta(lay, ws)
+    qs = [w.q[0] for w in ws_]
+    outs = [torch.empty((1, 32, 128), dtype=torch.float16, device=dev) for _ in range(n_layers)]
+    lses = [torch.empty((1, 32), dtype=torch.float32, device=dev) for _ in range(n_layers)]
+
+    def one_launch():
+        q.decode_layers(base, layers, qs, K, ws, out=outs, lse=lses)
+
+    def per_layer():
+        for i, lay in enumerate(layers):
+            q.decode(lay, qs[i], K, ws, out=outs[i], lse=lses[i])
+
+    def timed(fn, reps=16):
+        es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for _ in range(3):
+            fn()
+        for a, b in es:
+            flush_l2()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(1e3 * a.elapsed_time(b) for a, b in es) / reps
+
+    fused_us = timed(one_launch)
+    per_us = timed(per_layer)
+    rc, _ = q.read_status(ws)
+    L = int(base.seq_lens[0])
+    nbytes = n_layers * decode_bytes([L], 32 * K * PAGE, 1, 32, 32)
+    peak, _ = peaks()
+    gbs = nbytes / (fused_us * 1e-6) / 1e9
+    print(json.dumps({"workload": "yarn_128k_32_layers_budget2048", "layers": n_layers,
+                      "decode_layers_us": round(fused_us, 1),
+                      "decode_per_layer_launches_us": round(per_us, 1),
+                      "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
+                      "frac_of_measured": round(gbs / peak, 4), "status": rc}), flush=True)
+
+
 def profiled_traffic():
     """DRAM bytes per quest_decode launch from the committed ncu summary, if it was taken
     on the current kernel sources (else null)."""
@@ -572,6 +642,8 @@ def main():
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.layers:
+        run_layers(args)
     else:
         run_quest(args)
 

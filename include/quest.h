@@ -231,6 +231,35 @@ int quest_decode_step(const quest_cache_t* cache, const void* q, const void* k_n
                       quest_stream_t stream);
 
 /*
+ * Every layer of one decode step in one launch.  [Guide] Evaluation (end-to-end latency
+ * table): a whole token step runs the sparse decode in every layer, which is where the
+ * end-to-end gains are measured.  The same fused step as quest_decode_step (or
+ * quest_decode when k_new is NULL) for n_layers layers that share the batch, the block
+ * table and the lengths, each with its own K/V pools, boxes, query, new token and output.  The (layer, sequence, kv head) pairs are
+ * the work units of one persistent launch, so one pair's selection overlaps other pairs'
+ * streaming.  cache: the shared shape, block_table and seq_lens (its k_pool / v_pool / meta
+ * are not used).  layers: host array of n_layers (1..QUEST_MAX_LAYERS) quest_layer_t, read
+ * during the call only; pointers as in quest_decode_step.  k_new / v_new: given for every
+ * layer (each layer appends at slot seq_len[b]; seq_lens advance once, at the end) or for
+ * none.  No idx_out.  ws: as quest_decode for this cache and top_k.
+ */
+#define QUEST_MAX_LAYERS 32
+typedef struct {
+    void* k_pool;        /* fp16 [num_phys][num_kv_heads][page_size][128] */
+    void* v_pool;
+    void* meta;          /* fp16 [batch][num_kv_heads][max_pages][2][128] */
+    const void* q;       /* fp16 [batch][num_q_heads][128] */
+    const void* k_new;   /* fp16 [batch][num_kv_heads][128] or NULL */
+    const void* v_new;
+    void* out;           /* fp16 [batch][num_q_heads][128] */
+    float* lse;          /* fp32 [batch][num_q_heads] or NULL */
+} quest_layer_t;
+
+int quest_decode_layers(const quest_cache_t* cache, const quest_layer_t* layers, int32_t n_layers,
+                        int32_t top_k, void* ws, size_t ws_bytes, const quest_opts_t* opts,
+                        quest_stream_t stream);
+
+/*
  * Full-context attention over every token (every page kept): the library's own dense
  * baseline ([Summary] Key points compare Quest's attention with a dense kernel).
  */

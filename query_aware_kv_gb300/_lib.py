@@ -13,7 +13,7 @@ import ctypes
 import os
 import threading
 from dataclasses import dataclass
-from typing import Optional, Tuple
+from typing import Sequence, Optional, Tuple
 
 import torch
 
@@ -37,7 +37,7 @@ HEAD_DIM = 128
 # Every symbol include/quest.h declares.
 EXPORTS = (
     "quest_workspace_size", "quest_workspace_init", "quest_build_meta", "quest_append",
-    "quest_estimate", "quest_topk", "quest_sparse_decode", "quest_decode",
+    "quest_estimate", "quest_topk", "quest_sparse_decode", "quest_decode", "quest_decode_layers",
     "quest_decode_step", "quest_dense_decode", "quest_decode_static", "quest_read_status",
     "quest_last_error", "quest_status_string", "quest_version",
 )
@@ -58,6 +58,11 @@ class QuestCacheDesc(ctypes.Structure):
         ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("meta", ctypes.c_void_p),
         ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
     ]
+
+
+class QuestLayer(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("k_pool", "v_pool", "meta", "q", "k_new", "v_new", "out", "lse")]
 
 
 class QuestOpts(ctypes.Structure):
@@ -99,6 +104,8 @@ def load() -> ctypes.CDLL:
             "quest_sparse_decode": (ctypes.c_int, [C, V, V, V, I32, V, V, V, SZ, O, V]),
             "quest_decode": (ctypes.c_int, [C, V, I32, V, V, V, V, V, SZ, O, V]),
             "quest_decode_step": (ctypes.c_int, [C, V, V, V, I32, V, V, V, V, V, SZ, O, V]),
+            "quest_decode_layers": (ctypes.c_int, [C, ctypes.POINTER(QuestLayer), I32, I32, V,
+                                                   SZ, O, V]),
             "quest_dense_decode": (ctypes.c_int, [C, V, V, V, V, SZ, O, V]),
             "quest_read_status": (ctypes.c_int, [V, SZ, V, ctypes.POINTER(I32)]),
             "quest_last_error": (ctypes.c_char_p, []),
@@ -332,6 +339,40 @@ def decode_step(cache: PagedCache, q: torch.Tensor, k_new: torch.Tensor, v_new: 
                                     _ptr(idx_out), _ptr(count_out), ws.data_ptr(), ws.numel(),
                                     _opts_ref(o), _stream(stream)))
     return out, lse
+
+
+def decode_layers(cache: PagedCache, layers: Sequence[PagedCache], q: Sequence[torch.Tensor],
+                  top_k: int, ws: torch.Tensor, o: Optional[QuestOpts] = None,
+                  k_new: Optional[Sequence[torch.Tensor]] = None,
+                  v_new: Optional[Sequence[torch.Tensor]] = None, out=None, lse=None,
+                  want_lse: bool = True, stream=None):
+    """The fused step of every layer in one launch.  `cache` holds the shared shape, block
+    table and lengths; `layers[i]` holds layer i's pools and boxes (same shape); with
+    k_new / v_new every layer appends its token and the lengths advance once."""
+    n = len(layers)
+    if len(q) != n or (k_new is not None and (len(k_new) != n or len(v_new) != n)):
+        raise ValueError("one q (and k_new, v_new) per layer")
+    outs = list(out) if out is not None else [None] * n
+    lses = list(lse) if lse is not None else [None] * n
+    arr = (QuestLayer * max(n, 1))()
+    keep = []
+    for i, lay in enumerate(layers):
+        if (lay.k_pool.shape != cache.k_pool.shape or lay.meta.shape != cache.meta.shape):
+            raise ValueError(f"layer {i}: pools / boxes differ in shape from the cache")
+        _need(q[i], "q", torch.float16, (cache.batch, cache.desc.num_q_heads, HEAD_DIM))
+        outs[i], lses[i] = _out(cache, q[i], outs[i], lses[i], want_lse)
+        kn = vn = None
+        if k_new is not None:
+            shape = (cache.batch, cache.num_kv_heads, HEAD_DIM)
+            _need(k_new[i], "k_new", torch.float16, shape)
+            _need(v_new[i], "v_new", torch.float16, shape)
+            kn, vn = k_new[i].data_ptr(), v_new[i].data_ptr()
+        arr[i] = QuestLayer(lay.k_pool.data_ptr(), lay.v_pool.data_ptr(), lay.meta.data_ptr(),
+                            q[i].data_ptr(), kn, vn, outs[i].data_ptr(), _ptr(lses[i]))
+    keep.append(arr)
+    _check(load().quest_decode_layers(ctypes.byref(cache.desc), arr, int(n), int(top_k),
+                                      ws.data_ptr(), ws.numel(), _opts_ref(o), _stream(stream)))
+    return outs, lses
 
 
 def dense_decode(cache: PagedCache, q: torch.Tensor, ws: torch.Tensor,

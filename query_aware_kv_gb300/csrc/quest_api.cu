@@ -365,7 +365,10 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
                 cs);
   p.sel_idx = idx_out;     // the cluster kernel writes the selection only when asked
   p.sel_count = count_out;
-  return launched(launch_cluster(p, group_of(cache), cs, opts ? opts->max_ctas : 0,
+  LayerTable lt{};
+  lt.n = 1;
+  lt.l[0] = LayerPtrs{p.k_pool, p.v_pool, p.meta, p.q, p.k_new, p.v_new, p.out, p.lse};
+  return launched(launch_cluster(p, lt, group_of(cache), cs, opts ? opts->max_ctas : 0,
                                  static_cast<cudaStream_t>(stream)),
                   what);
 }
@@ -385,6 +388,71 @@ int quest_decode_step(const quest_cache_t* cache, const void* q, const void* k_n
     return fail(QUEST_ERR_INVALID_ARG, "quest_decode_step needs k_new and v_new");
   return decode_impl(cache, q, k_new, v_new, top_k, out, lse, idx_out, count_out, ws, ws_bytes,
                      opts, stream, "quest_decode_step");
+}
+
+static_assert(kMaxLayers == QUEST_MAX_LAYERS, "layer table size");
+
+int quest_decode_layers(const quest_cache_t* cache, const quest_layer_t* layers, int32_t n_layers,
+                        int32_t top_k, void* ws, size_t ws_bytes, const quest_opts_t* opts,
+                        quest_stream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if ((rc = check_topk(top_k))) return rc;
+  if ((rc = check_window(opts, top_k))) return rc;
+  if (!layers || n_layers < 1 || n_layers > QUEST_MAX_LAYERS)
+    return fail(QUEST_ERR_INVALID_ARG, "n_layers %d: use 1..%d layers", n_layers, QUEST_MAX_LAYERS);
+  if (cache->batch == 0) return QUEST_OK;
+  if ((long long)n_layers * cache->batch * cache->num_kv_heads > 0x7fffffffLL)
+    return fail(QUEST_ERR_UNSUPPORTED, "too many (layer, sequence, kv head) pairs");
+  const bool append = layers[0].k_new != nullptr;
+  LayerTable lt{};
+  lt.n = n_layers;
+  for (int i = 0; i < n_layers; ++i) {
+    const quest_layer_t& L = layers[i];
+    if (!L.k_pool || !L.v_pool || !L.meta || !L.q || !L.out || !aligned(L.k_pool, 16) ||
+        !aligned(L.v_pool, 16) || !aligned(L.meta, 16) || !aligned(L.q, 16) ||
+        !aligned(L.out, 16) || !aligned(L.lse, 4))
+      return fail(QUEST_ERR_INVALID_ARG, "layer %d: pools, boxes, q and out must be non-NULL "
+                  "and 16-byte aligned", i);
+    if ((L.k_new != nullptr) != append || (L.v_new != nullptr) != append ||
+        !aligned(L.k_new, 16) || !aligned(L.v_new, 16))
+      return fail(QUEST_ERR_INVALID_ARG, "layer %d: k_new / v_new must be given (16-byte "
+                  "aligned) for every layer or for none", i);
+    lt.l[i] = LayerPtrs{static_cast<__half*>(L.k_pool), static_cast<__half*>(L.v_pool),
+                        static_cast<__half*>(L.meta), static_cast<const __half*>(L.q),
+                        static_cast<const __half*>(L.k_new), static_cast<const __half*>(L.v_new),
+                        static_cast<__half*>(L.out), L.lse};
+  }
+  const Tiling t = make_tiling(cache, top_k, opts);
+  const WsLayout Lw = make_layout(cache, t);
+  if ((rc = check_ws(ws, ws_bytes, Lw.total))) return rc;
+  Params p = make_params(cache, ws, Lw, t, opts);
+  p.top_k = top_k;
+  p.dense = 0;
+  p.q = lt.l[0].q;
+  p.out = lt.l[0].out;
+  p.lse = lt.l[0].lse;
+  p.k_new = lt.l[0].k_new;  // non-NULL: every layer appends, lengths advance once
+  p.v_new = lt.l[0].v_new;
+  p.sel_idx = nullptr;
+  p.sel_count = nullptr;
+  p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
+  p.trace_capacity = opts ? opts->trace_capacity : 0;
+  const int cs = opts ? opts->cluster_size : 0;
+  if (cs < 0 || cs > kMaxClusterSize)
+    return fail(QUEST_ERR_INVALID_ARG, "cluster_size %d: use 0 (automatic) or 1..%d", cs,
+                kMaxClusterSize);
+  if (!cluster_any_fits(group_of(cache), cache->page_size, cache->max_pages, top_k))
+    return fail(QUEST_ERR_UNSUPPORTED, "max_pages %d needs more shared memory than a CTA has",
+                cache->max_pages);
+  if (cs > 0 &&
+      cluster_smem_bytes(group_of(cache), cache->page_size, cache->max_pages, cs, top_k) >
+          kMaxSmem)
+    return fail(QUEST_ERR_UNSUPPORTED, "cluster_size %d needs more shared memory than a CTA has",
+                cs);
+  return launched(launch_cluster(p, lt, group_of(cache), cs, opts ? opts->max_ctas : 0,
+                                 static_cast<cudaStream_t>(stream)),
+                  "quest_decode_layers");
 }
 
 int quest_dense_decode(const quest_cache_t* cache, const void* q, void* out, float* lse, void* ws,

@@ -247,7 +247,7 @@ struct Role {
   int cid, ncl, nbg, npairs;
 };
 
-__device__ __forceinline__ Role make_role(const Params& p, int cs) {
+__device__ __forceinline__ Role make_role(const Params& p, int cs, int n_layers) {
   Role r;
   r.rank = (int)cta_rank();
   r.cs = cs;
@@ -256,12 +256,13 @@ __device__ __forceinline__ Role make_role(const Params& p, int cs) {
   r.si = r.rank;
   r.cid = (int)cluster_index();
   r.ncl = (int)cluster_count();
-  r.nbg = p.B * p.Hkv;
+  r.nbg = n_layers * p.B * p.Hkv;
   r.npairs = r.cid < r.nbg ? (r.nbg - 1 - r.cid) / r.ncl + 1 : 0;
   return r;
 }
 
 struct Pair {
+  const LayerPtrs* lay;    // this pair's layer: pools, boxes, q, new token, output
   int b, g, L, N, count;
   int p_lo, p_hi;          // this streamer's scoring share
   int q_lo, q_hi;          // this streamer's decode share (ranks of the selection)
@@ -269,9 +270,13 @@ struct Pair {
   int append_page;         // page receiving the appended token, or -1
 };
 
-__device__ __forceinline__ Pair pair_geometry(const Params& p, const CSmem& s, const Role& r, int j) {
+__device__ __forceinline__ Pair pair_geometry(const Params& p, const LayerTable& lt,
+                                              const CSmem& s, const Role& r, int j) {
   Pair q;
-  const int bg = r.cid + j * r.ncl;
+  const int pair = r.cid + j * r.ncl;  // layer-major over (layer, sequence, kv head)
+  const int nbg1 = p.B * p.Hkv;
+  const int layer = pair / nbg1, bg = pair - layer * nbg1;
+  q.lay = &lt.l[layer];
   q.b = bg / p.Hkv;
   q.g = bg % p.Hkv;
   q.buf = j & 1;
@@ -309,7 +314,7 @@ __device__ void c_produce_score(const Params& p, const CSmem& s, const Pair& q, 
   // contiguous boxes, one bulk copy per stage
   const int n_live = q.p_hi - q.p_lo;
   if (lane == 0) {
-    const __half* box0 = p.meta + box_offset(p, q.b, q.g, q.p_lo);
+    const __half* box0 = q.lay->meta + box_offset(p, q.b, q.g, q.p_lo);
     for (int u0 = 0; u0 < n_live; u0 += kSP) {
       const uint32_t kk = stage_seq + (uint32_t)(u0 / kSP);
       const int st = (int)(kk % kStages);
@@ -380,8 +385,8 @@ __device__ void c_produce_decode(const Params& p, const CSmem& s, const Pair& q,
         } else {
           nv = min(P, q.L - lp * P);
           const size_t off = ((size_t)phys * p.Hkv + q.g) * chunk_elems;
-          ksrc = p.k_pool + off;
-          vsrc = p.v_pool + off;
+          ksrc = q.lay->k_pool + off;
+          vsrc = q.lay->v_pool + off;
         }
       }
     }
@@ -430,14 +435,14 @@ __device__ __forceinline__ int task_at(const Role& r, bool producer, int t, int*
 }
 
 template <int G, int P>
-__device__ void c_produce(const Params& p, const CSmem& s, const Role& r) {
+__device__ void c_produce(const Params& p, const LayerTable& lt, const CSmem& s, const Role& r) {
   uint32_t stage_seq = 0;
   int pslot = kProducerSlot0;
   const int n = task_count(r, true);
   for (int t = 0; t < n; ++t) {
     int j;
     const int kind = task_at(r, true, t, &j);
-    const Pair q = pair_geometry(p, s, r, j);
+    const Pair q = pair_geometry(p, lt, s, r, j);
     if (kind == kTaskScore)
       c_produce_score<G, P>(p, s, q, stage_seq, &pslot);
     else
@@ -472,15 +477,15 @@ __device__ void c_score_share(const Params& p, const CSmem& s, const Role& r, co
   uint32_t* kout = r.selector ? s.keys + (size_t)q.buf * keys_stride(p.max_pages) + q.p_lo : s.mykeys;
   uint32_t lo = 0xffffffffu, hi = 0u;
   QueryFrag<G> f;
-  load_query_frag<G>(p, q.b, q.g, c, f);
+  load_query_frag<G>(q.lay->q, p.Hq, q.b, q.g, c, f);
   uint4 knew = make_uint4(0, 0, 0, 0), vnew = make_uint4(0, 0, 0, 0);
   const bool mine_append = q.append_page >= q.p_lo && q.append_page < q.p_hi;
   const int slot_a = (q.L - 1) % P;
   int append_phys = -1;
   if (mine_append) {
     const size_t o = ((size_t)q.b * p.Hkv + q.g) * kHeadDim + 8 * c;
-    knew = *reinterpret_cast<const uint4*>(p.k_new + o);
-    vnew = *reinterpret_cast<const uint4*>(p.v_new + o);
+    knew = *reinterpret_cast<const uint4*>(q.lay->k_new + o);
+    vnew = *reinterpret_cast<const uint4*>(q.lay->v_new + o);
     const int phys = p.block_table[(size_t)q.b * p.max_pages + q.append_page];
     append_phys = (phys >= 0 && phys < p.num_phys) ? phys : -1;
   }
@@ -524,12 +529,12 @@ __device__ void c_score_share(const Params& p, const CSmem& s, const Role& r, co
             mn = make_uint4(ra[0], ra[1], ra[2], ra[3]);
             mx = make_uint4(rz[0], rz[1], rz[2], rz[3]);
           }
-          __half* box = p.meta + box_offset(p, q.b, q.g, page);
+          __half* box = q.lay->meta + box_offset(p, q.b, q.g, page);
           *reinterpret_cast<uint4*>(box + 8 * c) = mn;
           *reinterpret_cast<uint4*>(box + kHeadDim + 8 * c) = mx;
           const size_t kv = (((size_t)append_phys * p.Hkv + q.g) * P + slot_a) * kHeadDim + 8 * c;
-          *reinterpret_cast<uint4*>(p.k_pool + kv) = knew;
-          *reinterpret_cast<uint4*>(p.v_pool + kv) = vnew;
+          *reinterpret_cast<uint4*>(q.lay->k_pool + kv) = knew;
+          *reinterpret_cast<uint4*>(q.lay->v_pool + kv) = vnew;
         } else if (c == 0) {
           report(p, QUEST_ERR_BAD_PAGE, q.b, page, kSiteAppend);
         }
@@ -644,7 +649,7 @@ __device__ void c_decode_share(const Params& p, const CSmem& s, const Role& r, c
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     const uint2 raw =
-        *reinterpret_cast<const uint2*>(p.q + ((size_t)q.b * p.Hq + q.g * G + j) * kHeadDim + 4 * lane);
+        *reinterpret_cast<const uint2*>(q.lay->q + ((size_t)q.b * p.Hq + q.g * G + j) * kHeadDim + 4 * lane);
     const float2 a = h2f(raw.x), c = h2f(raw.y);
     qf[j][0] = a.x * p.qscale;
     qf[j][1] = a.y * p.qscale;
@@ -725,9 +730,9 @@ __device__ void c_merge(const Params& p, const CSmem& s, const Role& r, const Pa
       }
     }
     const int h = q.g * G + j;
-    p.out[((size_t)q.b * p.Hq + h) * kHeadDim + i] = __float2half_rn(ls > 0.f ? acc / ls : 0.f);
-    if (i == 0 && p.lse)
-      p.lse[(size_t)q.b * p.Hq + h] =
+    q.lay->out[((size_t)q.b * p.Hq + h) * kHeadDim + i] = __float2half_rn(ls > 0.f ? acc / ls : 0.f);
+    if (i == 0 && q.lay->lse)
+      q.lay->lse[(size_t)q.b * p.Hq + h] =
           ls > 0.f ? (Mx + log2f(ls)) * 0.69314718055994531f : -CUDART_INF_F;
   }
 }
@@ -796,14 +801,14 @@ __device__ void c_stream_decode(const Params& p, const CSmem& s, const Role& r, 
 }
 
 template <int G, int P>
-__device__ void c_consume(const Params& p, const CSmem& s, const Role& r) {
+__device__ void c_consume(const Params& p, const LayerTable& lt, const CSmem& s, const Role& r) {
   uint32_t stage_seq = 0;
   int tslot = 1;  // slot 0: the CTA's start record
   const int n = task_count(r, false);
   for (int t = 0; t < n; ++t) {
     int j;
     const int kind = task_at(r, false, t, &j);
-    const Pair q = pair_geometry(p, s, r, j);
+    const Pair q = pair_geometry(p, lt, s, r, j);
     if (kind == kTaskScore) {
       c_stream_score<G, P>(p, s, r, q, j, stage_seq, &tslot);
     } else if (kind == kTaskDecode) {
@@ -823,11 +828,11 @@ __device__ void c_consume(const Params& p, const CSmem& s, const Role& r) {
 
 template <int G, int P>
 __global__ void __launch_bounds__(kDecodeThreads, (P == 16 && G <= 4) ? 2 : 1)
-    cluster_kernel(Params p, int cs) {
+    cluster_kernel(Params p, int cs, const __grid_constant__ LayerTable lt) {
   extern __shared__ __align__(128) unsigned char smem[];
   CSmem s;
   cluster_smem_layout(G, P, p.max_pages, cs, p.top_k, &s, smem);
-  const Role r = make_role(p, cs);
+  const Role r = make_role(p, cs, lt.n);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
@@ -851,9 +856,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (P == 16 && G <= 4) ? 2 : 1)
     ctrace(p, &slot0, kCtStart, r.rank);
   }
   if (threadIdx.x >= kConsumerThreads) {
-    c_produce<G, P>(p, s, r);
+    c_produce<G, P>(p, lt, s, r);
   } else {
-    c_consume<G, P>(p, s, r);
+    c_consume<G, P>(p, lt, s, r);
   }
   __syncthreads();
   cluster_sync_all();  // no CTA leaves while another may still read its shared memory
@@ -986,8 +991,9 @@ bool cluster_any_fits(int G, int P, int max_pages, int top_k) {
   return false;
 }
 
-cudaError_t launch_cluster(const Params& p, int G, int cs, int max_clusters, cudaStream_t s) {
-  const int nbg = p.B * p.Hkv;
+cudaError_t launch_cluster(const Params& p, const LayerTable& lt, int G, int cs, int max_clusters,
+                           cudaStream_t s) {
+  const int nbg = lt.n * p.B * p.Hkv;
   cudaError_t e;
   if (cs <= 0 && (e = choose_cluster_size(G, p.P, p.max_pages, p.top_k, nbg, &cs)) != cudaSuccess)
     return e;
@@ -1005,7 +1011,8 @@ cudaError_t launch_cluster(const Params& p, int G, int cs, int max_clusters, cud
   cudaLaunchConfig_t cfg = cluster_config(cs, (int)ncl, smem, s, attr);
   Params pp = p;
   int c = cs;
-  void* args[] = {&pp, &c};
+  LayerTable tt = lt;
+  void* args[] = {&pp, &c, &tt};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

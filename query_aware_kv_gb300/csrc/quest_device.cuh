@@ -278,12 +278,12 @@ struct QueryFrag {
 };
 
 template <int G>
-__device__ __forceinline__ void load_query_frag(const Params& p, int b, int g, int c,
+__device__ __forceinline__ void load_query_frag(const __half* qry, int Hq, int b, int g, int c,
                                                 QueryFrag<G>& f) {
 #pragma unroll
   for (int j = 0; j < G; ++j) {
     const uint4 raw =
-        *reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.Hq + g * G + j) * kHeadDim + 8 * c);
+        *reinterpret_cast<const uint4*>(qry + ((size_t)b * Hq + g * G + j) * kHeadDim + 8 * c);
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -293,6 +293,12 @@ __device__ __forceinline__ void load_query_frag(const Params& p, int b, int g, i
       f.qf[j][2 * k + 1] = v.y;
     }
   }
+}
+
+template <int G>
+__device__ __forceinline__ void load_query_frag(const Params& p, int b, int g, int c,
+                                                QueryFrag<G>& f) {
+  load_query_frag<G>(p.q, p.Hq, b, g, c, f);
 }
 
 template <int G>

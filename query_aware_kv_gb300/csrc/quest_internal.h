@@ -121,6 +121,25 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
 size_t decode_smem_bytes(int G, int P, int topk_keys, int score_tile_pages);
 size_t fused_smem_bytes(int G, int P, int max_pages);
 // Raise a kernel's dynamic shared-memory cap (once per device and kernel).
+// Per-layer tensors of a multi-layer fused step (the shape, block table and lengths are
+// shared by every layer).  Passed by value as a kernel parameter.
+struct LayerPtrs {
+  __half* k_pool;
+  __half* v_pool;
+  __half* meta;
+  const __half* q;
+  const __half* k_new;
+  const __half* v_new;
+  __half* out;
+  float* lse;
+};
+constexpr int kMaxLayers = 32;
+struct LayerTable {
+  int n;
+  int pad;
+  LayerPtrs l[kMaxLayers];
+};
+
 cudaError_t ensure_smem(const void* fn, size_t bytes);
 
 // Host-side checks of quest_decode's cache / top_k arguments (status code, error text
@@ -140,7 +159,8 @@ cudaError_t launch_decode(const Params& p, int G, cudaStream_t s);
 cudaError_t launch_fused(const Params& p, int G, int max_ctas, cudaStream_t s);
 size_t cluster_smem_bytes(int G, int P, int max_pages, int cs, int top_k);
 bool cluster_any_fits(int G, int P, int max_pages, int top_k);
-cudaError_t launch_cluster(const Params& p, int G, int cs, int max_clusters, cudaStream_t s);
+cudaError_t launch_cluster(const Params& p, const LayerTable& lt, int G, int cs, int max_clusters,
+                           cudaStream_t s);
 constexpr int kMaxClusterSize = 16;
 constexpr size_t kMaxSmem = 227 * 1024;  // dynamic shared memory of one CTA
 

@@ -96,6 +96,18 @@ def test_calls_reject_bad_arguments_without_launching(lib):
         assert lib.quest_decode(ctypes.byref(d), 16, 4, 16, None, None, None, 256, 1 << 20,
                                 ctypes.byref(o), None) == q.QUEST_ERR_INVALID_ARG
         assert "sink_pages" in lib.quest_last_error().decode()
+    # multi-layer call: layer count out of range, k_new for some layers only
+    lay = (q.QuestLayer * 2)()
+    for i in range(2):
+        lay[i] = q.QuestLayer(16, 16, 16, 16, None, None, 16, None)
+    assert lib.quest_decode_layers(ctypes.byref(d), lay, 0, 4, 256, 1 << 20, None, None) == \
+        q.QUEST_ERR_INVALID_ARG
+    assert lib.quest_decode_layers(ctypes.byref(d), lay, 33, 4, 256, 1 << 20, None, None) == \
+        q.QUEST_ERR_INVALID_ARG
+    lay[1].k_new, lay[1].v_new = 16, 16
+    assert lib.quest_decode_layers(ctypes.byref(d), lay, 2, 4, 256, 1 << 20, None, None) == \
+        q.QUEST_ERR_INVALID_ARG
+    assert "k_new" in lib.quest_last_error().decode()
     # unsupported geometry
     d2 = desc(page_size=64)
     assert lib.quest_build_meta(ctypes.byref(d2), 256, 1 << 20, None) == q.QUEST_ERR_UNSUPPORTED
