@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--pages-per-split", type=int, default=0)
     ap.add_argument("--score-tile-pages", type=int, default=0)
     ap.add_argument("--trace", default="", help="write a fused-kernel timeline (npy) here")
+    ap.add_argument("--cluster-size", type=int, default=0,
+                    help="CTAs per (sequence, kv head) cluster for --sweep / --layers (0: automatic)")
     ap.add_argument("--layers", action="store_true",
                     help="time the 32-layer 128K step in one launch against one launch per layer")
     ap.add_argument("--sweep", action="store_true",
@@ -513,7 +515,8 @@ def run_sweep(args):
         cnt = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
         qv = w.q[0]
         reps = 64 if name != "tiny" else 256
-        fused = timed(lambda: q.decode(cache, qv, K, ws, out=out, lse=lse, idx_out=idx,
+        o = q.opts(cluster_size=args.cluster_size)
+        fused = timed(lambda: q.decode(cache, qv, K, ws, o, out=out, lse=lse, idx_out=idx,
                                        count_out=cnt), reps)
         L = [int(x) for x in cache.seq_lens.cpu().tolist()]
         tok = selected_tokens(idx, cnt, L, P)
@@ -538,7 +541,8 @@ def run_sweep(args):
         rc, detail = q.read_status(ws)
         gbs = nbytes / (fused * 1e-6) / 1e9
         print(json.dumps({
-            "workload": name, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv,
+            "workload": name, "cluster_size": args.cluster_size, "batch": B, "num_q_heads": Hq,
+            "num_kv_heads": Hkv,
             "page_size": P, "top_k_pages": K, "seq_lens_mean": round(sum(L) / len(L), 1),
             "quest_decode_us": round(fused, 2), "algorithmic_bytes": nbytes,
             "gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
@@ -583,12 +587,14 @@ def run_layers(args):
     outs = [torch.empty((1, 32, 128), dtype=torch.float16, device=dev) for _ in range(n_layers)]
     lses = [torch.empty((1, 32), dtype=torch.float32, device=dev) for _ in range(n_layers)]
 
+    o = q.opts(cluster_size=args.cluster_size)
+
     def one_launch():
-        q.decode_layers(base, layers, qs, K, ws, out=outs, lse=lses)
+        q.decode_layers(base, layers, qs, K, ws, o, out=outs, lse=lses)
 
     def per_layer():
         for i, lay in enumerate(layers):
-            q.decode(lay, qs[i], K, ws, out=outs[i], lse=lses[i])
+            q.decode(lay, qs[i], K, ws, o, out=outs[i], lse=lses[i])
 
     def timed(fn, reps=16):
         es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -611,6 +617,7 @@ def run_layers(args):
     peak, _ = peaks()
     gbs = nbytes / (fused_us * 1e-6) / 1e9
     print(json.dumps({"workload": "yarn_128k_32_layers_budget2048", "layers": n_layers,
+                      "cluster_size": args.cluster_size,
                       "decode_layers_us": round(fused_us, 1),
                       "decode_per_layer_launches_us": round(per_us, 1),
                       "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
