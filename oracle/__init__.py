@@ -61,8 +61,11 @@ def _load():
             lib.oq_append.argtypes = [D, P, P, P, P, P, P, P]
             lib.oq_score.argtypes = [D, P, P, P, P, P]
             lib.oq_topk.argtypes = [D, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
+            lib.oq_score_heads.argtypes = [D, P, P, P, P, P]
+            lib.oq_topk_union.argtypes = [D, P, P, ctypes.c_int, ctypes.c_int, P, P]
             lib.oq_attend.argtypes = [D, P, P, P, P, P, P, P, ctypes.c_int, P, P]
             for f in (lib.oq_build_meta, lib.oq_append, lib.oq_score, lib.oq_topk,
+                      lib.oq_score_heads, lib.oq_topk_union,
                       lib.oq_attend):
                 f.restype = ctypes.c_int
             _lib = lib
@@ -156,6 +159,34 @@ def topk(c: Cache, scores, K: int, sink: int = 0, local: int = 0) -> Tuple[np.nd
                          int(local), _ptr(idx), _ptr(cnt))
     if rc:
         raise OracleError("topk: bad K, window or length")
+    return idx, cnt
+
+
+def score_heads(c: Cache, q) -> np.ndarray:
+    """Per-query-head page scores [B][Hq][max_pages] float32 (-inf past the last page)."""
+    dims = c.dims()
+    qq = _f32(q)
+    out = np.empty((dims.batch, dims.num_q_heads, dims.max_pages), np.float32)
+    rc = _load().oq_score_heads(ctypes.byref(dims), _ptr(qq), _ptr(c.meta), _ptr(c.block_table),
+                                _ptr(c.seq_lens), _ptr(out))
+    if rc:
+        raise OracleError("score_heads: bad block table entry or length")
+    return out
+
+
+def topk_union(c: Cache, scores_h, K: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Union over each group's query heads of their top-K pages: idx [B][Hkv][min(G*K,
+    max_pages)] ascending (-1 padded) and counts [B][Hkv]."""
+    dims = c.dims()
+    G = dims.num_q_heads // dims.num_kv_heads
+    cap = min(G * K, dims.max_pages)
+    sc = _f32(scores_h)
+    idx = np.empty((dims.batch, dims.num_kv_heads, cap), np.int32)
+    cnt = np.empty((dims.batch, dims.num_kv_heads), np.int32)
+    rc = _load().oq_topk_union(ctypes.byref(dims), _ptr(sc), _ptr(c.seq_lens), int(K), int(cap),
+                               _ptr(idx), _ptr(cnt))
+    if rc:
+        raise OracleError("topk_union: bad K or length")
     return idx, cnt
 
 

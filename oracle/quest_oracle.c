@@ -195,6 +195,45 @@ int oq_score(const oq_dims* s, const float* q, const float* meta, const int32_t*
 }
 
 /* ---------------------------------------------------------------------------------
+ * The same bound per query head, without the maximum over a group: scores_h is
+ * [batch][num_q_heads][max_pages] (-inf past the last page).  Used by the group-level
+ * selection below.
+ * --------------------------------------------------------------------------------- */
+int oq_score_heads(const oq_dims* s, const float* q, const float* meta, const int32_t* block_table,
+                   const int32_t* seq_lens, float* scores_h) {
+    const int d = s->head_dim;
+    const int G = s->num_q_heads / s->num_kv_heads;
+    for (int b = 0; b < s->batch; ++b) {
+        const int L = seq_lens[b];
+        if (!len_ok(s, L)) return -1;
+        const int n_pages = pages_of(s, L);
+        for (int h = 0; h < s->num_q_heads; ++h) {
+            const int g = h / G;
+            const float* qh = q + ((size_t)b * s->num_q_heads + h) * d;
+            float* row = scores_h + ((size_t)b * s->num_q_heads + h) * s->max_pages;
+            for (int p = 0; p < s->max_pages; ++p) {
+                if (p >= n_pages) {
+                    row[p] = -INFINITY;
+                    continue;
+                }
+                const int64_t phys = phys_of(s, block_table, b, p);
+                if (phys < 0) return -1;
+                const float* mn = meta + meta_at(s, phys, g, 0);
+                const float* mx = meta + meta_at(s, phys, g, 1);
+                float u = 0.0f;
+                for (int i = 0; i < d; ++i) {
+                    float a = qh[i] * mn[i];
+                    float c = qh[i] * mx[i];
+                    u += (a > c) ? a : c;
+                }
+                row[p] = u;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------
  * Page selection.  [Guide] Solution, step 3: keep the K pages with the highest bounds
  * ([Summary]: "Top-K highest-scoring pages").  Pages are ordered by score, larger
  * first, and equal scores by page index, lower first; the first K_b = min(K, N_b) are
@@ -261,6 +300,55 @@ int oq_topk(const oq_dims* s, const float* scores, const int32_t* seq_lens, int 
         }
     }
     free(tmp);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------
+ * Group-level selection, union form.  [Guide] Best Practices step 2 (GQA): the bounds of
+ * every query head of a group are computed and the union of their top-k pages is kept,
+ * so the kv head's pages are loaded once for all of its query heads.  Each query head h of
+ * kv head g keeps its own K best pages (score larger first, then lower page, as above);
+ * the kv head keeps the union, at most G * K pages.  A sequence of at most K pages keeps
+ * every page.  idx: [batch][num_kv_heads][cap] with cap >= min(G * K, max_pages), the kept
+ * pages in ascending order, -1 after count.
+ * --------------------------------------------------------------------------------- */
+int oq_topk_union(const oq_dims* s, const float* scores_h, const int32_t* seq_lens, int K, int cap,
+                  int32_t* idx, int32_t* count) {
+    const int G = s->num_q_heads / s->num_kv_heads;
+    if (K < 1 || cap < 1) return -1;
+    oq_ranked* tmp = (oq_ranked*)malloc(sizeof(oq_ranked) * (size_t)(s->max_pages > 0 ? s->max_pages : 1));
+    unsigned char* kept = (unsigned char*)malloc((size_t)(s->max_pages > 0 ? s->max_pages : 1));
+    if (!tmp || !kept) { free(tmp); free(kept); return -1; }
+    for (int b = 0; b < s->batch; ++b) {
+        const int L = seq_lens[b];
+        if (!len_ok(s, L)) { free(tmp); free(kept); return -1; }
+        const int n_pages = pages_of(s, L);
+        for (int g = 0; g < s->num_kv_heads; ++g) {
+            for (int p = 0; p < n_pages; ++p) kept[p] = (unsigned char)(n_pages <= K);
+            if (n_pages > K) {
+                for (int h = g * G; h < (g + 1) * G; ++h) {
+                    const float* row = scores_h + ((size_t)b * s->num_q_heads + h) * s->max_pages;
+                    for (int p = 0; p < n_pages; ++p) {
+                        tmp[p].score = row[p];
+                        tmp[p].page = p;
+                    }
+                    qsort(tmp, (size_t)n_pages, sizeof(oq_ranked), oq_rank_cmp);
+                    for (int r = 0; r < K; ++r) kept[tmp[r].page] = 1;
+                }
+            }
+            int32_t* out = idx + ((size_t)b * s->num_kv_heads + g) * cap;
+            int n_out = 0;
+            for (int p = 0; p < n_pages; ++p) {
+                if (!kept[p]) continue;
+                if (n_out >= cap) { free(tmp); free(kept); return -1; }
+                out[n_out++] = p;
+            }
+            for (int r = n_out; r < cap; ++r) out[r] = -1;
+            count[(size_t)b * s->num_kv_heads + g] = n_out;
+        }
+    }
+    free(tmp);
+    free(kept);
     return 0;
 }
 

@@ -317,6 +317,67 @@ def test_topk_window_zero_is_plain_topk_and_local_zero_keeps_no_tail():
         oracle.topk(c, scores, 4, 3, 2)  # the window does not fit the budget
 
 
+def test_score_heads_are_the_per_head_bounds_whose_group_max_is_the_score():
+    """The per-query-head bound, by a float64 brute force over the page's boxes, and its
+    maximum over each group is the kv-head score."""
+    w, c = make(lens=(300, 40), batch=2, hq=8, hkv=2)
+    oracle.build_meta(c)
+    rng = np.random.default_rng(12)
+    qh = rng.standard_normal((2, 8, 128)).astype(np.float16).astype(np.float32)
+    sh = oracle.score_heads(c, qh)
+    sk = oracle.score(c, qh)
+    for b in range(2):
+        n = wl.pages_for(int(c.seq_lens[b]), 16)
+        assert np.all(np.isneginf(sh[b, :, n:]))
+        for h in range(8):
+            g = h // 4
+            for p in range(n):
+                ph = int(c.block_table[b, p])
+                mn = c.meta[ph, g, 0].astype(np.float64)
+                mx = c.meta[ph, g, 1].astype(np.float64)
+                qq = qh[b, h].astype(np.float64)
+                ref = np.maximum(qq * mn, qq * mx).sum()
+                assert abs(sh[b, h, p] - ref) <= 1e-4 * max(1.0, abs(ref))
+        for g in range(2):
+            np.testing.assert_array_equal(sh[b, 4 * g:4 * g + 4, :n].max(axis=0), sk[b, g, :n])
+
+
+def test_topk_union_is_the_union_of_per_head_topk():
+    """[Guide] Best Practices step 2 (GQA, union form): brute force per query head, union
+    per group, ascending; at most G * K pages; a group of one head is plain top-K; short
+    sequences keep every page."""
+    rng = np.random.default_rng(13)
+    w, c = make(lens=(16 * 90, 16 * 5, 16 * 33), batch=3, hq=8, hkv=2)
+    mp = c.block_table.shape[1]
+    n = [wl.pages_for(int(L), 16) for L in c.seq_lens]
+    sh = np.full((3, 8, mp), -np.inf, np.float32)
+    for b in range(3):
+        sh[b, :, :n[b]] = rng.standard_normal((8, n[b])).astype(np.float32)
+        sh[b, 1, :n[b]] = np.round(sh[b, 1, :n[b]])  # ties inside one head
+    for K in (1, 7, 20):
+        idx, cnt = oracle.topk_union(c, sh, K)
+        assert idx.shape[2] == min(4 * K, mp)
+        for b in range(3):
+            for g in range(2):
+                if n[b] <= K:
+                    want = list(range(n[b]))
+                else:
+                    want = set()
+                    for h in range(4 * g, 4 * g + 4):
+                        want |= set(sorted(range(n[b]), key=lambda p: (-float(sh[b, h, p]), p))[:K])
+                    want = sorted(want)
+                assert idx[b, g, :cnt[b, g]].tolist() == want
+                assert cnt[b, g] <= 4 * K and np.all(idx[b, g, cnt[b, g]:] == -1)
+    # one head per group: the union is the plain top-K set
+    w1, c1 = make(lens=(16 * 90,), batch=1, hq=2, hkv=2)
+    s1 = np.full((1, 2, c1.block_table.shape[1]), -np.inf, np.float32)
+    s1[0, :, :90] = rng.standard_normal((2, 90)).astype(np.float32)
+    iu, cu = oracle.topk_union(c1, s1, 9)
+    ip, cp = oracle.topk(c1, s1, 9)
+    for g in range(2):
+        assert iu[0, g, :cu[0, g]].tolist() == sorted(ip[0, g, :cp[0, g]].tolist())
+
+
 def test_planted_needles_are_selected():
     """[Guide] Evaluation: a page holding a key aligned with the query gets an elevated
     bound and is kept by the top-K."""
