@@ -529,6 +529,28 @@ def run_sweep(args):
             q.sparse_decode(cache, qv, i2, c2, K, ws, out=out, lse=lse)
 
         chain_us = timed(chain, reps)
+        union = {}
+        G = Hq // Hkv
+        if G > 1:
+            # the union form of the group-level selection: per-head bounds, each head's top-K,
+            # their union (rows of G*K), sparse decode over it
+            cap = min(G * K, cache.max_pages)
+            ws_u = q.workspace(cache, cap)
+            sh = torch.empty((B, Hq, cache.max_pages), dtype=torch.float32, device=dev)
+            ou = q.opts(gqa_union=True)
+            iu, cu = q.topk(cache, q.estimate_heads(cache, qv, ws_u, scores=sh), K, ws_u, ou)
+
+            def union_chain():
+                q.estimate_heads(cache, qv, ws_u, scores=sh)
+                i3, c3 = q.topk(cache, sh, K, ws_u, ou)
+                q.sparse_decode(cache, qv, i3, c3, cap, ws_u, out=out, lse=lse)
+
+            u_us = timed(union_chain, reps)
+            u_tok = selected_tokens(iu, cu, L, P)
+            u_bytes = decode_bytes(L, u_tok, B, Hq, Hkv, page=P)
+            union = {"union_chain_us": round(u_us, 2), "union_pages_mean":
+                     round(float(cu.float().mean()), 1), "union_algorithmic_bytes": u_bytes,
+                     "union_gbs": round(u_bytes / (u_us * 1e-6) / 1e9, 1)}
         dense_us = timed(lambda: q.dense_decode(cache, qv, ws, out=out, lse=lse), max(8, reps // 4))
         snap_meta, snap_len = cache.meta.clone(), cache.seq_lens.clone()
 
@@ -548,7 +570,7 @@ def run_sweep(args):
             "gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
             "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
             "unfused_chain_us": round(chain_us, 2), "append_plus_len_reset_us": round(append_us, 2),
-            "dense_decode_us": round(dense_us, 2), "status": rc}), flush=True)
+            "dense_decode_us": round(dense_us, 2), "status": rc, **union}), flush=True)
         del w, cache, ws, scores
         torch.cuda.empty_cache()
 

@@ -125,7 +125,12 @@ typedef struct quest_opts {
                                  Implementation step 2).  0 and 0 (the default): plain
                                  top-K.  Needs sink_pages, local_pages >= 0 and
                                  sink_pages + local_pages <= top_k (QUEST_ERR_INVALID_ARG) */
-    int32_t pad_;
+    int32_t gqa_union;        /* quest_topk only: scores are per query head ([batch]
+                                 [num_q_heads][max_pages], quest_estimate_heads); each query
+                                 head keeps its top_k pages and the kv head keeps their union
+                                 ([Guide] Best Practices step 2), written to idx rows of
+                                 min(G * top_k, max_pages) entries.  Not with sink / local
+                                 pages; the fused calls answer QUEST_ERR_UNSUPPORTED.        */
 } quest_opts_t;
 
 /* quest_decode only: never publish the selection, so that every decode work item's
@@ -176,6 +181,15 @@ int quest_append(const quest_cache_t* cache, const void* k_new, const void* v_ne
  */
 int quest_estimate(const quest_cache_t* cache, const void* q, float* scores, void* ws,
                    size_t ws_bytes, quest_stream_t stream);
+
+/*
+ * The same bound per query head, without the maximum over its group: scores is fp32
+ * [batch][num_q_heads][max_pages] (-inf at and past ceil(seq_len / P)).  Input of the
+ * union form of the group-level selection ([Guide] Best Practices step 2; quest_topk with
+ * opts->gqa_union).
+ */
+int quest_estimate_heads(const quest_cache_t* cache, const void* q, float* scores, void* ws,
+                         size_t ws_bytes, quest_stream_t stream);
 
 /*
  * Top-K page selection.  [Guide] Solution step 3; [Summary] "Top-K highest-scoring

@@ -37,7 +37,8 @@ HEAD_DIM = 128
 # Every symbol include/quest.h declares.
 EXPORTS = (
     "quest_workspace_size", "quest_workspace_init", "quest_build_meta", "quest_append",
-    "quest_estimate", "quest_topk", "quest_sparse_decode", "quest_decode", "quest_decode_layers",
+    "quest_estimate", "quest_estimate_heads", "quest_topk", "quest_sparse_decode",
+    "quest_decode", "quest_decode_layers",
     "quest_decode_step", "quest_dense_decode", "quest_decode_static", "quest_read_status",
     "quest_last_error", "quest_status_string", "quest_version",
 )
@@ -72,7 +73,7 @@ class QuestOpts(ctypes.Structure):
         ("wait_limit_ns", ctypes.c_int64), ("decode_lag", ctypes.c_int32),
         ("trace_capacity", ctypes.c_int32), ("trace", ctypes.c_void_p),
         ("cluster_size", ctypes.c_int32), ("sink_pages", ctypes.c_int32),
-        ("local_pages", ctypes.c_int32), ("pad_", ctypes.c_int32),
+        ("local_pages", ctypes.c_int32), ("gqa_union", ctypes.c_int32),
     ]
 
 
@@ -100,6 +101,7 @@ def load() -> ctypes.CDLL:
             "quest_build_meta": (ctypes.c_int, [C, V, SZ, V]),
             "quest_append": (ctypes.c_int, [C, V, V, V, SZ, V]),
             "quest_estimate": (ctypes.c_int, [C, V, V, V, SZ, V]),
+            "quest_estimate_heads": (ctypes.c_int, [C, V, V, V, SZ, V]),
             "quest_topk": (ctypes.c_int, [C, V, I32, V, V, V, SZ, O, V]),
             "quest_sparse_decode": (ctypes.c_int, [C, V, V, V, I32, V, V, V, SZ, O, V]),
             "quest_decode": (ctypes.c_int, [C, V, I32, V, V, V, V, V, SZ, O, V]),
@@ -151,7 +153,7 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
 def opts(pages_per_split: int = 0, score_tile_pages: int = 0, max_ctas: int = 0,
          debug_flags: int = 0, wait_limit_ns: int = 0, decode_lag: int = 0,
          trace: Optional[torch.Tensor] = None, cluster_size: int = 0, sink_pages: int = 0,
-         local_pages: int = 0) -> QuestOpts:
+         local_pages: int = 0, gqa_union: bool = False) -> QuestOpts:
     """Launch tuning (0 = default).  ``trace``: int64 CUDA tensor of 1 + 2n elements whose
     first element is zero; receives up to n timeline records of the fused kernel.
     ``sink_pages`` / ``local_pages``: pages always kept at the start / end of a sequence
@@ -161,7 +163,7 @@ def opts(pages_per_split: int = 0, score_tile_pages: int = 0, max_ctas: int = 0,
         _need(trace, "trace", torch.int64)
         cap, ptr = (trace.numel() - 1) // 2, trace.data_ptr()
     o = QuestOpts(pages_per_split, score_tile_pages, max_ctas, debug_flags, wait_limit_ns,
-                  decode_lag, cap, ptr, cluster_size, sink_pages, local_pages, 0)
+                  decode_lag, cap, ptr, cluster_size, sink_pages, local_pages, int(gqa_union))
     o._trace_ref = trace  # keep the buffer alive with the options
     return o
 
@@ -266,10 +268,29 @@ def estimate(cache: PagedCache, q: torch.Tensor, ws: torch.Tensor,
     return scores
 
 
+def estimate_heads(cache: PagedCache, q: torch.Tensor, ws: torch.Tensor,
+                   scores: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Per-query-head page bounds [B][Hq][max_pages] (input of the union selection)."""
+    _need(q, "q", torch.float16, (cache.batch, cache.desc.num_q_heads, HEAD_DIM))
+    shape = (cache.batch, cache.desc.num_q_heads, cache.max_pages)
+    if scores is None:
+        scores = torch.empty(shape, dtype=torch.float32, device=q.device)
+    _need(scores, "scores", torch.float32, shape)
+    _check(load().quest_estimate_heads(ctypes.byref(cache.desc), q.data_ptr(), scores.data_ptr(),
+                                       ws.data_ptr(), ws.numel(), _stream(stream)))
+    return scores
+
+
 def topk(cache: PagedCache, scores: torch.Tensor, top_k: int, ws: torch.Tensor,
          o: Optional[QuestOpts] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    _need(scores, "scores", torch.float32, (cache.batch, cache.num_kv_heads, cache.max_pages))
-    idx = torch.empty((cache.batch, cache.num_kv_heads, top_k), dtype=torch.int32,
+    """Kept pages (ascending, -1 padded) and counts.  With o.gqa_union the scores are per
+    query head and the rows hold min(G * top_k, max_pages) entries."""
+    union = o is not None and bool(o.gqa_union)
+    rows = cache.desc.num_q_heads if union else cache.num_kv_heads
+    _need(scores, "scores", torch.float32, (cache.batch, rows, cache.max_pages))
+    G = cache.desc.num_q_heads // cache.num_kv_heads
+    cap = min(G * top_k, cache.max_pages) if union else top_k
+    idx = torch.empty((cache.batch, cache.num_kv_heads, cap), dtype=torch.int32,
                       device=scores.device)
     cnt = torch.empty((cache.batch, cache.num_kv_heads), dtype=torch.int32, device=scores.device)
     _check(load().quest_topk(ctypes.byref(cache.desc), scores.data_ptr(), int(top_k),

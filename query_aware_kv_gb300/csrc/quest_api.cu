@@ -6,6 +6,8 @@
 #include <cstdio>
 #include <string>
 
+#include <algorithm>
+
 #include "quest_internal.h"
 
 using namespace quest;
@@ -258,8 +260,24 @@ int quest_estimate(const quest_cache_t* cache, const void* q, float* scores, voi
   Params p = make_params(cache, ws, make_layout(cache, t), t, nullptr);
   p.q = static_cast<const __half*>(q);
   p.scores = scores;
-  return launched(launch_estimate(p, group_of(cache), static_cast<cudaStream_t>(stream)),
+  return launched(launch_estimate(p, group_of(cache), false, static_cast<cudaStream_t>(stream)),
                   "quest_estimate");
+}
+
+int quest_estimate_heads(const quest_cache_t* cache, const void* q, float* scores, void* ws,
+                         size_t ws_bytes, quest_stream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (cache->batch == 0) return QUEST_OK;
+  if (!q || !scores || !aligned(q, 16) || !aligned(scores, 4))
+    return fail(QUEST_ERR_INVALID_ARG, "q must be 16-byte aligned, scores 4-byte aligned");
+  if ((rc = check_ws(ws, ws_bytes, sizeof(WsHeader)))) return rc;
+  const Tiling t = make_tiling(cache, 1, nullptr);
+  Params p = make_params(cache, ws, make_layout(cache, t), t, nullptr);
+  p.q = static_cast<const __half*>(q);
+  p.scores = scores;
+  return launched(launch_estimate(p, group_of(cache), true, static_cast<cudaStream_t>(stream)),
+                  "quest_estimate_heads");
 }
 
 int quest_topk(const quest_cache_t* cache, const float* scores, int32_t top_k, int32_t* idx,
@@ -279,6 +297,13 @@ int quest_topk(const quest_cache_t* cache, const float* scores, int32_t top_k, i
   p.sel_idx = idx;
   p.sel_count = count;
   p.top_k = top_k;
+  if (opts && opts->gqa_union) {
+    if (opts->sink_pages || opts->local_pages)
+      return fail(QUEST_ERR_INVALID_ARG, "gqa_union does not combine with sink / local pages");
+    const long long cap = std::min((long long)group_of(cache) * top_k, (long long)cache->max_pages);
+    return launched(launch_topk_union(p, (int)cap, static_cast<cudaStream_t>(stream)),
+                    "quest_topk");
+  }
   return launched(launch_topk(p, static_cast<cudaStream_t>(stream)), "quest_topk");
 }
 
@@ -317,6 +342,9 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   if (rc) return rc;
   if ((rc = check_topk(top_k))) return rc;
   if ((rc = check_window(opts, top_k))) return rc;
+  if (opts && opts->gqa_union)
+    return fail(QUEST_ERR_UNSUPPORTED, "gqa_union: use quest_estimate_heads + quest_topk + "
+                "quest_sparse_decode (the fused step selects per kv head)");
   if (cache->batch == 0) return QUEST_OK;
   if (!q || !out || !aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(idx_out, 4) || !aligned(count_out, 4))
@@ -399,6 +427,8 @@ int quest_decode_layers(const quest_cache_t* cache, const quest_layer_t* layers,
   if (rc) return rc;
   if ((rc = check_topk(top_k))) return rc;
   if ((rc = check_window(opts, top_k))) return rc;
+  if (opts && opts->gqa_union)
+    return fail(QUEST_ERR_UNSUPPORTED, "gqa_union: the fused step selects per kv head");
   if (!layers || n_layers < 1 || n_layers > QUEST_MAX_LAYERS)
     return fail(QUEST_ERR_INVALID_ARG, "n_layers %d: use 1..%d layers", n_layers, QUEST_MAX_LAYERS);
   if (cache->batch == 0) return QUEST_OK;

@@ -320,8 +320,11 @@ __device__ __forceinline__ float corner_dot(const QueryFrag<G>& f, int j, const 
 // Scores pages [p0, p0 + n_live) of (b, g) into dst[0 .. n_live).  The boxes of those pages
 // are contiguous (logical page order).  Half-warp per page, 16 B of the min row and 16 B of
 // the max row per lane, 4 pages in flight per half-warp.  Called by the whole block.
-template <int G>
-__device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, float* dst) {
+// PerHead: dst is query head (g * G)'s row of a [B][Hq][max_pages] array and every head of
+// the group writes its own bound (rows `stride` floats apart) instead of the group maximum.
+template <int G, bool PerHead = false>
+__device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, float* dst,
+                           size_t stride = 0) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int hw = tid >> 4, c = tid & 15, nhw = nthr >> 4;
   QueryFrag<G> f;
@@ -352,9 +355,13 @@ __device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, fl
         s += __shfl_xor_sync(0xffffffffu, s, 2);
         s += __shfl_xor_sync(0xffffffffu, s, 1);
         best = fmaxf(best, s);
+        if (PerHead) {
+          const int r = base + u * nhw + hw;
+          if (c == 0 && r < n_live) dst[(size_t)j * stride + r] = s;
+        }
       }
       const int r = base + u * nhw + hw;
-      if (c == 0 && r < n_live) dst[r] = best;
+      if (!PerHead && c == 0 && r < n_live) dst[r] = best;
     }
   }
 }

@@ -29,7 +29,8 @@ cudaError_t ensure_smem(const void* fn, size_t bytes) {
 
 // ---------------------------------------------------------------- scoring
 // grid (n_score_tiles, B*Hkv), 256 threads.
-template <int G>
+// PerHead: scores is [B][Hq][max_pages], one row per query head (quest_estimate_heads).
+template <int G, bool PerHead>
 __global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
   pdl_wait();
   const int tile = blockIdx.x, bg = blockIdx.y;
@@ -39,9 +40,12 @@ __global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
   const int p0 = tile * p.score_tile_pages;
   const int np = min(p.score_tile_pages, p.max_pages - p0);
   const int n_live = max(0, min(N - p0, np));
-  float* row = p.scores + (size_t)bg * p.max_pages + p0;
-  for (int i = n_live + (int)threadIdx.x; i < np; i += blockDim.x) row[i] = -CUDART_INF_F;
-  if (n_live > 0) score_tile<G>(p, b, g, p0, n_live, row);
+  const size_t first_row = PerHead ? (size_t)b * p.Hq + (size_t)g * G : (size_t)bg;
+  float* row = p.scores + first_row * p.max_pages + p0;
+  for (int j = 0; j < (PerHead ? G : 1); ++j)
+    for (int i = n_live + (int)threadIdx.x; i < np; i += blockDim.x)
+      row[(size_t)j * p.max_pages + i] = -CUDART_INF_F;
+  if (n_live > 0) score_tile<G, PerHead>(p, b, g, p0, n_live, row, (size_t)p.max_pages);
 }
 
 // ---------------------------------------------------------------- top-K
@@ -56,6 +60,61 @@ __global__ void __launch_bounds__(kConsumerThreads) topk_kernel(Params p) {
   topk_row<kConsumerThreads, false>(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
                                     p.sink_pages, p.local_pages, p.sel_idx + (size_t)bg * p.top_k, p.sel_count + bg,
                                     topk_smem_at(sm, p.max_pages), scratch);
+}
+
+// Group-level selection, union form ("Guide to Quest", Best Practices step 2): each query
+// head of the group keeps its own top-K pages (the selection above, one row of the
+// per-head scores at a time), the kv head keeps their union, written in ascending order
+// into a row of `row_cap` entries.  grid (B*Hkv), 256 threads.
+__global__ void __launch_bounds__(kConsumerThreads) topk_union_kernel(Params p, int row_cap) {
+  extern __shared__ __align__(16) unsigned char sm[];
+  pdl_wait();
+  const int tid = threadIdx.x;
+  const int bg = blockIdx.x, b = bg / p.Hkv, g = bg % p.Hkv;
+  const int G = p.Hq / p.Hkv, K = p.top_k;
+  const int L = load_len(p, b, kSiteTopk);
+  const int N = (L + p.P - 1) / p.P;
+  int* idx_out = p.sel_idx + (size_t)bg * row_cap;
+  if (N <= K) {
+    for (int r = tid; r < row_cap; r += kConsumerThreads) idx_out[r] = r < N ? r : -1;
+    if (tid == 0) p.sel_count[bg] = N;
+    return;
+  }
+  const TopkSmem t = topk_smem_at(sm, p.max_pages);
+  int* scratch = reinterpret_cast<int*>(sm + topk_smem_bytes(p.max_pages));  // [256]
+  int* list = scratch + 256;                                                   // [K]
+  uint32_t* ubits = reinterpret_cast<uint32_t*>(list + K);                     // [nw]
+  const int nw = (N + 31) >> 5;
+  for (int i = tid; i < nw; i += kConsumerThreads) ubits[i] = 0u;
+  for (int j = 0; j < G; ++j) {
+    __syncthreads();
+    const float* row = p.scores + ((size_t)b * p.Hq + (size_t)g * G + j) * p.max_pages;
+    topk_row<kConsumerThreads, false>(row, N, K, 0, 0, list, scratch + 255, t, scratch);
+    __syncthreads();
+    for (int r = tid; r < K; r += kConsumerThreads)
+      atomicOr(&ubits[list[r] >> 5], 1u << (list[r] & 31));
+  }
+  __syncthreads();
+  // the union in ascending order: per-thread word counts, one block scan, then the bits
+  const int wpt = (nw + kConsumerThreads - 1) / kConsumerThreads;
+  const int w0 = min(nw, tid * wpt), w1 = min(nw, w0 + wpt);
+  int n = 0;
+  for (int w = w0; w < w1; ++w) n += __popc(ubits[w]);
+  int pos = block_excl_sum<kConsumerThreads, false>(n, scratch + 32);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t A = ubits[w];
+    while (A) {
+      const int bit = __ffs(A) - 1;
+      A &= A - 1u;
+      idx_out[pos++] = w * 32 + bit;
+    }
+  }
+  __syncthreads();
+  if (tid == kConsumerThreads - 1) scratch[48] = pos;  // the last thread ends at the total
+  __syncthreads();
+  const int total = scratch[48];
+  for (int r = total + tid; r < row_cap; r += kConsumerThreads) idx_out[r] = -1;
+  if (tid == 0) p.sel_count[bg] = total;
 }
 
 // ---------------------------------------------------------------- decode
@@ -95,17 +154,19 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Params p) {
 }
 
 template <int G>
-static const void* estimate_fn() { return (const void*)estimate_kernel<G>; }
+static const void* estimate_fn(bool per_head) {
+  return per_head ? (const void*)estimate_kernel<G, true> : (const void*)estimate_kernel<G, false>;
+}
 
 template <int G, int P>
 static const void* decode_fn() { return (const void*)decode_kernel<G, P>; }
 
-static const void* pick_estimate(int G) {
+static const void* pick_estimate(int G, bool per_head) {
   switch (G) {
-    case 1: return estimate_fn<1>();
-    case 2: return estimate_fn<2>();
-    case 4: return estimate_fn<4>();
-    default: return estimate_fn<8>();
+    case 1: return estimate_fn<1>(per_head);
+    case 2: return estimate_fn<2>(per_head);
+    case 4: return estimate_fn<4>(per_head);
+    default: return estimate_fn<8>(per_head);
   }
 }
 
@@ -126,13 +187,25 @@ static const void* pick_decode(int G, int P) {
   }
 }
 
-cudaError_t launch_estimate(const Params& p, int G, cudaStream_t s) {
-  const void* fn = pick_estimate(G);
+cudaError_t launch_estimate(const Params& p, int G, bool per_head, cudaStream_t s) {
+  const void* fn = pick_estimate(G, per_head);
   const size_t smem = 0;
   Params pp = p;
   void* args[] = {&pp};
   return launch_pdl(fn, dim3(p.n_score_tiles, p.B * p.Hkv), dim3(kConsumerThreads), smem, s,
                     args);
+}
+
+cudaError_t launch_topk_union(const Params& p, int row_cap, cudaStream_t s) {
+  const void* fn = (const void*)topk_union_kernel;
+  const size_t smem = topk_smem_bytes(p.max_pages) + 256 * 4 + (size_t)p.top_k * 4 +
+                      (size_t)((p.max_pages + 31) / 32) * 4;
+  cudaError_t e = ensure_smem(fn, smem);
+  if (e != cudaSuccess) return e;
+  Params pp = p;
+  int rc = row_cap;
+  void* args[] = {&pp, &rc};
+  return launch_pdl(fn, dim3(p.B * p.Hkv), dim3(kConsumerThreads), smem, s, args);
 }
 
 cudaError_t launch_topk(const Params& p, cudaStream_t s) {

@@ -96,6 +96,13 @@ def test_calls_reject_bad_arguments_without_launching(lib):
         assert lib.quest_decode(ctypes.byref(d), 16, 4, 16, None, None, None, 256, 1 << 20,
                                 ctypes.byref(o), None) == q.QUEST_ERR_INVALID_ARG
         assert "sink_pages" in lib.quest_last_error().decode()
+    # the union selection is for the separate calls only
+    ou = q.opts(gqa_union=True)
+    assert lib.quest_decode(ctypes.byref(d), 16, 4, 16, None, None, None, 256, 1 << 20,
+                            ctypes.byref(ou), None) == q.QUEST_ERR_UNSUPPORTED
+    ou2 = q.opts(gqa_union=True, sink_pages=1)
+    assert lib.quest_topk(ctypes.byref(d), 16, 4, 16, 16, 256, 1 << 20, ctypes.byref(ou2),
+                          None) == q.QUEST_ERR_INVALID_ARG
     # multi-layer call: layer count out of range, k_new for some layers only
     lay = (q.QuestLayer * 2)()
     for i in range(2):

@@ -177,6 +177,83 @@ def test_fused_step_with_sink_and_local_pages(cs):
                                check_cache=(t == w.steps - 1))
 
 
+def test_estimate_heads_and_group_max():
+    """Per-query-head bounds within fp32 reordering of the oracle's; their group maximum is
+    bit-identical to quest_estimate."""
+    w = small(lens=(1000, 1, 333), hq=8, hkv=2, outliers=4)
+    pair = H.on_device(w)
+    qd = w.q[0].cuda()
+    sh = q.estimate_heads(pair.cache, qd, pair.ws).cpu().numpy()
+    sk = q.estimate(pair.cache, qd, pair.ws).cpu().numpy()
+    H.assert_status_ok(pair.ws)
+    qh = w.q[0].numpy().astype(np.float32)
+    ref = oracle.score_heads(pair.ref, qh)
+    tol = H.score_tolerance(pair.ref, qh)  # [B][Hkv][max_pages], valid for every head of g
+    tol_h = np.repeat(tol, 4, axis=1)
+    H.assert_scores_close(sh, ref, tol_h)
+    G = 4
+    for g in range(2):
+        np.testing.assert_array_equal(sh[:, g * G:(g + 1) * G].max(axis=1), sk[:, g])
+
+
+@pytest.mark.parametrize("K", [1, 9, 40])
+def test_topk_union_matches_oracle_on_identical_scores(K):
+    """[Guide] Best Practices step 2, union form: given the oracle's own per-head scores the
+    union must be exactly the oracle's."""
+    w = small(lens=(16 * 200 - 3, 16 * 6, 16 * 41), batch=3, hq=8, hkv=2, budget=16 * K)
+    pair = H.on_device(w)
+    sh = oracle.score_heads(pair.ref, w.q[0].numpy().astype(np.float32))
+    sh[0, 1] = np.where(np.isfinite(sh[0, 1]), np.round(sh[0, 1] / 50.0), sh[0, 1])  # ties
+    o = q.opts(gqa_union=True)
+    idx, cnt = q.topk(pair.cache, torch.from_numpy(sh).cuda(), K, pair.ws, o)
+    H.assert_status_ok(pair.ws)
+    ri, rc = oracle.topk_union(pair.ref, sh, K)
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    assert gi.shape == ri.shape
+    assert np.array_equal(gc, rc)
+    for b in range(3):
+        for g in range(2):
+            assert gi[b, g, :gc[b, g]].tolist() == ri[b, g, :rc[b, g]].tolist()
+            assert np.all(gi[b, g, gc[b, g]:] == -1)
+
+
+def test_union_chain_matches_oracle():
+    """Per-head bounds, union selection and sparse decode over the union (rows of G*K),
+    against the oracle: swaps only among pages near some head's K-th score; attention over
+    the GPU's union."""
+    w = small(lens=(3000, 700, 16 * 9), batch=3, hq=8, hkv=2, budget=256, outliers=4,
+              steps=1)
+    pair = H.on_device(w)
+    K = w.top_k
+    G = 4
+    qd = w.q[0].cuda()
+    qh = w.q[0].numpy().astype(np.float32)
+    sh = q.estimate_heads(pair.cache, qd, pair.ws)
+    idx, cnt = q.topk(pair.cache, sh, K, pair.ws, q.opts(gqa_union=True))
+    cap = idx.shape[2]
+    ws_u = q.workspace(pair.cache, cap)  # partials for rows of G*K pages
+    out, lse = q.sparse_decode(pair.cache, qd, idx, cnt, cap, ws_u)
+    H.assert_status_ok(pair.ws)
+    H.assert_status_ok(ws_u)
+    ref_sh = oracle.score_heads(pair.ref, qh)
+    ri, rc = oracle.topk_union(pair.ref, ref_sh, K)
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    for b in range(3):
+        n = wl.pages_for(int(pair.ref.seq_lens[b]), 16)
+        for g in range(2):
+            got = set(gi[b, g, :gc[b, g]].tolist())
+            want = set(ri[b, g, :rc[b, g]].tolist())
+            window = set()
+            if n > K:
+                for h in range(g * G, (g + 1) * G):
+                    row = ref_sh[b, h, :n]
+                    sk = float(np.sort(row)[::-1][K - 1])
+                    window |= {p for p in range(n) if abs(float(row[p]) - sk) <= H.TIE_REL * abs(sk)}
+            assert got - window == want - window, (b, g)
+    out_ref, lse_ref = oracle.attend(pair.ref, qh, gi, gc)
+    H.assert_attention_close(out, lse, out_ref, lse_ref)
+
+
 def test_topk_at_max_pages():
     """The largest supported row: 16384 pages."""
     n = q.QUEST_MAX_PAGES
