@@ -179,6 +179,38 @@ def oracle_timing(w, budget_s: float, max_steps: int):
     return us, len(times)
 
 
+def oracle_timing_all_cores(w, budget_s: float):
+    """The oracle's score + top-K + attend on every host core at once (one thread per core,
+    each on its own query of the workload, the cache shared read-only; the C calls release
+    the interpreter lock).  Returns (us per step at full occupancy, steps, threads)."""
+    import concurrent.futures as cf
+    import oracle
+    oracle.build()
+    ref = oracle.Cache.from_arrays(w.k_pool.cpu().numpy(), w.v_pool.cpu().numpy(),
+                                   w.block_table.cpu().numpy(), w.seq_lens.cpu().numpy(),
+                                   w.num_q_heads)
+    oracle.build_meta(ref)
+    qs = w.q.cpu().numpy()
+    threads = max(1, os.cpu_count() or 1)
+
+    def one(t):
+        s = oracle.score(ref, qs[t % w.steps])
+        i, c = oracle.topk(ref, s, w.top_k)
+        oracle.attend(ref, qs[t % w.steps], i, c)
+
+    one(0)
+    steps = 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        while True:
+            list(ex.map(one, range(steps, steps + threads)))
+            steps += threads
+            if time.perf_counter() - t0 > budget_s:
+                break
+    wall = time.perf_counter() - t0
+    return 1e6 * wall / steps, steps, threads
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -451,6 +483,11 @@ def run_quest(args):
             "value": round(us, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
             "sample": f"{k} decode steps (append + score + top-K + attend) of the same "
                       f"workload, single-threaded C oracle"}
+        us_all, k_all, threads = oracle_timing_all_cores(w, budget_s=min(10.0, args.cpu_seconds))
+        line["cpu_baseline_all_cores"] = {
+            "value": round(us_all, 1), "unit": "us/step", "cores": threads, "kind": "oracle",
+            "sample": f"{k_all} score + top-K + attend steps at the prefill context, one "
+                      f"thread per host core, time per step at full occupancy"}
     print(json.dumps(line), flush=True)
 
 
