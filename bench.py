@@ -45,6 +45,8 @@ def parse():
                     help="CTAs per (sequence, kv head) cluster for --sweep / --layers (0: automatic)")
     ap.add_argument("--layers", action="store_true",
                     help="time the 32-layer 128K step in one launch against one launch per layer")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the chunked-prefill write (quest_prefill) at several chunk sizes")
     ap.add_argument("--sweep", action="store_true",
                     help="measure every workload (one JSON line each) instead of the step")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="N",
@@ -612,6 +614,102 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def prefill_bytes(batch, n, num_kv_heads, page, first_lens):
+    """Algorithmic bytes of one quest_prefill: the chunk's K and V read once and written once,
+    and the box of every page the chunk touches written (read too when it was partial)."""
+    rows = 2 * batch * n * num_kv_heads * 256
+    boxes = 0
+    for L in first_lens:
+        touched = (L + n - 1) // page - L // page + 1
+        boxes += touched * num_kv_heads * 512 + (num_kv_heads * 512 if L % page else 0)
+    return 2 * rows + boxes
+
+
+def run_prefill(args):
+    """quest_prefill on the 32K-context MHA geometry (1 x 32 heads, page 16) and the GQA
+    geometry (4 x 8 kv heads, page 16): chunks of 512, 4096 and 32768 tokens from an empty
+    cache, and a 32K prompt written with a torch scatter + quest_build_meta for comparison;
+    L2 flushed before each timed launch; one JSON line per case."""
+    import torch
+
+    import query_aware_kv_gb300 as q
+    from query_aware_kv_gb300 import build as cuda_build
+
+    cuda_build.build()
+    q.load()
+    dev = torch.device("cuda")
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sum = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush_buf.zero_()
+        torch.sum(flush_buf[: FLUSH_BYTES // 2].view(torch.int64), dim=0, out=flush_sum)
+
+    def timed(reset, fn, reps):
+        es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for _ in range(3):
+            reset()
+            fn()
+        for a, b in es:
+            reset()
+            flush_l2()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(1e3 * a.elapsed_time(b) for a, b in es) / reps
+
+    peak, _ = peaks()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    for name, B, Hq, Hkv in (("longchat_32k_mha", 1, 32, 32), ("llama31_gqa", 4, 32, 8)):
+        P, total = 16, 32768
+        pages = total // P
+        num_phys = B * pages
+        k_pool = torch.empty((num_phys, Hkv, P, 128), dtype=torch.float16, device=dev)
+        v_pool = torch.empty_like(k_pool)
+        bt = torch.randperm(num_phys, generator=gen, device=dev).to(torch.int32).view(B, pages)
+        lens = torch.zeros(B, dtype=torch.int32, device=dev)
+        cache = q.PagedCache.allocate_meta(k_pool, v_pool, bt, lens, Hq)
+        ws = q.workspace(cache, 64)
+        for n in (512, 4096, 32768):
+            kc = torch.randn((B, n, Hkv, 128), generator=gen, device=dev).to(torch.float16)
+            vc = torch.randn((B, n, Hkv, 128), generator=gen, device=dev).to(torch.float16)
+            us = timed(lambda: lens.zero_(),
+                       lambda: q.prefill(cache, kc, vc, ws), 32 if n < 32768 else 8)
+            nbytes = prefill_bytes(B, n, Hkv, P, [0] * B)
+            rec = {"workload": name, "batch": B, "num_kv_heads": Hkv, "page_size": P,
+                   "chunk_tokens": n, "quest_prefill_us": round(us, 2), "algorithmic_bytes": nbytes,
+                   "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                   "frac_of_measured": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)}
+            if n == total:
+                fused_meta = cache.meta.clone()
+                # the same prompt written without the fused boxes: scatter into the pages,
+                # then a box pass that reads every key again
+                flat = bt.view(-1).long()
+
+                def scatter():
+                    k_pool[flat] = kc.view(B, pages, P, Hkv, 128).permute(0, 1, 3, 2, 4) \
+                        .reshape(-1, Hkv, P, 128)
+                    v_pool[flat] = vc.view(B, pages, P, Hkv, 128).permute(0, 1, 3, 2, 4) \
+                        .reshape(-1, Hkv, P, 128)
+
+                def unfused():
+                    scatter()
+                    lens.fill_(total)
+                    q.build_meta(cache, ws)
+
+                rec["scatter_plus_build_meta_us"] = round(timed(lambda: None, unfused, 8), 2)
+                rec["boxes_equal_build_meta"] = bool(torch.equal(
+                    fused_meta.view(torch.int16), cache.meta.view(torch.int16)))
+            rc, _ = q.read_status(ws)
+            rec["status"] = rc
+            print(json.dumps(rec), flush=True)
+        del cache, k_pool, v_pool, kc, vc
+        torch.cuda.empty_cache()
+
+
 def run_layers(args):
     """All 32 layers of the 128K-context model in one quest_decode_layers launch against 32
     quest_decode launches, L2 flushed before each timed step; one JSON line."""
@@ -710,6 +808,8 @@ def main():
         run_sweep(args)
     elif args.layers:
         run_layers(args)
+    elif args.prefill:
+        run_prefill(args)
     else:
         run_quest(args)
 

@@ -78,7 +78,8 @@ typedef void* quest_stream_t; /* cudaStream_t */
  *                    table.
  *   block_table    : int32 [batch][max_pages], logical page -> physical page.  Entries at
  *                    or past ceil(seq_len / page_size) are never read.
- *   seq_lens       : int32 [batch], tokens present; only quest_append writes it.
+ *   seq_lens       : int32 [batch], tokens present; written by quest_append,
+ *                    quest_prefill and the decode calls that append.
  */
 typedef struct quest_cache {
     int32_t batch;
@@ -169,6 +170,22 @@ int quest_build_meta(const quest_cache_t* cache, void* ws, size_t ws_bytes,
  */
 int quest_append(const quest_cache_t* cache, const void* k_new, const void* v_new, void* ws,
                  size_t ws_bytes, quest_stream_t stream);
+
+/*
+ * Chunked prefill with the boxes formed in the same pass.  [Guide] Solution step 1: the
+ * box is formed as pages fill during prompt prefill.  k, v: fp16
+ * [batch][n_tokens][num_kv_heads][128], token j of sequence b going to position
+ * L_b + j (L_b = seq_lens[b]; every page it reaches must be mapped in block_table).
+ * Each touched page's box becomes the per-dimension min / max over its old box (when the
+ * page already held tokens) and its new keys: the same boxes as n_tokens quest_append
+ * calls, or as quest_build_meta after the whole prompt, bit for bit.  Then seq_lens[b]
+ * becomes L_b + n_tokens.  Reads the chunk once, writes it once plus the touched boxes.
+ * A sequence with no room (L_b + n_tokens > max_pages * P) or a page outside
+ * [0, num_phys) is reported (QUEST_ERR_BAD_LENGTH / QUEST_ERR_BAD_PAGE in the status)
+ * and its length is left unchanged.  n_tokens = 0 does nothing.
+ */
+int quest_prefill(const quest_cache_t* cache, const void* k, const void* v, int32_t n_tokens,
+                  void* ws, size_t ws_bytes, quest_stream_t stream);
 
 /*
  * Query-aware criticality.  [Guide] Solution step 2, the upper-bound inequality:

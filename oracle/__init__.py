@@ -135,6 +135,15 @@ def append(c: Cache, k_new, v_new) -> None:
         raise OracleError("append: page not allocated or cache full")
 
 
+def prefill(c: Cache, k, v) -> None:
+    """Chunked prefill: n tokens per sequence ([B][n][Hkv][d]) written in token order, each
+    one exactly as ``append`` places it and widens its page's box ("Guide to Quest",
+    Solution step 1: boxes are formed as pages fill, in prefill as in generation)."""
+    kk, vv = _f32(k), _f32(v)
+    for j in range(kk.shape[1]):
+        append(c, kk[:, j], vv[:, j])
+
+
 def score(c: Cache, q) -> np.ndarray:
     """Page scores [B][Hkv][max_pages] float32 (-inf past the last page)."""
     dims = c.dims()

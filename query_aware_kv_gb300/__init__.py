@@ -10,6 +10,6 @@ from ._lib import (  # noqa: F401
     QUEST_ERR_TIMEOUT, QUEST_ERR_UNSUPPORTED, QUEST_ERR_WORKSPACE, QUEST_MAX_PAGES, QUEST_OK,
     PagedCache, QuestCacheDesc, QuestError, QuestLayer, QuestOpts, append, build_meta, decode,
     decode_layers, decode_step,
-    dense_decode, estimate, estimate_heads, load, opts, read_status, sparse_decode, topk, workspace,
+    dense_decode, estimate, estimate_heads, load, opts, prefill, read_status, sparse_decode, topk, workspace,
     workspace_init, workspace_size,
 )

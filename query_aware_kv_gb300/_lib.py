@@ -37,6 +37,7 @@ HEAD_DIM = 128
 # Every symbol include/quest.h declares.
 EXPORTS = (
     "quest_workspace_size", "quest_workspace_init", "quest_build_meta", "quest_append",
+    "quest_prefill",
     "quest_estimate", "quest_estimate_heads", "quest_topk", "quest_sparse_decode",
     "quest_decode", "quest_decode_layers",
     "quest_decode_step", "quest_dense_decode", "quest_decode_static", "quest_read_status",
@@ -100,6 +101,7 @@ def load() -> ctypes.CDLL:
             "quest_workspace_init": (ctypes.c_int, [V, SZ, V]),
             "quest_build_meta": (ctypes.c_int, [C, V, SZ, V]),
             "quest_append": (ctypes.c_int, [C, V, V, V, SZ, V]),
+            "quest_prefill": (ctypes.c_int, [C, V, V, I32, V, SZ, V]),
             "quest_estimate": (ctypes.c_int, [C, V, V, V, SZ, V]),
             "quest_estimate_heads": (ctypes.c_int, [C, V, V, V, SZ, V]),
             "quest_topk": (ctypes.c_int, [C, V, I32, V, V, V, SZ, O, V]),
@@ -254,6 +256,19 @@ def append(cache: PagedCache, k_new: torch.Tensor, v_new: torch.Tensor, ws: torc
     _need(v_new, "v_new", torch.float16, shape)
     _check(load().quest_append(ctypes.byref(cache.desc), k_new.data_ptr(), v_new.data_ptr(),
                                ws.data_ptr(), ws.numel(), _stream(stream)))
+
+
+def prefill(cache: PagedCache, k: torch.Tensor, v: torch.Tensor, ws: torch.Tensor,
+            stream=None) -> None:
+    """Write a chunk of n tokens per sequence ([B][n][Hkv][128] fp16) at seq_lens and fold
+    it into the page boxes; seq_lens grows by n."""
+    if k.dim() != 4:
+        raise ValueError("k must be [batch][n_tokens][num_kv_heads][128]")
+    shape = (cache.batch, k.shape[1], cache.num_kv_heads, HEAD_DIM)
+    _need(k, "k", torch.float16, shape)
+    _need(v, "v", torch.float16, shape)
+    _check(load().quest_prefill(ctypes.byref(cache.desc), k.data_ptr(), v.data_ptr(),
+                                int(k.shape[1]), ws.data_ptr(), ws.numel(), _stream(stream)))
 
 
 def estimate(cache: PagedCache, q: torch.Tensor, ws: torch.Tensor,

@@ -248,6 +248,24 @@ int quest_append(const quest_cache_t* cache, const void* k_new, const void* v_ne
                   "quest_append");
 }
 
+int quest_prefill(const quest_cache_t* cache, const void* k, const void* v, int32_t n_tokens,
+                  void* ws, size_t ws_bytes, quest_stream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (n_tokens < 0) return fail(QUEST_ERR_INVALID_ARG, "n_tokens must be >= 0");
+  if (cache->batch == 0 || n_tokens == 0) return QUEST_OK;
+  if ((long long)n_tokens > (long long)cache->max_pages * cache->page_size)
+    return fail(QUEST_ERR_INVALID_ARG, "n_tokens exceeds max_pages * page_size");
+  if (!k || !v || !aligned(k, 16) || !aligned(v, 16))
+    return fail(QUEST_ERR_INVALID_ARG, "k / v must be non-NULL and 16-byte aligned");
+  if ((rc = check_ws(ws, ws_bytes, sizeof(WsHeader)))) return rc;
+  const Tiling t = make_tiling(cache, 1, nullptr);
+  const Params p = make_params(cache, ws, make_layout(cache, t), t, nullptr);
+  return launched(launch_prefill(p, static_cast<const __half*>(k), static_cast<const __half*>(v),
+                                 n_tokens, static_cast<cudaStream_t>(stream)),
+                  "quest_prefill");
+}
+
 int quest_estimate(const quest_cache_t* cache, const void* q, float* scores, void* ws,
                    size_t ws_bytes, quest_stream_t stream) {
   int rc = check_cache(cache);

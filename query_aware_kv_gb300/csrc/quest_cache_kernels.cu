@@ -1,4 +1,5 @@
-// quest_cache_kernels.cu - page bounding boxes after prefill, and the decode-time append.
+// quest_cache_kernels.cu - page bounding boxes after prefill, the chunked-prefill write that
+// forms them on the fly, and the decode-time append.
 //
 // "Guide to Quest: Query-Aware KV Cache Sparsity for LLMs", Solution step 1: each page
 // is summarised by the per-dimension minimum and maximum of its keys, formed while the
@@ -134,6 +135,133 @@ __global__ void __launch_bounds__(256) append_kernel(Params p, const __half* k_n
   }
   __syncthreads();
   if (threadIdx.x == 0) p.seq_lens[b] = L + 1;
+}
+
+// Chunked prefill: n new tokens per sequence are written at slots [L, L + n) and folded
+// into their pages' boxes in the same pass ("Guide to Quest", Solution step 1: the boxes
+// are formed while pages are filled during prefill).  grid (pages a chunk can touch, B),
+// 256 threads: block (j, b) owns logical page L / P + j of sequence b; warp w takes kv
+// heads w, w + 8, ...; half-warp hw takes the page's new rows hw, hw + 2, ... and lane c
+// dims [8c, 8c + 8).  The box of a page that already held tokens is widened, otherwise
+// replaced.  k, v: fp16 [B][n][Hkv][128].  Lengths advance in prefill_lens_kernel.
+template <int P>
+__global__ void __launch_bounds__(256) prefill_kernel(Params p, const __half* k, const __half* v,
+                                                      int n) {
+  pdl_wait();
+  const int b = blockIdx.y;
+  const int L = p.seq_lens[b];
+  if (L < 0 || (long long)L + n > (long long)p.max_pages * P) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(p, QUEST_ERR_BAD_LENGTH, b, -1, kSiteAppend);
+    return;
+  }
+  const int page = L / P + (int)blockIdx.x;
+  const int t0 = max(page * P, L), t1 = min(page * P + P, L + n);  // new tokens of this page
+  if (t0 >= t1) return;  // block-uniform
+  const int phys = p.block_table[(size_t)b * p.max_pages + page];
+  if (phys < 0 || phys >= p.num_phys) {
+    if (threadIdx.x == 0) report(p, QUEST_ERR_BAD_PAGE, b, page, kSiteAppend);
+    return;
+  }
+  const bool had_tokens = page * P < L;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, hw = lane >> 4, c = lane & 15;
+  for (int g = warp; g < p.Hkv; g += 8) {
+    __half2 mn[4], mx[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mn[e] = mx[e] = __float2half2_rn(0.f);
+    bool any = false;
+    // four rows per half-warp in flight: loads first, then stores and min / max
+    for (int tb = t0 + hw; tb < t1; tb += 8) {
+      uint4 kk[4], vv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int t = tb + 2 * r;
+        if (t < t1) {
+          const size_t in = (((size_t)b * n + (t - L)) * p.Hkv + g) * kHeadDim + 8 * c;
+          kk[r] = __ldcs(reinterpret_cast<const uint4*>(k + in));
+          vv[r] = __ldcs(reinterpret_cast<const uint4*>(v + in));
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int t = tb + 2 * r;
+        if (t >= t1) break;
+        const size_t out = (((size_t)phys * p.Hkv + g) * P + (t % P)) * kHeadDim + 8 * c;
+        *reinterpret_cast<uint4*>(p.k_pool + out) = kk[r];
+        *reinterpret_cast<uint4*>(p.v_pool + out) = vv[r];
+        const uint32_t w[4] = {kk[r].x, kk[r].y, kk[r].z, kk[r].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half2 h = *reinterpret_cast<const __half2*>(&w[e]);
+          mn[e] = any ? __hmin2(mn[e], h) : h;
+          mx[e] = any ? __hmax2(mx[e], h) : h;
+        }
+        any = true;
+      }
+    }
+    // combine the two half-warps (the upper one may have no row when one row is new)
+    const bool other = __shfl_xor_sync(0xffffffffu, any ? 1 : 0, 16) != 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t a = *reinterpret_cast<uint32_t*>(&mn[q]), z = *reinterpret_cast<uint32_t*>(&mx[q]);
+      const uint32_t oa = __shfl_xor_sync(0xffffffffu, a, 16);
+      const uint32_t oz = __shfl_xor_sync(0xffffffffu, z, 16);
+      if (other) {
+        const __half2 ha = *reinterpret_cast<const __half2*>(&oa);
+        const __half2 hz = *reinterpret_cast<const __half2*>(&oz);
+        mn[q] = any ? __hmin2(mn[q], ha) : ha;
+        mx[q] = any ? __hmax2(mx[q], hz) : hz;
+      }
+    }
+    if (hw == 0) {
+      uint4* box = reinterpret_cast<uint4*>(p.meta + box_offset(p, b, g, page) + 8 * c);
+      uint4* boxmax = reinterpret_cast<uint4*>(p.meta + box_offset(p, b, g, page) + kHeadDim + 8 * c);
+      if (had_tokens) {
+        const uint4 cmn = *box, cmx = *boxmax;
+        const uint32_t a[4] = {cmn.x, cmn.y, cmn.z, cmn.w};
+        const uint32_t z[4] = {cmx.x, cmx.y, cmx.z, cmx.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mn[q] = __hmin2(mn[q], *reinterpret_cast<const __half2*>(&a[q]));
+          mx[q] = __hmax2(mx[q], *reinterpret_cast<const __half2*>(&z[q]));
+        }
+      }
+      *box = make_uint4(*reinterpret_cast<uint32_t*>(&mn[0]), *reinterpret_cast<uint32_t*>(&mn[1]),
+                        *reinterpret_cast<uint32_t*>(&mn[2]), *reinterpret_cast<uint32_t*>(&mn[3]));
+      *boxmax = make_uint4(*reinterpret_cast<uint32_t*>(&mx[0]), *reinterpret_cast<uint32_t*>(&mx[1]),
+                           *reinterpret_cast<uint32_t*>(&mx[2]), *reinterpret_cast<uint32_t*>(&mx[3]));
+    }
+  }
+}
+
+// Advances the lengths of the sequences the chunk fitted into (the same test as above).
+__global__ void prefill_lens_kernel(Params p, int n) {
+  pdl_wait();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= p.B) return;
+  const int L = p.seq_lens[b];
+  if (L < 0 || (long long)L + n > (long long)p.max_pages * p.P) return;
+  const int first = L / p.P, last = (L + n - 1) / p.P;
+  for (int pg = first; pg <= last; ++pg) {
+    const int phys = p.block_table[(size_t)b * p.max_pages + pg];
+    if (phys < 0 || phys >= p.num_phys) return;  // reported by the write kernel
+  }
+  p.seq_lens[b] = L + n;
+}
+
+cudaError_t launch_prefill(const Params& p, const __half* k, const __half* v, int n,
+                           cudaStream_t s) {
+  Params pp = p;
+  const __half* kk = k;
+  const __half* vv = v;
+  int nn = n;
+  void* args[] = {&pp, &kk, &vv, &nn};
+  const unsigned pages = (unsigned)((n + p.P - 1) / p.P + 1);
+  const void* fn = p.P == 16 ? (const void*)prefill_kernel<16> : (const void*)prefill_kernel<32>;
+  cudaError_t e = launch_pdl(fn, dim3(pages, p.B), dim3(256), 0, s, args);
+  if (e != cudaSuccess) return e;
+  void* args2[] = {&pp, &nn};
+  return launch_pdl((const void*)prefill_lens_kernel, dim3((p.B + 255) / 256), dim3(256), 0, s,
+                    args2);
 }
 
 cudaError_t launch_build_meta(const Params& p, cudaStream_t s) {

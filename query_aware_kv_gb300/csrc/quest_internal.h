@@ -155,6 +155,8 @@ cudaError_t launch_append(const Params& p, const __half* k_new, const __half* v_
                           cudaStream_t s);
 cudaError_t launch_estimate(const Params& p, int G, bool per_head, cudaStream_t s);
 cudaError_t launch_topk_union(const Params& p, int row_cap, cudaStream_t s);
+cudaError_t launch_prefill(const Params& p, const __half* k, const __half* v, int n,
+                           cudaStream_t s);
 cudaError_t launch_topk(const Params& p, cudaStream_t s);
 cudaError_t launch_decode(const Params& p, int G, cudaStream_t s);
 cudaError_t launch_fused(const Params& p, int G, int max_ctas, cudaStream_t s);

@@ -123,6 +123,21 @@ def test_calls_reject_bad_arguments_without_launching(lib):
     assert lib.quest_append(ctypes.byref(d3), 16, 16, 256, 1 << 20, None) == q.QUEST_OK
 
 
+def test_prefill_rejects_bad_arguments_without_launching(lib):
+    d = desc()
+    ws = ctypes.create_string_buffer(1 << 12)
+    assert lib.quest_prefill(ctypes.byref(d), 16, 16, -1, ws, 1 << 12, None) == \
+        q.QUEST_ERR_INVALID_ARG
+    assert lib.quest_prefill(ctypes.byref(d), 16, 16, 64 * 16 + 1, ws, 1 << 12, None) == \
+        q.QUEST_ERR_INVALID_ARG
+    assert lib.quest_prefill(ctypes.byref(d), 16, 24, 8, ws, 1 << 12, None) == \
+        q.QUEST_ERR_INVALID_ARG
+    assert "aligned" in lib.quest_last_error().decode()
+    assert lib.quest_prefill(ctypes.byref(d), 16, 16, 8, None, 0, None) == q.QUEST_ERR_WORKSPACE
+    # an empty chunk is a no-op, so it touches nothing
+    assert lib.quest_prefill(ctypes.byref(d), 16, 16, 0, None, 0, None) == q.QUEST_OK
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     from query_aware_kv_gb300 import _lib
     monkeypatch.setattr(_lib, "_lib", None)

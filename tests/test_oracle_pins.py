@@ -564,3 +564,31 @@ def test_append_past_capacity_is_an_error():
     assert c.block_table.shape[1] == 2
     with pytest.raises(oracle.OracleError):
         oracle.append(c, np.zeros((1, 4, 128)), np.zeros((1, 4, 128)))
+
+
+def test_chunked_prefill_boxes_are_the_prompt_boxes():
+    """Chunks of 5, 16 and 40 tokens from lengths 0 and 7: every page's box is the
+    per-dimension min / max of its keys (numpy reduction over the final pool), stale
+    boxes of fresh pages are replaced, and each token sits at its position."""
+    w, c = make(lens=(0, 7), batch=2, steps=61, hq=4, hkv=2)
+    c.meta[...] = 1e4  # stale boxes on every page that holds no token yet
+    oracle.build_meta(c)  # boxes the 7 rows sequence 1 holds before the chunks
+    kc = w.k_new.permute(1, 0, 2, 3).float().numpy()  # [B][61][Hkv][d]
+    vc = w.v_new.permute(1, 0, 2, 3).float().numpy()
+    done = 0
+    for n in (5, 16, 40):
+        oracle.prefill(c, kc[:, done:done + n], vc[:, done:done + n])
+        done += n
+    assert c.seq_lens.tolist() == [61, 68]
+    for b, L0 in ((0, 0), (1, 7)):
+        for t in (0, 4, 5, 20, 60):
+            pos = L0 + t
+            phys = int(c.block_table[b, pos // 16])
+            np.testing.assert_array_equal(c.k_pool[phys, :, pos % 16], kc[b, t])
+            np.testing.assert_array_equal(c.v_pool[phys, :, pos % 16], vc[b, t])
+        for p in range(wl.pages_for(int(c.seq_lens[b]), 16)):
+            phys = int(c.block_table[b, p])
+            for g in range(2):
+                keys = logical_keys(c, b, g, p)
+                np.testing.assert_array_equal(c.meta[phys, g, 0], keys.min(axis=0))
+                np.testing.assert_array_equal(c.meta[phys, g, 1], keys.max(axis=0))
