@@ -139,55 +139,64 @@ __global__ void __launch_bounds__(256) append_kernel(Params p, const __half* k_n
 
 // Chunked prefill: n new tokens per sequence are written at slots [L, L + n) and folded
 // into their pages' boxes in the same pass ("Guide to Quest", Solution step 1: the boxes
-// are formed while pages are filled during prefill).  grid (pages a chunk can touch, B),
-// 256 threads: block (j, b) owns logical page L / P + j of sequence b; warp w takes kv
-// heads w, w + 8, ...; half-warp hw takes the page's new rows hw, hw + 2, ... and lane c
-// dims [8c, 8c + 8).  The box of a page that already held tokens is widened, otherwise
-// replaced.  k, v: fp16 [B][n][Hkv][128].  Lengths advance in prefill_lens_kernel.
+// are formed while pages are filled during prefill).  grid (ceil(Hkv / 4), pages a chunk
+// can touch, B), 128 threads: block (z, j, b) owns logical page L / P + j of sequence b,
+// warp w its kv head 4z + w.  Heads vary fastest across blocks, so that the blocks in
+// flight read whole token rows of the chunk and write whole physical pages.  Half-warp hw takes the page's new rows hw, hw + 2, ... and
+// lane c dims [8c, 8c + 8); all of a half-warp's rows (8 at a time) are loaded before any
+// is stored, so that a warp keeps 8 KB in flight.  The box of a page that already held
+// tokens is widened, otherwise replaced.  k, v: fp16 [B][n][Hkv][128].  Lengths advance
+// in prefill_lens_kernel.
+constexpr int kPrefillWarps = 4;
+
 template <int P>
-__global__ void __launch_bounds__(256) prefill_kernel(Params p, const __half* k, const __half* v,
-                                                      int n) {
+__global__ void __launch_bounds__(32 * kPrefillWarps) prefill_kernel(Params p, const __half* k,
+                                                                     const __half* v, int n) {
   pdl_wait();
-  const int b = blockIdx.y;
+  const int b = blockIdx.z;
+  const int g = blockIdx.x * kPrefillWarps + (threadIdx.x >> 5);
   const int L = p.seq_lens[b];
   if (L < 0 || (long long)L + n > (long long)p.max_pages * P) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) report(p, QUEST_ERR_BAD_LENGTH, b, -1, kSiteAppend);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+      report(p, QUEST_ERR_BAD_LENGTH, b, -1, kSiteAppend);
     return;
   }
-  const int page = L / P + (int)blockIdx.x;
+  const int page = L / P + (int)blockIdx.y;
   const int t0 = max(page * P, L), t1 = min(page * P + P, L + n);  // new tokens of this page
-  if (t0 >= t1) return;  // block-uniform
+  if (t0 >= t1 || g >= p.Hkv) return;  // warp-uniform; no block barrier below
   const int phys = p.block_table[(size_t)b * p.max_pages + page];
   if (phys < 0 || phys >= p.num_phys) {
-    if (threadIdx.x == 0) report(p, QUEST_ERR_BAD_PAGE, b, page, kSiteAppend);
+    if ((threadIdx.x & 31) == 0 && g == 0) report(p, QUEST_ERR_BAD_PAGE, b, page, kSiteAppend);
     return;
   }
-  const bool had_tokens = page * P < L;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, hw = lane >> 4, c = lane & 15;
-  for (int g = warp; g < p.Hkv; g += 8) {
-    __half2 mn[4], mx[4];
+  const int lane = threadIdx.x & 31, hw = lane >> 4, c = lane & 15;
+  const size_t in_stride = (size_t)p.Hkv * kHeadDim;  // one token of the chunk
+  const __half* kin = k + ((size_t)b * n * p.Hkv + g) * kHeadDim + 8 * c;
+  const __half* vin = v + ((size_t)b * n * p.Hkv + g) * kHeadDim + 8 * c;
+  __half* kout = p.k_pool + ((size_t)phys * p.Hkv + g) * P * kHeadDim + 8 * c;
+  __half* vout = p.v_pool + ((size_t)phys * p.Hkv + g) * P * kHeadDim + 8 * c;
+  __half2 mn[4], mx[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) mn[e] = mx[e] = __float2half2_rn(0.f);
-    bool any = false;
-    // four rows per half-warp in flight: loads first, then stores and min / max
-    for (int tb = t0 + hw; tb < t1; tb += 8) {
-      uint4 kk[4], vv[4];
+  for (int e = 0; e < 4; ++e) mn[e] = mx[e] = __float2half2_rn(0.f);
+  bool any = false;
+  constexpr int R = 8;
+#pragma unroll 1
+  for (int tb = t0 + hw; tb < t1; tb += 2 * R) {
+    uint4 kk[R], vv[R];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int t = tb + 2 * r;
-        if (t < t1) {
-          const size_t in = (((size_t)b * n + (t - L)) * p.Hkv + g) * kHeadDim + 8 * c;
-          kk[r] = __ldcs(reinterpret_cast<const uint4*>(k + in));
-          vv[r] = __ldcs(reinterpret_cast<const uint4*>(v + in));
-        }
+    for (int r = 0; r < R; ++r) {
+      const int t = tb + 2 * r;
+      if (t < t1) {
+        kk[r] = __ldcs(reinterpret_cast<const uint4*>(kin + (size_t)(t - L) * in_stride));
+        vv[r] = __ldcs(reinterpret_cast<const uint4*>(vin + (size_t)(t - L) * in_stride));
       }
+    }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int t = tb + 2 * r;
-        if (t >= t1) break;
-        const size_t out = (((size_t)phys * p.Hkv + g) * P + (t % P)) * kHeadDim + 8 * c;
-        *reinterpret_cast<uint4*>(p.k_pool + out) = kk[r];
-        *reinterpret_cast<uint4*>(p.v_pool + out) = vv[r];
+    for (int r = 0; r < R; ++r) {
+      const int t = tb + 2 * r;
+      if (t < t1) {
+        __stcs(reinterpret_cast<uint4*>(kout + (size_t)(t % P) * kHeadDim), kk[r]);
+        __stcs(reinterpret_cast<uint4*>(vout + (size_t)(t % P) * kHeadDim), vv[r]);
         const uint32_t w[4] = {kk[r].x, kk[r].y, kk[r].z, kk[r].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -198,54 +207,59 @@ __global__ void __launch_bounds__(256) prefill_kernel(Params p, const __half* k,
         any = true;
       }
     }
-    // combine the two half-warps (the upper one may have no row when one row is new)
-    const bool other = __shfl_xor_sync(0xffffffffu, any ? 1 : 0, 16) != 0;
+  }
+  // combine the two half-warps (the upper one has no row when the page gets one token)
+  const bool other = __shfl_xor_sync(0xffffffffu, any ? 1 : 0, 16) != 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t a = *reinterpret_cast<uint32_t*>(&mn[q]), z = *reinterpret_cast<uint32_t*>(&mx[q]);
-      const uint32_t oa = __shfl_xor_sync(0xffffffffu, a, 16);
-      const uint32_t oz = __shfl_xor_sync(0xffffffffu, z, 16);
-      if (other) {
-        const __half2 ha = *reinterpret_cast<const __half2*>(&oa);
-        const __half2 hz = *reinterpret_cast<const __half2*>(&oz);
-        mn[q] = any ? __hmin2(mn[q], ha) : ha;
-        mx[q] = any ? __hmax2(mx[q], hz) : hz;
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t a = *reinterpret_cast<uint32_t*>(&mn[e]), z = *reinterpret_cast<uint32_t*>(&mx[e]);
+    const uint32_t oa = __shfl_xor_sync(0xffffffffu, a, 16);
+    const uint32_t oz = __shfl_xor_sync(0xffffffffu, z, 16);
+    if (other) {
+      const __half2 ha = *reinterpret_cast<const __half2*>(&oa);
+      const __half2 hz = *reinterpret_cast<const __half2*>(&oz);
+      mn[e] = any ? __hmin2(mn[e], ha) : ha;
+      mx[e] = any ? __hmax2(mx[e], hz) : hz;
+    }
+  }
+  if (hw == 0) {
+    uint4* bmin = reinterpret_cast<uint4*>(p.meta + box_offset(p, b, g, page) + 8 * c);
+    uint4* bmax = reinterpret_cast<uint4*>(p.meta + box_offset(p, b, g, page) + kHeadDim + 8 * c);
+    if (page * P < L) {  // the page already held tokens: widen its box
+      const uint4 cmn = *bmin, cmx = *bmax;
+      const uint32_t a[4] = {cmn.x, cmn.y, cmn.z, cmn.w};
+      const uint32_t z[4] = {cmx.x, cmx.y, cmx.z, cmx.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        mn[e] = __hmin2(mn[e], *reinterpret_cast<const __half2*>(&a[e]));
+        mx[e] = __hmax2(mx[e], *reinterpret_cast<const __half2*>(&z[e]));
       }
     }
-    if (hw == 0) {
-      uint4* box = reinterpret_cast<uint4*>(p.meta + box_offset(p, b, g, page) + 8 * c);
-      uint4* boxmax = reinterpret_cast<uint4*>(p.meta + box_offset(p, b, g, page) + kHeadDim + 8 * c);
-      if (had_tokens) {
-        const uint4 cmn = *box, cmx = *boxmax;
-        const uint32_t a[4] = {cmn.x, cmn.y, cmn.z, cmn.w};
-        const uint32_t z[4] = {cmx.x, cmx.y, cmx.z, cmx.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mn[q] = __hmin2(mn[q], *reinterpret_cast<const __half2*>(&a[q]));
-          mx[q] = __hmax2(mx[q], *reinterpret_cast<const __half2*>(&z[q]));
-        }
-      }
-      *box = make_uint4(*reinterpret_cast<uint32_t*>(&mn[0]), *reinterpret_cast<uint32_t*>(&mn[1]),
-                        *reinterpret_cast<uint32_t*>(&mn[2]), *reinterpret_cast<uint32_t*>(&mn[3]));
-      *boxmax = make_uint4(*reinterpret_cast<uint32_t*>(&mx[0]), *reinterpret_cast<uint32_t*>(&mx[1]),
-                           *reinterpret_cast<uint32_t*>(&mx[2]), *reinterpret_cast<uint32_t*>(&mx[3]));
-    }
+    *bmin = make_uint4(*reinterpret_cast<uint32_t*>(&mn[0]), *reinterpret_cast<uint32_t*>(&mn[1]),
+                       *reinterpret_cast<uint32_t*>(&mn[2]), *reinterpret_cast<uint32_t*>(&mn[3]));
+    *bmax = make_uint4(*reinterpret_cast<uint32_t*>(&mx[0]), *reinterpret_cast<uint32_t*>(&mx[1]),
+                       *reinterpret_cast<uint32_t*>(&mx[2]), *reinterpret_cast<uint32_t*>(&mx[3]));
   }
 }
 
-// Advances the lengths of the sequences the chunk fitted into (the same test as above).
-__global__ void prefill_lens_kernel(Params p, int n) {
+// Advances the lengths of the sequences the chunk fitted into (the same tests as above).
+// One block per sequence; its threads check the block-table entries of the touched pages
+// side by side (a serial scan of a long chunk's pages by one thread cost ~150 us).
+__global__ void __launch_bounds__(256) prefill_lens_kernel(Params p, int n) {
   pdl_wait();
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= p.B) return;
+  const int b = blockIdx.x;
   const int L = p.seq_lens[b];
-  if (L < 0 || (long long)L + n > (long long)p.max_pages * p.P) return;
-  const int first = L / p.P, last = (L + n - 1) / p.P;
-  for (int pg = first; pg <= last; ++pg) {
-    const int phys = p.block_table[(size_t)b * p.max_pages + pg];
-    if (phys < 0 || phys >= p.num_phys) return;  // reported by the write kernel
+  const bool fits = L >= 0 && (long long)L + n <= (long long)p.max_pages * p.P;
+  int bad = 0;
+  if (fits) {
+    const int first = L / p.P, last = (L + n - 1) / p.P;
+    for (int pg = first + (int)threadIdx.x; pg <= last; pg += blockDim.x) {
+      const int phys = p.block_table[(size_t)b * p.max_pages + pg];
+      bad |= phys < 0 || phys >= p.num_phys;  // reported by the write kernel
+    }
   }
-  p.seq_lens[b] = L + n;
+  bad = __syncthreads_or(bad);
+  if (fits && !bad && threadIdx.x == 0) p.seq_lens[b] = L + n;
 }
 
 cudaError_t launch_prefill(const Params& p, const __half* k, const __half* v, int n,
@@ -257,11 +271,11 @@ cudaError_t launch_prefill(const Params& p, const __half* k, const __half* v, in
   void* args[] = {&pp, &kk, &vv, &nn};
   const unsigned pages = (unsigned)((n + p.P - 1) / p.P + 1);
   const void* fn = p.P == 16 ? (const void*)prefill_kernel<16> : (const void*)prefill_kernel<32>;
-  cudaError_t e = launch_pdl(fn, dim3(pages, p.B), dim3(256), 0, s, args);
+  cudaError_t e = launch_pdl(fn, dim3((p.Hkv + kPrefillWarps - 1) / kPrefillWarps, pages, p.B),
+                             dim3(32 * kPrefillWarps), 0, s, args);
   if (e != cudaSuccess) return e;
   void* args2[] = {&pp, &nn};
-  return launch_pdl((const void*)prefill_lens_kernel, dim3((p.B + 255) / 256), dim3(256), 0, s,
-                    args2);
+  return launch_pdl((const void*)prefill_lens_kernel, dim3(p.B), dim3(256), 0, s, args2);
 }
 
 cudaError_t launch_build_meta(const Params& p, cudaStream_t s) {
