@@ -865,21 +865,26 @@ __global__ void __launch_bounds__(kDecodeThreads, (P == 16 && G <= 4) ? 2 : 1)
   if (threadIdx.x == 0) {
     int slot_last = kTraceSlots - 1;
     ctrace(p, &slot_last, kCtExit, r.rank, kTraceSlots);
-    __threadfence();
-    if (atomicAdd(p.exited, 1u) == gridDim.x - 1u) {
-      // every CTA is done: advance the lengths of the sequences that received a token
-      if (p.k_new != nullptr) {
-        for (int b = 0; b < p.B; ++b) {
-          const int L0 = p.seq_lens[b];
-          if (L0 < 0 || (long long)L0 + 1 > (long long)p.max_pages * p.P) {
-            report(p, QUEST_ERR_BAD_LENGTH, b, -1, kSiteAppend);
-            continue;
-          }
-          const int phys = p.block_table[(size_t)b * p.max_pages + L0 / p.P];
-          if (phys >= 0 && phys < p.num_phys) p.seq_lens[b] = L0 + 1;
+  }
+  // With an appended token, the last CTA to leave advances the lengths (pairs past the
+  // shared-memory cache read seq_lens as they go), one sequence per lane of its warp 0.
+  if (p.k_new != nullptr && threadIdx.x < 32) {
+    unsigned last = 0;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      last = atomicAdd(p.exited, 1u) == gridDim.x - 1u;
+    }
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+      for (int b = threadIdx.x; b < p.B; b += 32) {
+        const int L0 = p.seq_lens[b];
+        if (L0 < 0 || (long long)L0 + 1 > (long long)p.max_pages * p.P) {
+          report(p, QUEST_ERR_BAD_LENGTH, b, -1, kSiteAppend);
+          continue;
         }
+        const int phys = p.block_table[(size_t)b * p.max_pages + L0 / p.P];
+        if (phys >= 0 && phys < p.num_phys) p.seq_lens[b] = L0 + 1;
       }
-      *p.exited = 0u;
+      if (threadIdx.x == 0) *p.exited = 0u;
     }
   }
 }
