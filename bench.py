@@ -557,9 +557,12 @@ def run_sweep(args):
         cnt = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
         qv = w.q[0]
         reps = 64 if name != "tiny" else 256
-        o = q.opts(cluster_size=args.cluster_size)
+        o = q.opts(cluster_size=args.cluster_size, path=q.QUEST_PATH_FUSED)
         fused = timed(lambda: q.decode(cache, qv, K, ws, o, out=out, lse=lse, idx_out=idx,
                                        count_out=cnt), reps)
+        # the library's own choice between the one-launch kernel and the chain
+        auto_us = timed(lambda: q.decode(cache, qv, K, ws, None, out=out, lse=lse, idx_out=idx,
+                                         count_out=cnt), reps)
         L = [int(x) for x in cache.seq_lens.cpu().tolist()]
         tok = selected_tokens(idx, cnt, L, P)
         nbytes = decode_bytes(L, tok, B, Hq, Hkv, page=P)
@@ -608,7 +611,8 @@ def run_sweep(args):
             "workload": name, "cluster_size": args.cluster_size, "batch": B, "num_q_heads": Hq,
             "num_kv_heads": Hkv,
             "page_size": P, "top_k_pages": K, "seq_lens_mean": round(sum(L) / len(L), 1),
-            "quest_decode_us": round(fused, 2), "algorithmic_bytes": nbytes,
+            "quest_decode_us": round(fused, 2), "quest_decode_auto_us": round(auto_us, 2),
+            "algorithmic_bytes": nbytes,
             "gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
             "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
             "unfused_chain_us": round(chain_us, 2), "append_plus_len_reset_us": round(append_us, 2),

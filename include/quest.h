@@ -132,7 +132,22 @@ typedef struct quest_opts {
                                  ([Guide] Best Practices step 2), written to idx rows of
                                  min(G * top_k, max_pages) entries.  Not with sink / local
                                  pages; the fused calls answer QUEST_ERR_UNSUPPORTED.        */
+    int32_t path;             /* quest_decode / quest_decode_step: QUEST_PATH_*.  The chain
+                                 computes the same step as separate append, estimate, top-K
+                                 and sparse-decode kernels (selection kept in the workspace
+                                 unless idx_out / count_out are given).                     */
 } quest_opts_t;
+
+/* Values of quest_opts_t.path.  AUTO (0) takes the one-launch kernel unless it would run
+ * with a single CTA per SM (a CTA needs more than half an SM's shared memory), or with one
+ * CTA per (sequence, kv head) while the pair's boxes weigh at least twice its kept K/V
+ * (max_pages boxes against top_k pages): there the pair's serial scoring and selection
+ * cost more than three launches whose scoring and selection run across the whole GPU.
+ * AUTO always takes the one-launch kernel when cluster_size, trace or debug_flags is set,
+ * and the chain when no cluster of the one-launch kernel fits in shared memory. */
+#define QUEST_PATH_AUTO 0
+#define QUEST_PATH_FUSED 1
+#define QUEST_PATH_CHAIN 2
 
 /* quest_decode only: never publish the selection, so that every decode work item's
  * bounded wait runs out and the call reports QUEST_ERR_TIMEOUT.  For testing the

@@ -32,6 +32,7 @@ QUEST_ERR_BAD_SELECTION = 8
 QUEST_MAX_PAGES = 16384
 QUEST_DEBUG_WITHHOLD_SELECTION = 1
 QUEST_DEBUG_QUEUE_KERNEL = 2
+QUEST_PATH_AUTO, QUEST_PATH_FUSED, QUEST_PATH_CHAIN = 0, 1, 2
 HEAD_DIM = 128
 
 # Every symbol include/quest.h declares.
@@ -75,6 +76,7 @@ class QuestOpts(ctypes.Structure):
         ("trace_capacity", ctypes.c_int32), ("trace", ctypes.c_void_p),
         ("cluster_size", ctypes.c_int32), ("sink_pages", ctypes.c_int32),
         ("local_pages", ctypes.c_int32), ("gqa_union", ctypes.c_int32),
+        ("path", ctypes.c_int32),
     ]
 
 
@@ -155,17 +157,19 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
 def opts(pages_per_split: int = 0, score_tile_pages: int = 0, max_ctas: int = 0,
          debug_flags: int = 0, wait_limit_ns: int = 0, decode_lag: int = 0,
          trace: Optional[torch.Tensor] = None, cluster_size: int = 0, sink_pages: int = 0,
-         local_pages: int = 0, gqa_union: bool = False) -> QuestOpts:
+         local_pages: int = 0, gqa_union: bool = False, path: int = 0) -> QuestOpts:
     """Launch tuning (0 = default).  ``trace``: int64 CUDA tensor of 1 + 2n elements whose
     first element is zero; receives up to n timeline records of the fused kernel.
     ``sink_pages`` / ``local_pages``: pages always kept at the start / end of a sequence
-    longer than top_k pages."""
+    longer than top_k pages.  ``path``: QUEST_PATH_AUTO / _FUSED / _CHAIN for the decode
+    calls."""
     cap, ptr = 0, None
     if trace is not None:
         _need(trace, "trace", torch.int64)
         cap, ptr = (trace.numel() - 1) // 2, trace.data_ptr()
     o = QuestOpts(pages_per_split, score_tile_pages, max_ctas, debug_flags, wait_limit_ns,
-                  decode_lag, cap, ptr, cluster_size, sink_pages, local_pages, int(gqa_union))
+                  decode_lag, cap, ptr, cluster_size, sink_pages, local_pages, int(gqa_union),
+                  int(path))
     o._trace_ref = trace  # keep the buffer alive with the options
     return o
 

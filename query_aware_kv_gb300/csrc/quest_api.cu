@@ -401,7 +401,30 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   if (cs < 0 || cs > kMaxClusterSize)
     return fail(QUEST_ERR_INVALID_ARG, "cluster_size %d: use 0 (automatic) or 1..%d", cs,
                 kMaxClusterSize);
-  if (!cluster_any_fits(group_of(cache), cache->page_size, cache->max_pages, top_k))
+  const int path = opts ? opts->path : QUEST_PATH_AUTO;
+  if (path < QUEST_PATH_AUTO || path > QUEST_PATH_CHAIN)
+    return fail(QUEST_ERR_INVALID_ARG, "path %d: use QUEST_PATH_AUTO, _FUSED or _CHAIN", path);
+  const bool fits = cluster_any_fits(group_of(cache), cache->page_size, cache->max_pages, top_k);
+  bool chain = path == QUEST_PATH_CHAIN;
+  if (path == QUEST_PATH_AUTO && cs == 0 && !(opts && (opts->trace || opts->debug_flags))) {
+    bool fused = false;
+    cudaError_t e = fits ? cluster_preferred(p, group_of(cache), 1, &fused) : cudaSuccess;
+    if (e != cudaSuccess) return launched(e, what);
+    chain = !fused;
+  }
+  if (chain) {
+    // the same step as separate kernels: append, estimate, top-K, sparse decode (the
+    // selection goes to idx_out / count_out if given, else to the workspace)
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int G = group_of(cache);
+    cudaError_t e = cudaSuccess;
+    if (p.k_new) e = launch_append(p, p.k_new, p.v_new, s);
+    if (e == cudaSuccess) e = launch_estimate(p, G, false, s);
+    if (e == cudaSuccess) e = launch_topk(p, s);
+    if (e == cudaSuccess) e = launch_decode(p, G, s);
+    return launched(e, what);
+  }
+  if (!fits)
     return fail(QUEST_ERR_UNSUPPORTED, "max_pages %d needs more shared memory than a CTA has",
                 cache->max_pages);
   if (cs > 0 &&

@@ -990,6 +990,24 @@ cudaError_t choose_cluster_size(int G, int P, int max_pages, int top_k, int nbg,
 
 }  // namespace
 
+cudaError_t cluster_preferred(const Params& p, int G, int n_layers, bool* out) {
+  const int nbg = n_layers * p.B * p.Hkv;
+  int cs = 0;
+  cudaError_t e = choose_cluster_size(G, p.P, p.max_pages, p.top_k, nbg, &cs);
+  if (e != cudaSuccess) return e;
+  const void* fn = pick_cluster(G, p.P);
+  const size_t smem = cluster_smem_bytes(G, p.P, p.max_pages, cs, p.top_k);
+  if ((e = ensure_smem(fn, smem)) != cudaSuccess) return e;
+  int per_sm = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDecodeThreads, smem)) !=
+      cudaSuccess)
+    return e;
+  const long long boxes = (long long)p.max_pages * 2 * kHeadDim * 2;
+  const long long kept = (long long)std::min(p.top_k, p.max_pages) * p.P * 2 * kHeadDim * 2;
+  *out = per_sm >= 2 && !(cs == 1 && boxes >= 2 * kept);
+  return cudaSuccess;
+}
+
 bool cluster_any_fits(int G, int P, int max_pages, int top_k) {
   for (int cs = 1; cs <= kMaxClusterSize; ++cs)
     if (cluster_smem_bytes(G, P, max_pages, cs, top_k) <= kMaxSmem) return true;

@@ -157,6 +157,8 @@ cudaError_t launch_estimate(const Params& p, int G, bool per_head, cudaStream_t 
 cudaError_t launch_topk_union(const Params& p, int row_cap, cudaStream_t s);
 cudaError_t launch_prefill(const Params& p, const __half* k, const __half* v, int n,
                            cudaStream_t s);
+// Whether QUEST_PATH_AUTO takes the one-launch cluster kernel for this step (see quest.h).
+cudaError_t cluster_preferred(const Params& p, int G, int n_layers, bool* out);
 cudaError_t launch_topk(const Params& p, cudaStream_t s);
 cudaError_t launch_decode(const Params& p, int G, cudaStream_t s);
 cudaError_t launch_fused(const Params& p, int G, int max_ctas, cudaStream_t s);

@@ -123,6 +123,15 @@ def test_calls_reject_bad_arguments_without_launching(lib):
     assert lib.quest_append(ctypes.byref(d3), 16, 16, 256, 1 << 20, None) == q.QUEST_OK
 
 
+def test_decode_rejects_unknown_path(lib):
+    d = desc()
+    o = q.opts(path=3)
+    ws = ctypes.c_void_p(1 << 20)  # never dereferenced: the call fails before any launch
+    assert lib.quest_decode(ctypes.byref(d), 16, 16, 16, 256, 256, 256, ws,
+                            1 << 40, ctypes.byref(o), None) == q.QUEST_ERR_INVALID_ARG
+    assert "path" in lib.quest_last_error().decode()
+
+
 def test_prefill_rejects_bad_arguments_without_launching(lib):
     d = desc()
     ws = ctypes.create_string_buffer(1 << 12)

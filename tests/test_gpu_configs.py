@@ -8,10 +8,15 @@ CPU oracle on the same seeded inputs.  Acceptance rules as in tests/harness.py:
   the GPU's selected pages;
 * lengths, appended rows and boxes: bit-exact (checked on the last step);
 * planted needle pages are selected.
+
+The decode calls choose between the one-launch kernel and the chain of separate kernels
+(QUEST_PATH_AUTO); the larger workloads run both through that choice and through the
+one-launch kernel.
 """
 import pytest
 import torch
 
+import query_aware_kv_gb300 as q
 from query_aware_kv_gb300 import workloads as wl
 
 import harness as H
@@ -19,11 +24,16 @@ import harness as H
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, steps, check_needles=True):
+PATHS = [q.QUEST_PATH_AUTO, q.QUEST_PATH_FUSED]
+PATH_IDS = ["auto", "fused"]
+
+
+def _run(w, steps, check_needles=True, path=q.QUEST_PATH_AUTO):
     pair = H.on_device(w)
+    o = q.opts(path=path)
     for t in range(steps):
-        H.run_step_and_compare(pair, t, w.top_k, one_launch=True, check_needles=check_needles,
-                               check_cache=(t == steps - 1))
+        H.run_step_and_compare(pair, t, w.top_k, opts=o, one_launch=True,
+                               check_needles=check_needles, check_cache=(t == steps - 1))
 
 
 def test_longchat_32k_every_step():
@@ -33,24 +43,28 @@ def test_longchat_32k_every_step():
     _run(w, w.steps)
 
 
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("budget", [256, 512, 1024, 2048, 4096])
-def test_batched_ragged(budget):
-    """8 sequences of 8K-32K tokens, 32 heads, the five budgets; four decode steps."""
+def test_batched_ragged(budget, path):
+    """8 sequences of 8K-32K tokens, 32 heads, the five budgets; four decode steps, through
+    the automatic path choice and through the one-launch kernel."""
     w = wl.batched_ragged(seed=0, device="cuda", budget=budget, steps=4)
-    _run(w, w.steps, check_needles=False)
+    _run(w, w.steps, check_needles=False, path=path)
 
 
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("layer,budget", [(0, 1024), (13, 2048), (31, 2048)])
-def test_yarn_128k_layers(layer, budget):
+def test_yarn_128k_layers(layer, budget, path):
     """Single layers of the 128K-context model (8192 pages per head); each head's needle
     page must be kept."""
     w = wl.yarn_128k_layer(layer, seed=0, device="cuda", budget=budget)
-    _run(w, 1)
+    _run(w, 1, path=path)
 
 
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("page_size", [16, 32])
-def test_gqa_llama31(page_size):
+def test_gqa_llama31(page_size, path):
     """4 sequences of 64K tokens, 32 query / 8 kv heads, budget 4096, page 16 and 32."""
     w = wl.gqa_llama31(seed=0, device="cuda", page_size=page_size)
-    _run(w, 1, check_needles=False)
+    _run(w, 1, check_needles=False, path=path)
     torch.cuda.empty_cache()

@@ -306,14 +306,37 @@ def test_decode_steps_match_oracle(geom, fused):
         H.run_step_and_compare(pair, t, w.top_k, fused=fused)
 
 
+@pytest.mark.parametrize("path", [q.QUEST_PATH_FUSED, q.QUEST_PATH_CHAIN], ids=["fused", "chain"])
 @pytest.mark.parametrize("geom", GEOMS, ids=lambda g: f"hq{g['hq']}_hkv{g['hkv']}_p{g['P']}")
-def test_one_launch_step_matches_oracle(geom):
-    """quest_decode_step: append folded into the fused kernel; boxes, pools, lengths,
-    selection and attention all match the oracle step after step (pages open and fill)."""
+def test_one_launch_step_matches_oracle(geom, path):
+    """quest_decode_step, as the one-launch kernel (append folded in) and as the chain of
+    separate kernels: boxes, pools, lengths, selection and attention all match the oracle
+    step after step (pages open and fill)."""
     w = small(lens=(1500, 1, 333, 0, 16 * 30 - 2), batch=5, steps=20, outliers=4, **geom)
     pair = H.on_device(w)
+    o = q.opts(path=path)
     for t in range(w.steps):
-        H.run_step_and_compare(pair, t, w.top_k, one_launch=True, check_cache=(t % 5 == 4))
+        H.run_step_and_compare(pair, t, w.top_k, opts=o, one_launch=True,
+                               check_cache=(t % 5 == 4))
+
+
+def test_chain_path_window_and_no_selection_outputs():
+    """The chain path honours sink / local pages and runs without idx_out / count_out (the
+    selection then stays in the workspace)."""
+    w = small(lens=(3000, 700), batch=2, hq=8, hkv=4, steps=2, budget=256, outliers=4)
+    pair = H.on_device(w)
+    o = q.opts(path=q.QUEST_PATH_CHAIN, sink_pages=2, local_pages=3)
+    H.run_step_and_compare(pair, 0, w.top_k, opts=o, one_launch=True, sink=2, local=3,
+                           check_cache=True)
+    out, lse = q.decode_step(pair.cache, w.q[1].cuda(), w.k_new[1].cuda(), w.v_new[1].cuda(),
+                             w.top_k, pair.ws, o)
+    oracle.append(pair.ref, w.k_new[1].numpy(), w.v_new[1].numpy())
+    H.assert_status_ok(pair.ws)
+    qh = w.q[1].numpy().astype(np.float32)
+    ref_scores = oracle.score(pair.ref, qh)
+    ri, rc = oracle.topk(pair.ref, ref_scores, w.top_k, 2, 3)
+    out_ref, lse_ref = oracle.attend(pair.ref, qh, ri, rc)
+    H.assert_attention_close(out, lse, out_ref, lse_ref)
 
 
 def test_tiny_config():
