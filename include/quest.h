@@ -140,7 +140,7 @@ typedef struct quest_opts {
 
 /* Values of quest_opts_t.path.  AUTO (0) takes the one-launch kernel unless it would run
  * with a single CTA per SM (a CTA needs more than half an SM's shared memory), or with one
- * CTA per (sequence, kv head) while the pair's boxes weigh at least twice its kept K/V
+ * CTA per (sequence, kv head) while the pair's boxes weigh at least 1.5 times its kept K/V
  * (max_pages boxes against top_k pages): there the pair's serial scoring and selection
  * cost more than three launches whose scoring and selection run across the whole GPU.
  * AUTO always takes the one-launch kernel when cluster_size, trace or debug_flags is set,

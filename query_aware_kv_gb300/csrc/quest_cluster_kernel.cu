@@ -1004,7 +1004,7 @@ cudaError_t cluster_preferred(const Params& p, int G, int n_layers, bool* out) {
     return e;
   const long long boxes = (long long)p.max_pages * 2 * kHeadDim * 2;
   const long long kept = (long long)std::min(p.top_k, p.max_pages) * p.P * 2 * kHeadDim * 2;
-  *out = per_sm >= 2 && !(cs == 1 && boxes >= 2 * kept);
+  *out = per_sm >= 2 && !(cs == 1 && 2 * boxes >= 3 * kept);
   return cudaSuccess;
 }
 

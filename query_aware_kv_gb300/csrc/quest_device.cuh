@@ -495,7 +495,7 @@ __device__ __forceinline__ int block_excl_sum(int v, int* tot) {
 // level and the marking pass through one loop keeps the code small: this routine runs once
 // per launch and its first pass waits for instruction fetches.
 // hist: 2 * kTopkBins ints, zero on entry (left zero); bits: 2 * ceil(N / 32) words;
-// scratch: 64 ints.  Called by threads 0..NT-1.
+// scratch: 64 ints up to 8 warps, 128 with 16.  Called by threads 0..NT-1.
 // ------------------------------------------------------------------------------------
 template <int NT, bool kNamed>
 __device__ __forceinline__ void topk_find_bin(const int* hist, int need, int* out3, int* sums) {
@@ -531,7 +531,12 @@ template <int NT, bool kNamed>
 __device__ void topk_keys(const uint32_t* keys, int N, int K, uint32_t lo, uint32_t hi,
                           int* idx_out, int* count_out, int* hist, uint32_t* bits,
                           int* scratch) {
-  static_assert(NT % 32 == 0 && NT <= 256 && kTopkBins % (4 * NT) == 0, "up to 8 whole warps");
+  static_assert(NT % 32 == 0 && NT <= 512 && kTopkBins % (4 * NT) == 0, "up to 16 whole warps");
+  // scratch: [40, 48) bin search results; per-warp sums of the two alternating bin searches
+  // and of the final placement scan after them (within 64 ints up to 8 warps)
+  constexpr int NW = NT / 32;
+  constexpr int kSums = NW <= 8 ? 16 : 48;
+  constexpr int kFinal = NW <= 8 ? 32 : 48 + 2 * NW;
   const int tid = threadIdx.x;
   const int nw = (N + 31) >> 5;
   uint32_t* dbits = bits;
@@ -565,7 +570,7 @@ __device__ void topk_keys(const uint32_t* keys, int N, int K, uint32_t lo, uint3
     if (mark) break;
     bsync<NT, kNamed>();
     int* f = scratch + 40 + 4 * (level & 1);
-    topk_find_bin<NT, kNamed>(h, need, f, scratch + 16 + 8 * (level & 1));
+    topk_find_bin<NT, kNamed>(h, need, f, scratch + kSums + NW * (level & 1));
     const int bstar = f[0], above = f[1], bucket = f[2];
     // clear this level's histogram for the level after next (the next one uses the other)
     for (int i = tid; i < kTopkBins / 4; i += NT) reinterpret_cast<int4*>(h)[i] = make_int4(0, 0, 0, 0);
@@ -589,7 +594,7 @@ __device__ void topk_keys(const uint32_t* keys, int N, int K, uint32_t lo, uint3
     nd += __popc(dbits[w]);
     nt += __popc(tbits[w]);
   }
-  const int before = block_excl_sum<NT, kNamed>((nd << 16) | nt, scratch + 32);
+  const int before = block_excl_sum<NT, kNamed>((nd << 16) | nt, scratch + kFinal);
   int dcnt = before >> 16, tcnt = before & 0xffff;
   for (int w = w0; w < w1; ++w) {
     const uint32_t D = dbits[w], T = tbits[w];
@@ -651,7 +656,7 @@ __device__ void topk_row(const float* row, int N, int K, int sink, int local, in
   }
   if (lane == 0) {
     scratch[warp] = (int)lo;
-    scratch[8 + warp] = (int)hi;
+    scratch[NW + warp] = (int)hi;
   }
   for (int i = tid; i < 2 * kTopkBins / 4; i += NT)
     reinterpret_cast<int4*>(t.hist)[i] = make_int4(0, 0, 0, 0);
@@ -661,7 +666,7 @@ __device__ void topk_row(const float* row, int N, int K, int sink, int local, in
 #pragma unroll
   for (int w = 0; w < NW; ++w) {
     lo = min(lo, (uint32_t)scratch[w]);
-    hi = max(hi, (uint32_t)scratch[8 + w]);
+    hi = max(hi, (uint32_t)scratch[NW + w]);
   }
   topk_keys<NT, kNamed>(t.keys, N, K, lo, hi, idx_out, count_out, t.hist, t.kept, scratch);
 }

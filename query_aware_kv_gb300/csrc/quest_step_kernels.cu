@@ -49,15 +49,20 @@ __global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
 }
 
 // ---------------------------------------------------------------- top-K
-// grid (B*Hkv), 256 threads; dynamic smem: keys of one score row + histogram + scratch.
-__global__ void __launch_bounds__(kConsumerThreads) topk_kernel(Params p) {
+// grid (B*Hkv), kTopkThreads threads; dynamic smem: keys of one score row + histogram +
+// scratch.  The selection is bound by instruction latency (dependent steps per key, block
+// barriers between passes), so a row gets 16 warps: fewer keys per thread, and four warps
+// per scheduler to hide each other's waits.
+constexpr int kTopkThreads = 512;
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(Params p) {
   extern __shared__ __align__(16) unsigned char sm[];
   pdl_wait();
   const int bg = blockIdx.x, b = bg / p.Hkv;
   const int L = load_len(p, b, kSiteTopk);
   const int N = (L + p.P - 1) / p.P;
   int* scratch = reinterpret_cast<int*>(sm + topk_smem_bytes(p.max_pages));
-  topk_row<kConsumerThreads, false>(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
+  topk_row<kTopkThreads, false>(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
                                     p.sink_pages, p.local_pages, p.sel_idx + (size_t)bg * p.top_k, p.sel_count + bg,
                                     topk_smem_at(sm, p.max_pages), scratch);
 }
@@ -215,7 +220,7 @@ cudaError_t launch_topk(const Params& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   Params pp = p;
   void* args[] = {&pp};
-  return launch_pdl(fn, dim3(p.B * p.Hkv), dim3(kConsumerThreads), smem, s, args);
+  return launch_pdl(fn, dim3(p.B * p.Hkv), dim3(kTopkThreads), smem, s, args);
 }
 
 cudaError_t launch_decode(const Params& p, int G, cudaStream_t s) {
