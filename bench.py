@@ -730,7 +730,8 @@ def run_prefill(args):
 
 def run_layers(args):
     """All 32 layers of the 128K-context model in one quest_decode_layers launch against 32
-    quest_decode launches, L2 flushed before each timed step; one JSON line."""
+    quest_decode calls (automatic path, and forced to the one-launch kernel), L2 flushed
+    before each timed step; one JSON line."""
     import torch
 
     import query_aware_kv_gb300 as q
@@ -763,13 +764,21 @@ def run_layers(args):
     lses = [torch.empty((1, 32), dtype=torch.float32, device=dev) for _ in range(n_layers)]
 
     o = q.opts(cluster_size=args.cluster_size)
+    o_fused = q.opts(cluster_size=args.cluster_size, path=q.QUEST_PATH_FUSED)
 
     def one_launch():
         q.decode_layers(base, layers, qs, K, ws, o, out=outs, lse=lses)
 
+    def one_launch_kernel():
+        q.decode_layers(base, layers, qs, K, ws, o_fused, out=outs, lse=lses)
+
     def per_layer():
         for i, lay in enumerate(layers):
             q.decode(lay, qs[i], K, ws, o, out=outs[i], lse=lses[i])
+
+    def per_layer_fused():
+        for i, lay in enumerate(layers):
+            q.decode(lay, qs[i], K, ws, o_fused, out=outs[i], lse=lses[i])
 
     def timed(fn, reps=16):
         es = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -786,6 +795,8 @@ def run_layers(args):
 
     fused_us = timed(one_launch)
     per_us = timed(per_layer)
+    per_fused_us = timed(per_layer_fused)
+    one_kernel_us = timed(one_launch_kernel)
     rc, _ = q.read_status(ws)
     L = int(base.seq_lens[0])
     nbytes = n_layers * decode_bytes([L], 32 * K * PAGE, 1, 32, 32)
@@ -794,7 +805,9 @@ def run_layers(args):
     print(json.dumps({"workload": "yarn_128k_32_layers_budget2048", "layers": n_layers,
                       "cluster_size": args.cluster_size,
                       "decode_layers_us": round(fused_us, 1),
+                      "decode_layers_one_launch_kernel_us": round(one_kernel_us, 1),
                       "decode_per_layer_launches_us": round(per_us, 1),
+                      "decode_per_layer_one_launch_kernel_us": round(per_fused_us, 1),
                       "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
                       "frac_of_measured": round(gbs / peak, 4), "status": rc}), flush=True)
 

@@ -277,14 +277,17 @@ int quest_decode_step(const quest_cache_t* cache, const void* q, const void* k_n
                       quest_stream_t stream);
 
 /*
- * Every layer of one decode step in one launch.  [Guide] Evaluation (end-to-end latency
+ * Every layer of one decode step in one call.  [Guide] Evaluation (end-to-end latency
  * table): a whole token step runs the sparse decode in every layer, which is where the
  * end-to-end gains are measured.  The same fused step as quest_decode_step (or
  * quest_decode when k_new is NULL) for n_layers layers that share the batch, the block
- * table and the lengths, each with its own K/V pools, boxes, query, new token and output.  The (layer, sequence, kv head) pairs are
- * the work units of one persistent launch, so one pair's selection overlaps other pairs'
- * streaming.  cache: the shared shape, block_table and seq_lens (its k_pool / v_pool / meta
- * are not used).  layers: host array of n_layers (1..QUEST_MAX_LAYERS) quest_layer_t, read
+ * table and the lengths, each with its own K/V pools, boxes, query, new token and output.
+ * With the one-launch kernel the (layer, sequence, kv head) pairs are the work units of
+ * one persistent launch, so one pair's selection overlaps other pairs' streaming.
+ * opts.path as for quest_decode, the rule counting every layer's pairs; the chain writes
+ * every layer's new token first, advances the lengths once, then runs each layer's
+ * estimate, top-K and sparse decode.  cache: the shared shape, block_table and seq_lens
+ * (its k_pool / v_pool / meta are not used).  layers: host array of n_layers (1..QUEST_MAX_LAYERS) quest_layer_t, read
  * during the call only; pointers as in quest_decode_step.  k_new / v_new: given for every
  * layer (each layer appends at slot seq_len[b]; seq_lens advance once, at the end) or for
  * none.  No idx_out.  ws: as quest_decode for this cache and top_k.

@@ -513,15 +513,60 @@ int quest_decode_layers(const quest_cache_t* cache, const quest_layer_t* layers,
   if (cs < 0 || cs > kMaxClusterSize)
     return fail(QUEST_ERR_INVALID_ARG, "cluster_size %d: use 0 (automatic) or 1..%d", cs,
                 kMaxClusterSize);
-  if (!cluster_any_fits(group_of(cache), cache->page_size, cache->max_pages, top_k))
+  const int path = opts ? opts->path : QUEST_PATH_AUTO;
+  if (path < QUEST_PATH_AUTO || path > QUEST_PATH_CHAIN)
+    return fail(QUEST_ERR_INVALID_ARG, "path %d: use QUEST_PATH_AUTO, _FUSED or _CHAIN", path);
+  const int G = group_of(cache);
+  const bool fits = cluster_any_fits(G, cache->page_size, cache->max_pages, top_k);
+  bool chain = path == QUEST_PATH_CHAIN;
+  if (path == QUEST_PATH_AUTO && cs == 0 && !(opts && (opts->trace || opts->debug_flags))) {
+    bool fused = false;
+    const cudaError_t e = fits ? cluster_preferred(p, G, n_layers, &fused) : cudaSuccess;
+    if (e != cudaSuccess) return launched(e, "quest_decode_layers");
+    chain = !fused;
+  }
+  if (chain) {
+    // layer after layer as separate kernels: every layer's token row and box first (at the
+    // same position), the lengths advanced once, then each layer's estimate, top-K and
+    // sparse decode over the cache that holds the new token
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Params c = make_params(cache, ws, Lw, t, opts);
+    c.top_k = top_k;
+    c.pps = t.pps_sparse;
+    c.n_splits = t.n_splits_sparse;
+    c.dense = 0;
+    auto at = [&](int i) {
+      Params l = c;
+      l.k_pool = lt.l[i].k_pool;
+      l.v_pool = lt.l[i].v_pool;
+      l.meta = lt.l[i].meta;
+      l.q = lt.l[i].q;
+      l.out = lt.l[i].out;
+      l.lse = lt.l[i].lse;
+      return l;
+    };
+    cudaError_t e = cudaSuccess;
+    if (append) {
+      for (int i = 0; i < n_layers && e == cudaSuccess; ++i)
+        e = launch_append(at(i), lt.l[i].k_new, lt.l[i].v_new, s, false);
+      if (e == cudaSuccess) e = launch_advance_lengths(c, 1, s);
+    }
+    for (int i = 0; i < n_layers && e == cudaSuccess; ++i) {
+      const Params l = at(i);
+      e = launch_estimate(l, G, false, s);
+      if (e == cudaSuccess) e = launch_topk(l, s);
+      if (e == cudaSuccess) e = launch_decode(l, G, s);
+    }
+    return launched(e, "quest_decode_layers");
+  }
+  if (!fits)
     return fail(QUEST_ERR_UNSUPPORTED, "max_pages %d needs more shared memory than a CTA has",
                 cache->max_pages);
   if (cs > 0 &&
-      cluster_smem_bytes(group_of(cache), cache->page_size, cache->max_pages, cs, top_k) >
-          kMaxSmem)
+      cluster_smem_bytes(G, cache->page_size, cache->max_pages, cs, top_k) > kMaxSmem)
     return fail(QUEST_ERR_UNSUPPORTED, "cluster_size %d needs more shared memory than a CTA has",
                 cs);
-  return launched(launch_cluster(p, lt, group_of(cache), cs, opts ? opts->max_ctas : 0,
+  return launched(launch_cluster(p, lt, G, cs, opts ? opts->max_ctas : 0,
                                  static_cast<cudaStream_t>(stream)),
                   "quest_decode_layers");
 }

@@ -78,10 +78,11 @@ __global__ void __launch_bounds__(256) build_meta_kernel(Params p) {
 // One CTA per sequence; warps loop over kv heads.  Lanes 0-15 move the key row and own
 // the box minimum, lanes 16-31 move the value row and own the maximum.  The new token
 // opens a fresh box in slot 0 and widens the existing one otherwise.  The length grows
-// once every head is written.
+// once every head is written (unless `advance` is 0: a caller appending the same position
+// in several layers advances the lengths once, afterwards).
 template <int P>
 __global__ void __launch_bounds__(256) append_kernel(Params p, const __half* k_new,
-                                                     const __half* v_new) {
+                                                     const __half* v_new, int advance) {
   pdl_wait();
   pdl_trigger();  // the decode step that follows may start its prologue
   __shared__ int s_len, s_phys;
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(256) append_kernel(Params p, const __half* k_n
     *box = res;
   }
   __syncthreads();
-  if (threadIdx.x == 0) p.seq_lens[b] = L + 1;
+  if (advance && threadIdx.x == 0) p.seq_lens[b] = L + 1;
 }
 
 // Chunked prefill: n new tokens per sequence are written at slots [L, L + n) and folded
@@ -262,6 +263,13 @@ __global__ void __launch_bounds__(256) prefill_lens_kernel(Params p, int n) {
   if (fits && !bad && threadIdx.x == 0) p.seq_lens[b] = L + n;
 }
 
+cudaError_t launch_advance_lengths(const Params& p, int n, cudaStream_t s) {
+  Params pp = p;
+  int nn = n;
+  void* args[] = {&pp, &nn};
+  return launch_pdl((const void*)prefill_lens_kernel, dim3(p.B), dim3(256), 0, s, args);
+}
+
 cudaError_t launch_prefill(const Params& p, const __half* k, const __half* v, int n,
                            cudaStream_t s) {
   Params pp = p;
@@ -274,8 +282,7 @@ cudaError_t launch_prefill(const Params& p, const __half* k, const __half* v, in
   cudaError_t e = launch_pdl(fn, dim3((p.Hkv + kPrefillWarps - 1) / kPrefillWarps, pages, p.B),
                              dim3(32 * kPrefillWarps), 0, s, args);
   if (e != cudaSuccess) return e;
-  void* args2[] = {&pp, &nn};
-  return launch_pdl((const void*)prefill_lens_kernel, dim3(p.B), dim3(256), 0, s, args2);
+  return launch_advance_lengths(p, n, s);
 }
 
 cudaError_t launch_build_meta(const Params& p, cudaStream_t s) {
@@ -288,11 +295,12 @@ cudaError_t launch_build_meta(const Params& p, cudaStream_t s) {
 }
 
 cudaError_t launch_append(const Params& p, const __half* k_new, const __half* v_new,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool advance) {
   Params pp = p;
   const __half* kn = k_new;
   const __half* vn = v_new;
-  void* args[] = {&pp, &kn, &vn};
+  int adv = advance ? 1 : 0;
+  void* args[] = {&pp, &kn, &vn, &adv};
   const void* fn = p.P == 16 ? (const void*)append_kernel<16> : (const void*)append_kernel<32>;
   return launch_pdl(fn, dim3(p.B), dim3(256), 0, s, args);
 }

@@ -152,7 +152,9 @@ int set_last_error(int code, const char* message);
 
 cudaError_t launch_build_meta(const Params& p, cudaStream_t s);
 cudaError_t launch_append(const Params& p, const __half* k_new, const __half* v_new,
-                          cudaStream_t s);
+                          cudaStream_t s, bool advance = true);
+// seq_lens[b] += n for every sequence with room whose touched pages are mapped.
+cudaError_t launch_advance_lengths(const Params& p, int n, cudaStream_t s);
 cudaError_t launch_estimate(const Params& p, int G, bool per_head, cudaStream_t s);
 cudaError_t launch_topk_union(const Params& p, int row_cap, cudaStream_t s);
 cudaError_t launch_prefill(const Params& p, const __half* k, const __half* v, int n,

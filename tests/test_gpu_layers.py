@@ -1,5 +1,6 @@
-"""Every layer of a decode step in one launch (quest_decode_layers): the layers share the
-batch, block table and lengths, each has its own pools, boxes, query and new token.
+"""Every layer of a decode step in one call (quest_decode_layers: one launch, or the layers
+as separate kernels): the layers share the batch, block table and lengths, each has its own
+pools, boxes, query and new token.
 Checked against the oracle per layer (acceptance rules of tests/harness.py) and against
 one quest_decode_step call per layer with the same cluster size (bit-exact: the same pairs
 are computed by the same code)."""
@@ -35,8 +36,9 @@ def _shared_cache(ws_, layer):
     return c, ref
 
 
+@pytest.mark.parametrize("path", ["cluster4", "chain"])
 @pytest.mark.parametrize("append", [False, True])
-def test_layers_match_oracle_and_single_calls(append):
+def test_layers_match_oracle_and_single_calls(append, path):
     n = 4
     ws_ = _layers(n, lens=(2500, 700, 16 * 40 + 3))
     K = ws_[0].top_k
@@ -55,7 +57,7 @@ def test_layers_match_oracle_and_single_calls(append):
     qs = [w.q[0].cuda() for w in ws_]
     kn = [w.k_new[0].cuda() for w in ws_] if append else None
     vn = [w.v_new[0].cuda() for w in ws_] if append else None
-    o = q.opts(cluster_size=4)
+    o = q.opts(cluster_size=4) if path == "cluster4" else q.opts(path=q.QUEST_PATH_CHAIN)
     outs, lses = q.decode_layers(base, layers, qs, K, ws, o, k_new=kn, v_new=vn)
     H.assert_status_ok(ws)
     assert base.seq_lens.cpu().tolist() == [int(x) + (1 if append else 0) for x in len0.cpu()]
@@ -69,7 +71,8 @@ def test_layers_match_oracle_and_single_calls(append):
         # oracle's attention over the oracle's own selection (no near-ties in these inputs)
         out_ref, lse_ref = oracle.attend(refs[i], qh, ri, rc)
         H.assert_attention_close(outs[i], lses[i], out_ref, lse_ref)
-    # one quest_decode_step / quest_decode per layer, same cluster size: bit-exact
+    # one quest_decode_step / quest_decode per layer, same cluster size or the same chain of
+    # kernels: bit-exact
     multi_out = [x.clone() for x in outs]
     multi_meta = [lay.meta.clone() for lay in layers]
     for i, lay in enumerate(layers):
@@ -85,9 +88,11 @@ def test_layers_match_oracle_and_single_calls(append):
     H.assert_status_ok(ws)
 
 
-def test_layers_of_the_128k_model():
-    """Four layers of the 128K-context shape (8192 pages per head) in one launch; every
-    head's needle page must be in the oracle's selection and the outputs must match."""
+@pytest.mark.parametrize("path", [q.QUEST_PATH_AUTO, q.QUEST_PATH_FUSED], ids=["auto", "fused"])
+def test_layers_of_the_128k_model(path):
+    """Four layers of the 128K-context shape (8192 pages per head), through the automatic
+    choice (the layers as separate kernels here) and in one launch; every head's needle
+    page must be in the oracle's selection and the outputs must match."""
     n = 4
     ws_ = [wl.yarn_128k_layer(layer, seed=0, device="cuda", budget=2048) for layer in range(n)]
     w0 = ws_[0]
@@ -102,7 +107,7 @@ def test_layers_of_the_128k_model():
     for lay in layers:
         q.build_meta(lay, ws)
     qs = [w.q[0] for w in ws_]
-    outs, lses = q.decode_layers(base, layers, qs, K, ws)
+    outs, lses = q.decode_layers(base, layers, qs, K, ws, q.opts(path=path))
     H.assert_status_ok(ws)
     bt = w0.block_table.cpu().numpy()
     sl = w0.seq_lens.cpu().numpy()
