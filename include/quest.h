@@ -99,7 +99,9 @@ typedef struct quest_cache {
 /* Optional launch tuning (pass NULL for defaults).  Results do not depend on it beyond
  * floating-point rounding of the split-K merge. */
 typedef struct quest_opts {
-    int32_t pages_per_split;  /* selected pages per decode work item (default 8)          */
+    int32_t pages_per_split;  /* selected pages per decode work item (default: about 8 work
+                                 items per (sequence, kv head), at least 16 pages; dense
+                                 decode: at least 8)                                         */
     int32_t score_tile_pages; /* pages per scoring work item (default 128)                */
     int32_t max_ctas;         /* fused kernel: cap on persistent CTAs (0 = all that fit)  */
     int32_t debug_flags;      /* QUEST_DEBUG_* (0 in normal use)                          */
@@ -138,13 +140,14 @@ typedef struct quest_opts {
                                  unless idx_out / count_out are given).                     */
 } quest_opts_t;
 
-/* Values of quest_opts_t.path.  AUTO (0) takes the one-launch kernel unless it would run
- * with a single CTA per SM (a CTA needs more than half an SM's shared memory), or with one
- * CTA per (sequence, kv head) while the pair's boxes weigh at least 1.5 times its kept K/V
- * (max_pages boxes against top_k pages): there the pair's serial scoring and selection
- * cost more than three launches whose scoring and selection run across the whole GPU.
- * AUTO always takes the one-launch kernel when cluster_size, trace or debug_flags is set,
- * and the chain when no cluster of the one-launch kernel fits in shared memory. */
+/* Values of quest_opts_t.path.  AUTO (0) takes the one-launch kernel when every
+ * (sequence, kv head) pair of the call gets a cluster of at least 2 CTAs, all resident at
+ * once with 2 CTAs per SM (the pair's scoring, selection and decode then run on several
+ * SMs, and the step pays one launch); otherwise (more pairs than that, or a CTA needing
+ * more than half an SM's shared memory) the chain, whose scoring, top-K and decode kernels
+ * spread over the whole GPU.  AUTO always takes the one-launch kernel when cluster_size,
+ * trace or debug_flags is set, and the chain when no cluster of the one-launch kernel fits
+ * in shared memory. */
 #define QUEST_PATH_AUTO 0
 #define QUEST_PATH_FUSED 1
 #define QUEST_PATH_CHAIN 2

@@ -89,9 +89,13 @@ Tiling make_tiling(const quest_cache_t* c, int top_k, const quest_opts_t* o) {
   if (stp > c->max_pages) stp = c->max_pages;
   t.score_tile_pages = stp;
   t.n_score_tiles = (int)cdiv(c->max_pages, stp);
-  const int pps = (o && o->pages_per_split > 0) ? o->pages_per_split : kDefaultPagesPerSplit;
+  const int user_pps = (o && o->pages_per_split > 0) ? o->pages_per_split : 0;
+  const int pps = user_pps ? user_pps : kDefaultPagesPerSplit;
   const int kcap = top_k < c->max_pages ? top_k : c->max_pages;
-  t.pps_sparse = (int)std::max<long long>(pps, cdiv(kcap, kMaxSplits));
+  // by default about 8 sparse work items per (sequence, kv head), of at least 16 pages: a
+  // work item of a few pages spends most of its time filling its ring and merging
+  t.pps_sparse = user_pps ? (int)std::max<long long>(user_pps, cdiv(kcap, kMaxSplits))
+                          : (int)std::max<long long>(kMinSparsePagesPerSplit, cdiv(kcap, 8));
   t.n_splits_sparse = (int)cdiv(kcap, t.pps_sparse);
   t.pps_dense = (int)std::max<long long>(pps, cdiv(c->max_pages, 64));
   t.n_splits_dense = (int)cdiv(c->max_pages, t.pps_dense);

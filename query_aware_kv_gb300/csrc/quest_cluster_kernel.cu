@@ -1002,9 +1002,7 @@ cudaError_t cluster_preferred(const Params& p, int G, int n_layers, bool* out) {
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDecodeThreads, smem)) !=
       cudaSuccess)
     return e;
-  const long long boxes = (long long)p.max_pages * 2 * kHeadDim * 2;
-  const long long kept = (long long)std::min(p.top_k, p.max_pages) * p.P * 2 * kHeadDim * 2;
-  *out = per_sm >= 2 && !(cs == 1 && 2 * boxes >= 3 * kept);
+  *out = per_sm >= 2 && cs >= 2;
   return cudaSuccess;
 }
 

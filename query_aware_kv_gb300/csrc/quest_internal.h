@@ -17,7 +17,8 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kDecodeThreads = kConsumerThreads + 32;  // + one bulk-copy producer warp
 constexpr int kStages = 8;                  // smem ring depth (pages in flight per CTA)
 constexpr int kMaxSplits = 256;             // split-K partials per (sequence, q head)
-constexpr int kDefaultPagesPerSplit = 8;
+constexpr int kDefaultPagesPerSplit = 8;    // dense decode work items (at least)
+constexpr int kMinSparsePagesPerSplit = 16;  // sparse decode work items, by default
 constexpr int kDefaultScoreTilePages = 128;
 constexpr long long kDefaultWaitNs = 1000000000LL;
 constexpr int kDefaultDecodeLag = 16;
