@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--pages-per-split", type=int, default=0)
     ap.add_argument("--score-tile-pages", type=int, default=0)
     ap.add_argument("--trace", default="", help="write a fused-kernel timeline (npy) here")
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "chain"],
+                    help="quest_decode / quest_decode_step path (default: the library's choice)")
     ap.add_argument("--cluster-size", type=int, default=0,
                     help="CTAs per (sequence, kv head) cluster for --sweep / --layers (0: automatic)")
     ap.add_argument("--layers", action="store_true",
@@ -154,7 +156,7 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------
 # CPU oracle timing (the reference arm, and the cpu_baseline key)
 # ------------------------------------------------------------------------------------
-def oracle_timing(w, budget_s: float, max_steps: int):
+def oracle_timing(w, budget_s: float, max_steps: int, warmup: int = 0):
     import numpy as np
     import oracle
     oracle.build()
@@ -163,6 +165,11 @@ def oracle_timing(w, budget_s: float, max_steps: int):
                                    w.num_q_heads)
     oracle.build_meta(ref)
     qs, ks, vs = w.q.cpu().numpy(), w.k_new.cpu().numpy(), w.v_new.cpu().numpy()
+    for t in range(min(warmup, w.steps)):  # untimed, then the cache is rewound
+        oracle.decode_step(ref, qs[t], w.top_k, ks[t], vs[t])
+    if warmup:
+        ref.seq_lens[:] = w.seq_lens.cpu().numpy()
+        oracle.build_meta(ref)
     times = []
     t_start = time.perf_counter()
     n = 0
@@ -219,13 +226,14 @@ def run_reference(args):
         return
     from query_aware_kv_gb300 import workloads as wl
     w = wl.longchat_32k(seed=0, device="cpu")
+    warm = max(0, args.warmup)
     us, n = oracle_timing(w, budget_s=min(240.0, 0.05 * max(1, args.steps) + 60.0),
-                          max_steps=max(1, args.steps))
+                          max_steps=max(1, args.steps), warmup=warm)
     cpu = {"value": us, "unit": "us/step", "cores": 1, "kind": "oracle",
            "sample": f"{n} of the {args.steps} requested decode steps (append + score + "
                      f"top-K + attend), single-threaded C oracle, contexts 32769..32832"}
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/step",
-            "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": us / 1e3,
+            "n_gpus": args.gpus, "steps": n, "warmup": min(warm, w.steps), "ms_per_step": us / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, **w.describe()},
             "cpu_baseline": cpu,
@@ -289,8 +297,10 @@ def run_quest(args):
     idx = torch.empty((1, w.num_kv_heads, K), dtype=torch.int32, device=dev)
     cnt = torch.empty((1, w.num_kv_heads), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
+    path = {"auto": q.QUEST_PATH_AUTO, "fused": q.QUEST_PATH_FUSED,
+            "chain": q.QUEST_PATH_CHAIN}[args.path]
     opts_main = q.opts(decode_lag=args.decode_lag, pages_per_split=args.pages_per_split,
-                       score_tile_pages=args.score_tile_pages)
+                       score_tile_pages=args.score_tile_pages, path=path)
 
     def rewind():
         cache.meta.copy_(meta0)
@@ -473,10 +483,13 @@ def run_quest(args):
         "data": "synthetic (seeded N(0,1) fp16 K/V, 4 key channels x8, 8 planted needles/head)",
         "config": {**w.describe(), "storage": "fp16 K/V/q/out, fp32 arithmetic",
                    "l2": "flushed before every timed step (512 MiB write, then 256 MiB read)",
-                   "step": "quest_decode_step: append + score + top-K + split-K decode, one launch",
+                   "step": "quest_decode_step: append + score + top-K + split-K decode "
+                           "(path " + args.path + ": one launch on this workload unless 'chain')",
                    "replicas": world},
         "gbs": round(replicas.job_bytes_per_second(step_bytes, world, mean_step * 1e-6) / 1e9, 1),
-        "roofline": {"bound": "hbm", "kernel": "quest_decode (fused)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "quest_decode (chain of estimate, top-K, sparse decode)"
+                     if args.path == "chain" else "quest_decode (fused)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
