@@ -475,7 +475,7 @@ def run_quest(args):
     peak, peak_kind = peaks()
     step_bytes = dec_bytes + append_bytes(1, w.num_kv_heads)
     achieved = dec_bytes / (dec_us * 1e-6) / 1e9
-    traffic = profiled_traffic()
+    traffic = profiled_traffic() if args.path != "chain" else None
     line = {
         "metric": METRIC, "value": round(mean_step, 3), "unit": "us/step", "n_gpus": world,
         "steps": n, "warmup": args.warmup, "ms_per_step": round(mean_step / 1e3, 6),
