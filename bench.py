@@ -475,7 +475,8 @@ def run_quest(args):
     peak, peak_kind = peaks()
     step_bytes = dec_bytes + append_bytes(1, w.num_kv_heads)
     achieved = dec_bytes / (dec_us * 1e-6) / 1e9
-    traffic = profiled_traffic() if args.path != "chain" else None
+    taken = "chain" if q.decode_path(cache, K, opts_main) == q.QUEST_PATH_CHAIN else "fused"
+    traffic = profiled_traffic(taken)
     line = {
         "metric": METRIC, "value": round(mean_step, 3), "unit": "us/step", "n_gpus": world,
         "steps": n, "warmup": args.warmup, "ms_per_step": round(mean_step / 1e3, 6),
@@ -483,13 +484,15 @@ def run_quest(args):
         "data": "synthetic (seeded N(0,1) fp16 K/V, 4 key channels x8, 8 planted needles/head)",
         "config": {**w.describe(), "storage": "fp16 K/V/q/out, fp32 arithmetic",
                    "l2": "flushed before every timed step (512 MiB write, then 256 MiB read)",
-                   "step": "quest_decode_step: append + score + top-K + split-K decode "
-                           "(path " + args.path + ": one launch on this workload unless 'chain')",
+                   "step": "quest_decode_step: append + score + top-K + split-K decode",
+                   "decode_path": taken + (" (library's choice)" if args.path == "auto" else
+                                           " (forced)"),
                    "replicas": world},
         "gbs": round(replicas.job_bytes_per_second(step_bytes, world, mean_step * 1e-6) / 1e9, 1),
         "roofline": {"bound": "hbm",
-                     "kernel": "quest_decode (chain of estimate, top-K, sparse decode)"
-                     if args.path == "chain" else "quest_decode (fused)",
+                     "kernel": "quest_decode, chain: estimate_kernel + topk_kernel + "
+                               "decode_kernel" if taken == "chain"
+                     else "quest_decode, one launch: cluster_kernel",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
@@ -825,9 +828,10 @@ def run_layers(args):
                       "frac_of_measured": round(gbs / peak, 4), "status": rc}), flush=True)
 
 
-def profiled_traffic():
-    """DRAM bytes per quest_decode launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else null)."""
+def profiled_traffic(path: str):
+    """DRAM bytes per quest_decode call on the bench workload, for the path it took, from
+    the committed ncu summaries, if they were taken on the current kernel sources (else
+    null)."""
     try:
         import hashlib
         with open(os.path.join(ROOT, "profiles", "quest_decode_traffic.json")) as f:
@@ -839,7 +843,7 @@ def profiled_traffic():
                 h.update(f.read())
         if rec.get("csrc_sha256") != h.hexdigest():
             return None
-        return rec.get("dram_bytes_per_launch_full_workload")
+        return rec[path]["dram_bytes_per_launch_full_workload"]
     except Exception:
         return None
 

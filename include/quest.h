@@ -135,22 +135,32 @@ typedef struct quest_opts {
                                  min(G * top_k, max_pages) entries.  Not with sink / local
                                  pages; the fused calls answer QUEST_ERR_UNSUPPORTED.        */
     int32_t path;             /* quest_decode / quest_decode_step: QUEST_PATH_*.  The chain
-                                 computes the same step as separate append, estimate, top-K
-                                 and sparse-decode kernels (selection kept in the workspace
-                                 unless idx_out / count_out are given).                     */
+                                 computes the same step as separate estimate, top-K and
+                                 sparse-decode kernels; the estimate writes the new token's
+                                 row and box as it scores that page, and the sparse decode
+                                 advances the lengths at its end (selection kept in the
+                                 workspace unless idx_out / count_out are given).           */
 } quest_opts_t;
 
-/* Values of quest_opts_t.path.  AUTO (0) takes the one-launch kernel when every
- * (sequence, kv head) pair of the call gets a cluster of at least 2 CTAs, all resident at
- * once with 2 CTAs per SM (the pair's scoring, selection and decode then run on several
- * SMs, and the step pays one launch); otherwise (more pairs than that, or a CTA needing
- * more than half an SM's shared memory) the chain, whose scoring, top-K and decode kernels
- * spread over the whole GPU.  AUTO always takes the one-launch kernel when cluster_size,
- * trace or debug_flags is set, and the chain when no cluster of the one-launch kernel fits
- * in shared memory. */
+/* Values of quest_opts_t.path.  AUTO (0) takes the one-launch kernel for short rows
+ * (max_pages below 1024) when every (sequence, kv head) pair of the call gets a cluster of
+ * at least 2 CTAs, all resident at once with 2 CTAs per SM: there the step's fixed cost
+ * dominates and one launch pays it once.  Otherwise (longer rows, more pairs, or a CTA
+ * needing more than half an SM's shared memory) it takes the chain, whose scoring, top-K
+ * and decode kernels spread over the whole GPU.  AUTO always takes the one-launch kernel
+ * when cluster_size, trace or debug_flags is set, and the chain when no cluster of the
+ * one-launch kernel fits in shared memory.  quest_decode_path() tells which one a call
+ * takes. */
 #define QUEST_PATH_AUTO 0
 #define QUEST_PATH_FUSED 1
 #define QUEST_PATH_CHAIN 2
+
+/* The path (QUEST_PATH_FUSED or QUEST_PATH_CHAIN) that quest_decode / quest_decode_step
+ * (n_layers = 1) or quest_decode_layers (n_layers layers) take for this cache, top_k and
+ * opts, or minus a QUEST_ERR_* status on invalid arguments.  Queries the device's occupancy
+ * for the one-launch kernel; launches nothing. */
+int quest_decode_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
+                      int32_t n_layers);
 
 /* quest_decode only: never publish the selection, so that every decode work item's
  * bounded wait runs out and the call reports QUEST_ERR_TIMEOUT.  For testing the

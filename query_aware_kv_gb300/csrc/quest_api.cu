@@ -111,6 +111,7 @@ WsLayout make_layout(const quest_cache_t* c, const Tiling& t) {
   L.score_arrive = off;  off = up256(off + nbg * 4);
   L.ready = off;         off = up256(off + nbg * 4);
   L.decode_arrive = off; off = up256(off + nbg * 4);
+  L.seq_done = off;      off = up256(off + (size_t)c->batch * 4);
   L.scores = off;        off = up256(off + nbg * c->max_pages * 4);
   L.sel_idx = off;       off = up256(off + nbg * (size_t)t.topk_cap * 4);
   L.sel_count = off;     off = up256(off + nbg * 4);
@@ -143,6 +144,7 @@ Params make_params(const quest_cache_t* c, void* ws, const WsLayout& L, const Ti
   p.score_arrive = reinterpret_cast<unsigned*>(w + L.score_arrive);
   p.ready = reinterpret_cast<unsigned*>(w + L.ready);
   p.decode_arrive = reinterpret_cast<unsigned*>(w + L.decode_arrive);
+  p.seq_done = reinterpret_cast<unsigned*>(w + L.seq_done);
   p.scores = reinterpret_cast<float*>(w + L.scores);
   p.sel_idx = reinterpret_cast<int*>(w + L.sel_idx);
   p.sel_count = reinterpret_cast<int*>(w + L.sel_count);
@@ -356,6 +358,32 @@ int quest_sparse_decode(const quest_cache_t* cache, const void* q, const int32_t
                   "quest_sparse_decode");
 }
 
+// The path of a decode call (QUEST_PATH_* in quest.h): *chain on return.
+static int decide_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
+                       int n_layers, bool* chain) {
+  const int cs = opts ? opts->cluster_size : 0;
+  if (cs < 0 || cs > kMaxClusterSize)
+    return fail(QUEST_ERR_INVALID_ARG, "cluster_size %d: use 0 (automatic) or 1..%d", cs,
+                kMaxClusterSize);
+  const int path = opts ? opts->path : QUEST_PATH_AUTO;
+  if (path < QUEST_PATH_AUTO || path > QUEST_PATH_CHAIN)
+    return fail(QUEST_ERR_INVALID_ARG, "path %d: use QUEST_PATH_AUTO, _FUSED or _CHAIN", path);
+  const int G = group_of(cache);
+  const bool fits = cluster_any_fits(G, cache->page_size, cache->max_pages, top_k);
+  *chain = path == QUEST_PATH_CHAIN;
+  if (path == QUEST_PATH_AUTO && cs == 0 && !(opts && (opts->trace || opts->debug_flags))) {
+    bool fused = false;
+    const long long nbg = (long long)n_layers * cache->batch * cache->num_kv_heads;
+    const cudaError_t e = fits ? cluster_preferred(G, cache->page_size, cache->max_pages, top_k,
+                                                   (int)std::min<long long>(nbg, 0x7fffffff),
+                                                   &fused)
+                               : cudaSuccess;
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy of the one-launch kernel");
+    *chain = !fused;
+  }
+  return QUEST_OK;
+}
+
 static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_new,
                        const void* v_new, int32_t top_k, void* out, float* lse, int32_t* idx_out,
                        int32_t* count_out, void* ws, size_t ws_bytes, const quest_opts_t* opts,
@@ -402,28 +430,17 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
                     what);
   }
   const int cs = opts ? opts->cluster_size : 0;  // 0: the library picks
-  if (cs < 0 || cs > kMaxClusterSize)
-    return fail(QUEST_ERR_INVALID_ARG, "cluster_size %d: use 0 (automatic) or 1..%d", cs,
-                kMaxClusterSize);
-  const int path = opts ? opts->path : QUEST_PATH_AUTO;
-  if (path < QUEST_PATH_AUTO || path > QUEST_PATH_CHAIN)
-    return fail(QUEST_ERR_INVALID_ARG, "path %d: use QUEST_PATH_AUTO, _FUSED or _CHAIN", path);
+  bool chain = false;
+  if ((rc = decide_path(cache, top_k, opts, 1, &chain))) return rc;
   const bool fits = cluster_any_fits(group_of(cache), cache->page_size, cache->max_pages, top_k);
-  bool chain = path == QUEST_PATH_CHAIN;
-  if (path == QUEST_PATH_AUTO && cs == 0 && !(opts && (opts->trace || opts->debug_flags))) {
-    bool fused = false;
-    cudaError_t e = fits ? cluster_preferred(p, group_of(cache), 1, &fused) : cudaSuccess;
-    if (e != cudaSuccess) return launched(e, what);
-    chain = !fused;
-  }
   if (chain) {
-    // the same step as separate kernels: append, estimate, top-K, sparse decode (the
-    // selection goes to idx_out / count_out if given, else to the workspace)
+    // the same step as separate kernels: estimate (which also writes the new token's row
+    // and widens its box), top-K, sparse decode (which advances the lengths at its end);
+    // the selection goes to idx_out / count_out if given, else to the workspace
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int G = group_of(cache);
-    cudaError_t e = cudaSuccess;
-    if (p.k_new) e = launch_append(p, p.k_new, p.v_new, s);
-    if (e == cudaSuccess) e = launch_estimate(p, G, false, s);
+    p.chain_append = p.k_new != nullptr ? 1 : 0;
+    cudaError_t e = launch_estimate(p, G, false, s);
     if (e == cudaSuccess) e = launch_topk(p, s);
     if (e == cudaSuccess) e = launch_decode(p, G, s);
     return launched(e, what);
@@ -444,6 +461,18 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   return launched(launch_cluster(p, lt, group_of(cache), cs, opts ? opts->max_ctas : 0,
                                  static_cast<cudaStream_t>(stream)),
                   what);
+}
+
+int quest_decode_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
+                      int32_t n_layers) {
+  int rc = check_cache(cache);
+  if (rc) return -rc;
+  if ((rc = check_topk(top_k))) return -rc;
+  if (n_layers < 1 || n_layers > QUEST_MAX_LAYERS)
+    return -fail(QUEST_ERR_INVALID_ARG, "n_layers %d: use 1..%d", n_layers, QUEST_MAX_LAYERS);
+  bool chain = false;
+  if ((rc = decide_path(cache, top_k, opts, n_layers, &chain))) return -rc;
+  return chain ? QUEST_PATH_CHAIN : QUEST_PATH_FUSED;
 }
 
 int quest_decode(const quest_cache_t* cache, const void* q, int32_t top_k, void* out, float* lse,
@@ -514,21 +543,10 @@ int quest_decode_layers(const quest_cache_t* cache, const quest_layer_t* layers,
   p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
   p.trace_capacity = opts ? opts->trace_capacity : 0;
   const int cs = opts ? opts->cluster_size : 0;
-  if (cs < 0 || cs > kMaxClusterSize)
-    return fail(QUEST_ERR_INVALID_ARG, "cluster_size %d: use 0 (automatic) or 1..%d", cs,
-                kMaxClusterSize);
-  const int path = opts ? opts->path : QUEST_PATH_AUTO;
-  if (path < QUEST_PATH_AUTO || path > QUEST_PATH_CHAIN)
-    return fail(QUEST_ERR_INVALID_ARG, "path %d: use QUEST_PATH_AUTO, _FUSED or _CHAIN", path);
   const int G = group_of(cache);
+  bool chain = false;
+  if ((rc = decide_path(cache, top_k, opts, n_layers, &chain))) return rc;
   const bool fits = cluster_any_fits(G, cache->page_size, cache->max_pages, top_k);
-  bool chain = path == QUEST_PATH_CHAIN;
-  if (path == QUEST_PATH_AUTO && cs == 0 && !(opts && (opts->trace || opts->debug_flags))) {
-    bool fused = false;
-    const cudaError_t e = fits ? cluster_preferred(p, G, n_layers, &fused) : cudaSuccess;
-    if (e != cudaSuccess) return launched(e, "quest_decode_layers");
-    chain = !fused;
-  }
   if (chain) {
     // layer after layer as separate kernels: every layer's token row and box first (at the
     // same position), the lengths advanced once, then each layer's estimate, top-K and

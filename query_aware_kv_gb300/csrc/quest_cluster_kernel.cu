@@ -990,19 +990,22 @@ cudaError_t choose_cluster_size(int G, int P, int max_pages, int top_k, int nbg,
 
 }  // namespace
 
-cudaError_t cluster_preferred(const Params& p, int G, int n_layers, bool* out) {
-  const int nbg = n_layers * p.B * p.Hkv;
+constexpr int kFusedMaxPages = 1024;
+
+cudaError_t cluster_preferred(int G, int P, int max_pages, int top_k, int nbg, bool* out) {
   int cs = 0;
-  cudaError_t e = choose_cluster_size(G, p.P, p.max_pages, p.top_k, nbg, &cs);
+  cudaError_t e = choose_cluster_size(G, P, max_pages, top_k, nbg, &cs);
   if (e != cudaSuccess) return e;
-  const void* fn = pick_cluster(G, p.P);
-  const size_t smem = cluster_smem_bytes(G, p.P, p.max_pages, cs, p.top_k);
+  const void* fn = pick_cluster(G, P);
+  const size_t smem = cluster_smem_bytes(G, P, max_pages, cs, top_k);
   if ((e = ensure_smem(fn, smem)) != cudaSuccess) return e;
   int per_sm = 0;
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDecodeThreads, smem)) !=
       cudaSuccess)
     return e;
-  *out = per_sm >= 2 && cs >= 2;
+  // rows of a thousand pages or more: the chain's whole-GPU scoring and decode kernels win
+  // over the pair's cluster (measured: equal near 16K tokens per sequence at page 16)
+  *out = per_sm >= 2 && cs >= 2 && max_pages < kFusedMaxPages;
   return cudaSuccess;
 }
 

@@ -51,6 +51,7 @@ struct Tiling {
 
 struct WsLayout {
   size_t score_arrive, ready, decode_arrive;  // u32 [B*Hkv] each
+  size_t seq_done;                            // u32 [B]
   size_t scores;                              // f32 [B*Hkv*max_pages]
   size_t sel_idx, sel_count;                  // i32 [B*Hkv*topk_cap], [B*Hkv]
   size_t part_ml, part_acc;                   // f32 [B*Hq*max_splits*2], [..*128]
@@ -93,6 +94,10 @@ struct Params {
   int debug_flags;
   float qscale;          // log2(e) / sqrt(128)
 
+  unsigned* seq_done;    // chain decode: kv heads of a sequence merged so far
+  int chain_append;      // chain: k_new is appended by the estimate kernel; every kernel
+                         // of the chain sees seq_lens + 1 (when there is room) and the
+                         // decode kernel advances seq_lens at its end
   const __half* k_new;   // fused step: token appended per (b, g) before scoring, or null
   const __half* v_new;
   int decode_lag;        // fused: (b, g)'s decode items follow the scoring of pair bg + lag
@@ -161,7 +166,7 @@ cudaError_t launch_topk_union(const Params& p, int row_cap, cudaStream_t s);
 cudaError_t launch_prefill(const Params& p, const __half* k, const __half* v, int n,
                            cudaStream_t s);
 // Whether QUEST_PATH_AUTO takes the one-launch cluster kernel for this step (see quest.h).
-cudaError_t cluster_preferred(const Params& p, int G, int n_layers, bool* out);
+cudaError_t cluster_preferred(int G, int P, int max_pages, int top_k, int nbg, bool* out);
 cudaError_t launch_topk(const Params& p, cudaStream_t s);
 cudaError_t launch_decode(const Params& p, int G, cudaStream_t s);
 cudaError_t launch_fused(const Params& p, int G, int max_ctas, cudaStream_t s);

@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
   pdl_wait();
   const int tile = blockIdx.x, bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
-  const int L = load_len(p, b, kSiteScore);
+  bool appended = false;
+  const int L = load_len(p, b, kSiteScore, &appended);
   const int N = (L + p.P - 1) / p.P;
   const int p0 = tile * p.score_tile_pages;
   const int np = min(p.score_tile_pages, p.max_pages - p0);
@@ -45,7 +46,21 @@ __global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
   for (int j = 0; j < (PerHead ? G : 1); ++j)
     for (int i = n_live + (int)threadIdx.x; i < np; i += blockDim.x)
       row[(size_t)j * p.max_pages + i] = -CUDART_INF_F;
-  if (n_live > 0) score_tile<G, PerHead>(p, b, g, p0, n_live, row, (size_t)p.max_pages);
+  // a chain step's new token goes in with the scoring of its page
+  int ap = -1, aslot = 0, aphys = -1;
+  if (!PerHead && appended) {
+    ap = (L - 1) / p.P;
+    aslot = (L - 1) % p.P;
+    if (ap >= p0 && ap < p0 + n_live) {
+      const int phys = p.block_table[(size_t)b * p.max_pages + ap];
+      aphys = (phys >= 0 && phys < p.num_phys) ? phys : -1;
+    }
+  } else if (!PerHead && p.chain_append && (long long)L == (long long)p.max_pages * p.P &&
+             tile == 0 && g == 0 && threadIdx.x == 0) {
+    report(p, QUEST_ERR_BAD_LENGTH, b, -1, kSiteAppend);  // no room for the new token
+  }
+  if (n_live > 0)
+    score_tile<G, PerHead>(p, b, g, p0, n_live, row, (size_t)p.max_pages, ap, aslot, aphys);
 }
 
 // ---------------------------------------------------------------- top-K
@@ -154,7 +169,22 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Params p) {
   if (arrive_last<kDecodeThreads, false>(&p.decode_arrive[bg], (unsigned)p.n_splits, misc)) {
     merge_splits<G, kDecodeThreads, false>(p, reinterpret_cast<float*>(smem + m.mscale), b, g,
                                            (count + p.pps - 1) / p.pps);
-    if (threadIdx.x == 0) p.decode_arrive[bg] = 0u;
+    if (threadIdx.x == 0) {
+      p.decode_arrive[bg] = 0u;
+      // a chain step that appended: once every kv head of the sequence has merged (so every
+      // work item of it has read its length), the length takes the new token
+      if (p.chain_append) {
+        __threadfence();
+        if (atomicAdd(&p.seq_done[b], 1u) == (unsigned)p.Hkv - 1u) {
+          p.seq_done[b] = 0u;
+          const int L0 = p.seq_lens[b];
+          if (L0 >= 0 && (long long)L0 + 1 <= (long long)p.max_pages * P) {
+            const int phys = p.block_table[(size_t)b * p.max_pages + L0 / P];
+            if (phys >= 0 && phys < p.num_phys) p.seq_lens[b] = L0 + 1;
+          }
+        }
+      }
+    }
   }
 }
 

@@ -132,6 +132,16 @@ def test_decode_rejects_unknown_path(lib):
     assert "path" in lib.quest_last_error().decode()
 
 
+def test_decode_path_rejects_bad_arguments_without_querying(lib):
+    d = desc()
+    assert lib.quest_decode_path(ctypes.byref(d), 16, None, 0) == -q.QUEST_ERR_INVALID_ARG
+    assert lib.quest_decode_path(ctypes.byref(d), 0, None, 1) == -q.QUEST_ERR_INVALID_ARG
+    o = q.opts(path=5)
+    assert lib.quest_decode_path(ctypes.byref(d), 16, ctypes.byref(o), 1) == \
+        -q.QUEST_ERR_INVALID_ARG
+    assert "path" in lib.quest_last_error().decode()
+
+
 def test_prefill_rejects_bad_arguments_without_launching(lib):
     d = desc()
     ws = ctypes.create_string_buffer(1 << 12)

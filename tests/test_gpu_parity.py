@@ -320,6 +320,23 @@ def test_one_launch_step_matches_oracle(geom, path):
                                check_cache=(t % 5 == 4))
 
 
+def test_decode_path_choice():
+    """Short rows with a resident cluster per pair take the one launch, long rows and
+    forced paths take what they are given."""
+    w = wl.tiny(seed=0)
+    pair = H.on_device(w)
+    assert q.decode_path(pair.cache, w.top_k) == q.QUEST_PATH_FUSED
+    assert q.decode_path(pair.cache, w.top_k, q.opts(path=q.QUEST_PATH_CHAIN)) == \
+        q.QUEST_PATH_CHAIN
+    long_w = small(lens=(20000, 3000), batch=2, hq=8, hkv=8, steps=1, budget=512)
+    long_pair = H.on_device(long_w)
+    assert long_pair.cache.max_pages >= 1024
+    assert q.decode_path(long_pair.cache, long_w.top_k) == q.QUEST_PATH_CHAIN
+    assert q.decode_path(long_pair.cache, long_w.top_k, q.opts(cluster_size=2)) == \
+        q.QUEST_PATH_FUSED
+    assert q.decode_path(long_pair.cache, long_w.top_k, n_layers=4) == q.QUEST_PATH_CHAIN
+
+
 def test_chain_path_window_and_no_selection_outputs():
     """The chain path honours sink / local pages and runs without idx_out / count_out (the
     selection then stays in the workspace)."""
