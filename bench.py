@@ -1,8 +1,10 @@
 """Benchmark of the Quest decode step on one GB300 (or N replicas under torchrun).
 
 Workload: one LongChat-7B-shaped layer (32 MHA heads, d=128, page 16), 32768 prefilled
-tokens, token budget 2048 (128 pages); a step appends one token (quest_append) and runs the
-fused score + top-K + sparse decode (quest_decode).  Steps cycle through the workload's 64
+tokens, token budget 2048 (128 pages); a step is one quest_decode_step call: append one
+token, score, top-K, sparse decode, through the path the library chooses (here the chain of
+estimate, top-K and sparse-decode kernels; --path fused for the one-launch kernel).  Steps
+cycle through the workload's 64
 appended tokens (contexts 32769..32832); before each cycle the cache is rewound (outside
 the timed region).  The L2 is flushed before every timed step: a 512 MiB write, then a
 256 MiB read, so that no dirty line of the flush is written back inside the step.
