@@ -559,6 +559,29 @@ def test_bad_lengths_are_reported():
     assert rc == q.QUEST_ERR_BAD_LENGTH
 
 
+@pytest.mark.parametrize("path", [q.QUEST_PATH_FUSED, q.QUEST_PATH_CHAIN], ids=["fused", "chain"])
+def test_step_without_room_or_page_is_reported(path):
+    """A decode step whose token has no room (full row) or whose next page is unmapped
+    reports it and leaves the length alone, through either path."""
+    o = q.opts(path=path)
+    w = small(lens=(32,), batch=1, steps=1)
+    pair = H.on_device(w)
+    cap = pair.cache.max_pages * w.page_size
+    kn, vn = w.k_new[0].cuda(), w.v_new[0].cuda()
+    pair.cache.seq_lens.fill_(cap)                      # full row
+    q.decode_step(pair.cache, w.q[0].cuda(), kn, vn, w.top_k, pair.ws, o)
+    rc, _ = q.read_status(pair.ws)
+    assert rc == q.QUEST_ERR_BAD_LENGTH
+    assert int(pair.cache.seq_lens[0]) == cap
+    q.workspace_init(pair.ws)
+    pair.cache.seq_lens.fill_(32)                       # next token opens page 2 ...
+    pair.cache.block_table[0, 2] = w.num_phys + 7       # ... which points outside the pool
+    q.decode_step(pair.cache, w.q[0].cuda(), kn, vn, w.top_k, pair.ws, o)
+    rc, detail = q.read_status(pair.ws)
+    assert rc == q.QUEST_ERR_BAD_PAGE and detail[0] == 0 and detail[1] == 2
+    assert int(pair.cache.seq_lens[0]) == 32
+
+
 def test_bad_selection_is_reported():
     w = small(lens=(300,), batch=1)
     pair = H.on_device(w)
