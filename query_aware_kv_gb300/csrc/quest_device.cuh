@@ -156,23 +156,25 @@ __device__ __forceinline__ void report(const Params& p, int code, int b, int pag
   }
 }
 
-// Tokens present in sequence b, or 0 (and a report) if seq_lens[b] is out of range.  In a
-// chain step that appends (p.chain_append), the new token counts when the sequence has room
-// for it; *appended then says so.
-__device__ __forceinline__ int load_len(const Params& p, int b, int site,
-                                        bool* appended = nullptr) {
+// Tokens present in sequence b, or 0 (and a report) if seq_lens[b] is out of range.
+__device__ __forceinline__ int load_len(const Params& p, int b, int site) {
   const int L = p.seq_lens[b];
-  const long long cap = (long long)p.max_pages * p.P;
-  if (appended) *appended = false;
-  if (L < 0 || (long long)L > cap) {
+  if (L < 0 || (long long)L > (long long)p.max_pages * p.P) {
     report(p, QUEST_ERR_BAD_LENGTH, b, -1, site);
     return 0;
   }
-  if (p.chain_append && (long long)L + 1 <= cap) {
-    if (appended) *appended = true;
-    return L + 1;
-  }
   return L;
+}
+
+// load_len for the kernels of a chain step: when the step appends (p.chain_append), the new
+// token counts if the sequence has room for it; *appended then says so.
+__device__ __forceinline__ int load_len_step(const Params& p, int b, int site,
+                                             bool* appended = nullptr) {
+  const int L = load_len(p, b, site);
+  const bool app = p.chain_append && (long long)L + 1 <= (long long)p.max_pages * p.P &&
+                   L == p.seq_lens[b];
+  if (appended) *appended = app;
+  return app ? L + 1 : L;
 }
 
 // Bounded wait on an mbarrier phase; false (and a report) once wait_limit_ns has passed.
@@ -326,16 +328,17 @@ __device__ __forceinline__ float corner_dot(const QueryFrag<G>& f, int j, const 
   return s;
 }
 
-// Scores pages [p0, p0 + n_live) of (b, g) into dst[0 .. n_live).  The boxes of those pages
-// are contiguous (logical page order).  Half-warp per page, 16 B of the min row and 16 B of
-// the max row per lane, 4 pages in flight per half-warp.  Called by the whole block.
+// Scores of pages [p0, p0 + n_live) of (b, g) into dst.  The boxes of those pages are
+// contiguous (logical page order).  Half-warp per page, 16 B of the min row and 16 B of the
+// max row per lane, 4 pages in flight per half-warp.  Called by the whole block.
 // PerHead: dst is query head (g * G)'s row of a [B][Hq][max_pages] array and every head of
 // the group writes its own bound (rows `stride` floats apart) instead of the group maximum.
-// Scores of pages [p0, p0 + n_live) of (b, g) into dst.  Page `ap` (if in the tile) first
-// receives this step's token: its K / V rows go to slot `aslot` of physical page `aphys`
-// (-1: unmapped, reported) and its box opens (slot 0) or widens with the new key before it
-// is scored, as in the one-launch kernel.
-template <int G, bool PerHead = false>
+// Append (a chain step, not PerHead): page ap, if in this tile, first takes the step's new
+// token: its K / V rows go to slot `aslot` of physical page `aphys` (-1: unmapped,
+// reported, nothing written) and its box opens (slot 0) or widens with the new key in
+// registers before it is scored, as in the one-launch kernel.  A variant of its own, so
+// that the plain estimate keeps its registers.
+template <int G, bool PerHead = false, bool Append = false>
 __device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, float* dst,
                            size_t stride = 0, int ap = -1, int aslot = 0, int aphys = -1) {
   const int tid = threadIdx.x, nthr = blockDim.x;
@@ -343,7 +346,7 @@ __device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, fl
   QueryFrag<G> f;
   load_query_frag<G>(p, b, g, c, f);
   const __half* box0 = p.meta + box_offset(p, b, g, p0) + 8 * c;
-  const bool has_append = ap >= p0 && ap < p0 + n_live;
+  const bool has_append = Append && !PerHead && ap >= p0 && ap < p0 + n_live;
   uint4 knew = make_uint4(0, 0, 0, 0), vnew = make_uint4(0, 0, 0, 0);
   if (has_append) {
     const size_t o = ((size_t)b * p.Hkv + g) * kHeadDim + 8 * c;
@@ -364,40 +367,42 @@ __device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, fl
         mx[u] = ld_stream_v4(src + kHeadDim);
       }
     }
-    if (has_append) {
+    if constexpr (Append && !PerHead) {
+      if (has_append) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int r = base + u * nhw + hw;
-        if (r >= n_live || p0 + r != ap) continue;
-        if (aphys < 0) {
-          if (c == 0) report(p, QUEST_ERR_BAD_PAGE, b, ap, kSiteAppend);
-          continue;
-        }
-        if (aslot == 0) {
-          mn[u] = knew;
-          mx[u] = knew;
-        } else {
-          const uint32_t a[4] = {mn[u].x, mn[u].y, mn[u].z, mn[u].w};
-          const uint32_t z[4] = {mx[u].x, mx[u].y, mx[u].z, mx[u].w};
-          const uint32_t n[4] = {knew.x, knew.y, knew.z, knew.w};
-          uint32_t ra[4], rz[4];
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const __half2 hn = *reinterpret_cast<const __half2*>(&n[w]);
-            const __half2 l2 = __hmin2(*reinterpret_cast<const __half2*>(&a[w]), hn);
-            const __half2 h2 = __hmax2(*reinterpret_cast<const __half2*>(&z[w]), hn);
-            ra[w] = *reinterpret_cast<const uint32_t*>(&l2);
-            rz[w] = *reinterpret_cast<const uint32_t*>(&h2);
+        for (int u = 0; u < U; ++u) {
+          const int r = base + u * nhw + hw;
+          if (r >= n_live || p0 + r != ap) continue;
+          if (aphys < 0) {
+            if (c == 0) report(p, QUEST_ERR_BAD_PAGE, b, ap, kSiteAppend);
+            continue;
           }
-          mn[u] = make_uint4(ra[0], ra[1], ra[2], ra[3]);
-          mx[u] = make_uint4(rz[0], rz[1], rz[2], rz[3]);
+          if (aslot == 0) {
+            mn[u] = knew;
+            mx[u] = knew;
+          } else {
+            const uint32_t a[4] = {mn[u].x, mn[u].y, mn[u].z, mn[u].w};
+            const uint32_t z[4] = {mx[u].x, mx[u].y, mx[u].z, mx[u].w};
+            const uint32_t n[4] = {knew.x, knew.y, knew.z, knew.w};
+            uint32_t ra[4], rz[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const __half2 hn = *reinterpret_cast<const __half2*>(&n[w]);
+              const __half2 l2 = __hmin2(*reinterpret_cast<const __half2*>(&a[w]), hn);
+              const __half2 h2 = __hmax2(*reinterpret_cast<const __half2*>(&z[w]), hn);
+              ra[w] = *reinterpret_cast<const uint32_t*>(&l2);
+              rz[w] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            mn[u] = make_uint4(ra[0], ra[1], ra[2], ra[3]);
+            mx[u] = make_uint4(rz[0], rz[1], rz[2], rz[3]);
+          }
+          __half* box = p.meta + box_offset(p, b, g, ap) + 8 * c;
+          *reinterpret_cast<uint4*>(box) = mn[u];
+          *reinterpret_cast<uint4*>(box + kHeadDim) = mx[u];
+          const size_t kv = (((size_t)aphys * p.Hkv + g) * p.P + aslot) * kHeadDim + 8 * c;
+          *reinterpret_cast<uint4*>(p.k_pool + kv) = knew;
+          *reinterpret_cast<uint4*>(p.v_pool + kv) = vnew;
         }
-        __half* box = p.meta + box_offset(p, b, g, ap) + 8 * c;
-        *reinterpret_cast<uint4*>(box) = mn[u];
-        *reinterpret_cast<uint4*>(box + kHeadDim) = mx[u];
-        const size_t kv = (((size_t)aphys * p.Hkv + g) * p.P + aslot) * kHeadDim + 8 * c;
-        *reinterpret_cast<uint4*>(p.k_pool + kv) = knew;
-        *reinterpret_cast<uint4*>(p.v_pool + kv) = vnew;
       }
     }
 #pragma unroll

@@ -30,13 +30,15 @@ cudaError_t ensure_smem(const void* fn, size_t bytes) {
 // ---------------------------------------------------------------- scoring
 // grid (n_score_tiles, B*Hkv), 256 threads.
 // PerHead: scores is [B][Hq][max_pages], one row per query head (quest_estimate_heads).
-template <int G, bool PerHead>
+// Append: a chain step that also writes its new token (a variant of its own, so that the
+// plain estimate keeps its registers).
+template <int G, bool PerHead, bool Append>
 __global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
   pdl_wait();
   const int tile = blockIdx.x, bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   bool appended = false;
-  const int L = load_len(p, b, kSiteScore, &appended);
+  const int L = Append ? load_len_step(p, b, kSiteScore, &appended) : load_len(p, b, kSiteScore);
   const int N = (L + p.P - 1) / p.P;
   const int p0 = tile * p.score_tile_pages;
   const int np = min(p.score_tile_pages, p.max_pages - p0);
@@ -48,19 +50,23 @@ __global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
       row[(size_t)j * p.max_pages + i] = -CUDART_INF_F;
   // a chain step's new token goes in with the scoring of its page
   int ap = -1, aslot = 0, aphys = -1;
-  if (!PerHead && appended) {
+  if (Append && appended) {
     ap = (L - 1) / p.P;
     aslot = (L - 1) % p.P;
     if (ap >= p0 && ap < p0 + n_live) {
       const int phys = p.block_table[(size_t)b * p.max_pages + ap];
       aphys = (phys >= 0 && phys < p.num_phys) ? phys : -1;
     }
-  } else if (!PerHead && p.chain_append && (long long)L == (long long)p.max_pages * p.P &&
-             tile == 0 && g == 0 && threadIdx.x == 0) {
+  } else if (Append && (long long)L == (long long)p.max_pages * p.P && tile == 0 && g == 0 &&
+             threadIdx.x == 0) {
     report(p, QUEST_ERR_BAD_LENGTH, b, -1, kSiteAppend);  // no room for the new token
   }
-  if (n_live > 0)
-    score_tile<G, PerHead>(p, b, g, p0, n_live, row, (size_t)p.max_pages, ap, aslot, aphys);
+  if (n_live > 0) {
+    if constexpr (Append)
+      score_tile<G, false, true>(p, b, g, p0, n_live, row, (size_t)p.max_pages, ap, aslot, aphys);
+    else
+      score_tile<G, PerHead>(p, b, g, p0, n_live, row, (size_t)p.max_pages);
+  }
 }
 
 // ---------------------------------------------------------------- top-K
@@ -74,7 +80,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(Params p) {
   extern __shared__ __align__(16) unsigned char sm[];
   pdl_wait();
   const int bg = blockIdx.x, b = bg / p.Hkv;
-  const int L = load_len(p, b, kSiteTopk);
+  const int L = load_len_step(p, b, kSiteTopk);
   const int N = (L + p.P - 1) / p.P;
   int* scratch = reinterpret_cast<int*>(sm + topk_smem_bytes(p.max_pages));
   topk_row<kTopkThreads, false>(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
@@ -149,7 +155,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Params p) {
   pdl_wait();
   const int split = blockIdx.x, bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
-  const int L = load_len(p, b, kSiteDecode);
+  const int L = load_len_step(p, b, kSiteDecode);
   const int N = (L + P - 1) / P;
   int count = N;
   const int* sel_row = nullptr;
@@ -189,19 +195,21 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Params p) {
 }
 
 template <int G>
-static const void* estimate_fn(bool per_head) {
-  return per_head ? (const void*)estimate_kernel<G, true> : (const void*)estimate_kernel<G, false>;
+static const void* estimate_fn(bool per_head, bool append) {
+  if (per_head) return (const void*)estimate_kernel<G, true, false>;
+  return append ? (const void*)estimate_kernel<G, false, true>
+                : (const void*)estimate_kernel<G, false, false>;
 }
 
 template <int G, int P>
 static const void* decode_fn() { return (const void*)decode_kernel<G, P>; }
 
-static const void* pick_estimate(int G, bool per_head) {
+static const void* pick_estimate(int G, bool per_head, bool append) {
   switch (G) {
-    case 1: return estimate_fn<1>(per_head);
-    case 2: return estimate_fn<2>(per_head);
-    case 4: return estimate_fn<4>(per_head);
-    default: return estimate_fn<8>(per_head);
+    case 1: return estimate_fn<1>(per_head, append);
+    case 2: return estimate_fn<2>(per_head, append);
+    case 4: return estimate_fn<4>(per_head, append);
+    default: return estimate_fn<8>(per_head, append);
   }
 }
 
@@ -223,7 +231,7 @@ static const void* pick_decode(int G, int P) {
 }
 
 cudaError_t launch_estimate(const Params& p, int G, bool per_head, cudaStream_t s) {
-  const void* fn = pick_estimate(G, per_head);
+  const void* fn = pick_estimate(G, per_head, !per_head && p.chain_append);
   const size_t smem = 0;
   Params pp = p;
   void* args[] = {&pp};
