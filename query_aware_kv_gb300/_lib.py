@@ -348,7 +348,8 @@ def decode(cache: PagedCache, q: torch.Tensor, top_k: int, ws: torch.Tensor,
            o: Optional[QuestOpts] = None, out=None, lse=None, want_lse: bool = True,
            idx_out: Optional[torch.Tensor] = None, count_out: Optional[torch.Tensor] = None,
            stream=None):
-    """Fused estimate + top-K + sparse decode (one persistent launch)."""
+    """Estimate + top-K + sparse decode: one launch of the cluster kernel or the chain of
+    three kernels (o.path; automatic by default, see decode_path)."""
     _need(q, "q", torch.float16, (cache.batch, cache.desc.num_q_heads, HEAD_DIM))
     out, lse = _out(cache, q, out, lse, want_lse)
     if idx_out is not None:
@@ -365,7 +366,8 @@ def decode_step(cache: PagedCache, q: torch.Tensor, k_new: torch.Tensor, v_new: 
                 top_k: int, ws: torch.Tensor, o: Optional[QuestOpts] = None, out=None, lse=None,
                 want_lse: bool = True, idx_out: Optional[torch.Tensor] = None,
                 count_out: Optional[torch.Tensor] = None, stream=None):
-    """Append (k_new, v_new) and run the fused decode step, in one launch."""
+    """Append (k_new, v_new) and run the decode step over the cache that holds them: one
+    launch, or the chain with the append folded into its estimate (o.path)."""
     _need(q, "q", torch.float16, (cache.batch, cache.desc.num_q_heads, HEAD_DIM))
     shape = (cache.batch, cache.num_kv_heads, HEAD_DIM)
     _need(k_new, "k_new", torch.float16, shape)
@@ -387,7 +389,8 @@ def decode_layers(cache: PagedCache, layers: Sequence[PagedCache], q: Sequence[t
                   k_new: Optional[Sequence[torch.Tensor]] = None,
                   v_new: Optional[Sequence[torch.Tensor]] = None, out=None, lse=None,
                   want_lse: bool = True, stream=None):
-    """The fused step of every layer in one launch.  `cache` holds the shared shape, block
+    """The step of every layer in one call (one launch, or the layers as chains: o.path).
+    `cache` holds the shared shape, block
     table and lengths; `layers[i]` holds layer i's pools and boxes (same shape); with
     k_new / v_new every layer appends its token and the lengths advance once."""
     n = len(layers)
