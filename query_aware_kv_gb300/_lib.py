@@ -390,9 +390,9 @@ def decode_layers(cache: PagedCache, layers: Sequence[PagedCache], q: Sequence[t
                   v_new: Optional[Sequence[torch.Tensor]] = None, out=None, lse=None,
                   want_lse: bool = True, stream=None):
     """The step of every layer in one call (one launch, or the layers as chains: o.path).
-    `cache` holds the shared shape, block
-    table and lengths; `layers[i]` holds layer i's pools and boxes (same shape); with
-    k_new / v_new every layer appends its token and the lengths advance once."""
+    `cache` holds the shared shape, block table and lengths; `layers[i]` holds layer i's
+    pools and boxes (same shape); with k_new / v_new every layer appends its token and the
+    lengths advance once."""
     n = len(layers)
     if len(q) != n or (k_new is not None and (len(k_new) != n or len(v_new) != n)):
         raise ValueError("one q (and k_new, v_new) per layer")
