@@ -77,7 +77,9 @@ typedef void* quest_stream_t; /* cudaStream_t */
  *                    page) so that scoring streams them contiguously without the block
  *                    table.
  *   block_table    : int32 [batch][max_pages], logical page -> physical page.  Entries at
- *                    or past ceil(seq_len / page_size) are never read.
+ *                    or past ceil(seq_len / page_size) are never read, except the page a
+ *                    call's new tokens go to (quest_append, quest_prefill, the decode
+ *                    calls that append).
  *   seq_lens       : int32 [batch], tokens present; written by quest_append,
  *                    quest_prefill and the decode calls that append.
  */
@@ -134,7 +136,8 @@ typedef struct quest_opts {
                                  ([Guide] Best Practices step 2), written to idx rows of
                                  min(G * top_k, max_pages) entries.  Not with sink / local
                                  pages; the fused calls answer QUEST_ERR_UNSUPPORTED.        */
-    int32_t path;             /* quest_decode / quest_decode_step: QUEST_PATH_*.  The chain
+    int32_t path;             /* quest_decode*: QUEST_PATH_* (quest_decode_layers: see there).
+                                 The chain
                                  computes the same step as separate estimate, top-K and
                                  sparse-decode kernels; the estimate writes the new token's
                                  row and box as it scores that page, and the sparse decode
@@ -162,9 +165,9 @@ typedef struct quest_opts {
 int quest_decode_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
                       int32_t n_layers);
 
-/* quest_decode only: never publish the selection, so that every decode work item's
- * bounded wait runs out and the call reports QUEST_ERR_TIMEOUT.  For testing the
- * timeout path; outputs are then unspecified. */
+/* quest_decode only (one-launch path): never publish the selection, so that every decode
+ * work item's bounded wait runs out and the call reports QUEST_ERR_TIMEOUT.  For testing
+ * the timeout path; outputs are then unspecified. */
 #define QUEST_DEBUG_WITHHOLD_SELECTION 1
 /* quest_decode / quest_decode_step: run the work-queue variant of the fused kernel
  * (one persistent grid, global arrival counters) instead of the cluster variant. */
@@ -264,25 +267,29 @@ int quest_sparse_decode(const quest_cache_t* cache, const void* q, const int32_t
                         size_t ws_bytes, const quest_opts_t* opts, quest_stream_t stream);
 
 /*
- * The whole decode step in one persistent launch: quest_estimate, quest_topk and
- * quest_sparse_decode fused ([Guide] Best Practices step 3 suggests fusing the bound
- * estimation with the page gather).  Work items (scoring tiles, then split-K decode
- * items) are taken from a queue in the workspace; the last scoring tile of a (b, g)
- * selects its pages, and that (b, g)'s decode items wait for the selection (a bounded
- * wait).  Same results as the three calls.  idx_out / count_out (layouts of
- * quest_topk) receive the selection if non-NULL.
+ * The whole decode step: quest_estimate, quest_topk and quest_sparse_decode as one call
+ * ([Guide] Best Practices step 3 suggests fusing the bound estimation with the page
+ * gather).  On the one-launch path (opts->path, quest_decode_path) a thread-block cluster
+ * per (sequence, kv head) pair does all of it: every CTA of the cluster scores a share of
+ * the pair's boxes and passes its keys to the cluster's first CTA over distributed shared
+ * memory, that CTA selects the pages (waits are bounded), every CTA attends over a share
+ * of the kept pages, and the first CTA merges the shares.  On the chain path the three
+ * kernels run back to back.  Same results as the three calls, up to the rounding of the
+ * split-K merge.  idx_out / count_out (layouts of quest_topk) receive the selection if
+ * non-NULL.
  */
 int quest_decode(const quest_cache_t* cache, const void* q, int32_t top_k, void* out,
                  float* lse, int32_t* idx_out, int32_t* count_out, void* ws, size_t ws_bytes,
                  const quest_opts_t* opts, quest_stream_t stream);
 
 /*
- * One whole decode step in one launch: the append of quest_append (k_new, v_new: fp16
- * [batch][num_kv_heads][128], NULL for none) folded into quest_decode.  The scoring work
- * item that holds the new token's page widens (or opens) that page's box, writes the
- * token's K/V rows and scores the page with the updated box; selection and attention
- * then cover seq_len + 1 tokens; seq_lens[b] becomes seq_len + 1 when the launch ends.
- * Results equal quest_append followed by quest_decode.
+ * One whole decode step: the append of quest_append (k_new, v_new: fp16
+ * [batch][num_kv_heads][128]) folded into quest_decode.  Whatever scores the new token's
+ * page (a CTA of the pair's cluster, or the chain's estimate kernel) widens (or opens)
+ * that page's box, writes the token's K/V rows and scores the page with the updated box;
+ * selection and attention then cover seq_len + 1 tokens; seq_lens[b] becomes seq_len + 1
+ * at the end of the step (a sequence with no room or an unmapped page is reported and
+ * keeps its length).  Results equal quest_append followed by quest_decode.
  */
 int quest_decode_step(const quest_cache_t* cache, const void* q, const void* k_new,
                       const void* v_new, int32_t top_k, void* out, float* lse, int32_t* idx_out,
@@ -300,8 +307,9 @@ int quest_decode_step(const quest_cache_t* cache, const void* q, const void* k_n
  * opts.path as for quest_decode, the rule counting every layer's pairs; the chain writes
  * every layer's new token first, advances the lengths once, then runs each layer's
  * estimate, top-K and sparse decode.  cache: the shared shape, block_table and seq_lens
- * (its k_pool / v_pool / meta are not used).  layers: host array of n_layers (1..QUEST_MAX_LAYERS) quest_layer_t, read
- * during the call only; pointers as in quest_decode_step.  k_new / v_new: given for every
+ * (its k_pool / v_pool / meta are not used).  layers: host array of n_layers
+ * (1..QUEST_MAX_LAYERS) quest_layer_t, read during the call only; pointers as in
+ * quest_decode_step.  k_new / v_new: given for every
  * layer (each layer appends at slot seq_len[b]; seq_lens advance once, at the end) or for
  * none.  No idx_out.  ws: as quest_decode for this cache and top_k.
  */
