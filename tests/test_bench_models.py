@@ -30,3 +30,23 @@ def test_prefill_bytes_closed_forms():
     assert bench.prefill_bytes(1, 20, 4, 16, [5]) == 2 * (2 * 20 * 4 * 256) + 2 * 4 * 512 + 4 * 512
     # page-aligned start: no box is read
     assert bench.prefill_bytes(2, 16, 1, 16, [16, 32]) == 2 * (2 * 2 * 16 * 256) + 2 * 512
+
+
+def test_clock_summary_reads_throttle_reasons_and_busy_clock():
+    """nvidia-smi lines (csv, no units): the median SM clock over samples under load (above
+    half the maximum), the maximum, and every throttle reason seen active."""
+    c = bench.ClockSampler(0)
+    c.lines = [
+        "345, 2070, 150.2, 0x0000000000000001, Not Active, Not Active, Not Active, Not Active",
+        "2070, 2070, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "1980, 2070, 1350.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "2010, 2070, 1200.0, 0x0000000000000000, Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ]
+    s = c.summary()
+    assert s["sm_max_mhz"] == 2070.0
+    assert s["sm_mhz"] == 2010.0             # median of 2070, 1980, 2010 (345 is idle)
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert s["samples"] == 4
+    c.lines = []
+    assert c.summary() is None
