@@ -460,68 +460,6 @@ __device__ inline TopkSmem topk_smem_at(unsigned char* base, int max_pages) {
   return t;
 }
 
-// Exact selection on keys[0..N) by MSB-first radix select (8-bit digits); used when the
-// threshold bin of the fast path holds too many keys.
-template <int NT, bool kNamed>
-__device__ void topk_radix_keys(const uint32_t* keys, int N, int K, int* idx_out, int* count_out,
-                                int* hist, int* scratch) {
-  const int tid = threadIdx.x;
-  uint32_t prefix = 0, mask = 0;
-  int need = K;
-  int* sel = scratch + 40;  // digit, keys above, keys in the digit's bucket
-#pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += NT) hist[i] = 0;
-    bsync<NT, kNamed>();
-    for (int i = tid; i < N; i += NT) {
-      const uint32_t k = keys[i];
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
-    }
-    bsync<NT, kNamed>();
-    const int cnt = tid < 256 ? hist[255 - tid] : 0;
-    const int incl = block_incl_scan<NT, kNamed>(cnt, scratch);
-    if (tid < 256 && incl >= need && incl - cnt < need) {
-      sel[0] = 255 - tid;
-      sel[1] = incl - cnt;
-      sel[2] = cnt;
-    }
-    bsync<NT, kNamed>();
-    const int digit = sel[0], above = sel[1], bucket = sel[2];
-    need -= above;
-    prefix |= (uint32_t)digit << shift;
-    mask |= 0xFFu << shift;
-    bsync<NT, kNamed>();
-    if (bucket == need) break;  // the whole bucket is kept: threshold found
-  }
-  const int chunk = (N + NT - 1) / NT;
-  const int lo = min(N, tid * chunk), hi = min(N, lo + chunk);
-  int ngt = 0, neq = 0;
-  for (int i = lo; i < hi; ++i) {
-    const uint32_t m = keys[i] & mask;
-    ngt += m > prefix;
-    neq += m == prefix;
-  }
-  const int packed = (ngt << 16) | neq;
-  const int excl = block_incl_scan<NT, kNamed>(packed, scratch) - packed;
-  int eq_before = excl & 0xFFFF;
-  int pos = (excl >> 16) + min(eq_before, need);
-  for (int i = lo; i < hi; ++i) {
-    const uint32_t m = keys[i] & mask;
-    if (m > prefix) {
-      idx_out[pos++] = i;
-    } else if (m == prefix) {
-      if (eq_before < need) idx_out[pos++] = i;
-      ++eq_before;
-    }
-  }
-  if (tid == 0) *count_out = K;
-}
-
-__device__ __forceinline__ unsigned lanemask_lt() {
-  unsigned m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
 
 // Inclusive / exclusive sum over NT threads with warp shuffles and one barrier; tot: shared
 // [NW] ints of the caller's choosing.
