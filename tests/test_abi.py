@@ -163,3 +163,31 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         _lib.load()
+
+
+def _c_layout(tmp_path, struct, fields):
+    """sizeof and offsetof of a quest.h struct as the C compiler lays it out."""
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "quest.h"', 'int main(void) {',
+             f'  printf("%zu\\n", sizeof({struct}));']
+    lines += [f'  printf("%zu\\n", offsetof({struct}, {f}));' for f in fields]
+    lines += ['  return 0;', '}']
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                           str(exe)])
+    out = subprocess.check_output([str(exe)], text=True).split()
+    return int(out[0]), [int(x) for x in out[1:]]
+
+
+@pytest.mark.parametrize("struct,ctype", [("quest_cache_t", q.QuestCacheDesc),
+                                          ("quest_opts_t", q.QuestOpts),
+                                          ("quest_layer_t", q.QuestLayer)])
+def test_binding_structs_match_the_header(tmp_path, struct, ctype):
+    """The ctypes mirrors of the header's structs have the C compiler's size and field
+    offsets, field by field."""
+    fields = [f for f, _ in ctype._fields_]
+    size, offsets = _c_layout(tmp_path, struct, fields)
+    assert ctypes.sizeof(ctype) == size
+    assert [getattr(ctype, f).offset for f in fields] == offsets
