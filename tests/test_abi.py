@@ -191,3 +191,15 @@ def test_binding_structs_match_the_header(tmp_path, struct, ctype):
     size, offsets = _c_layout(tmp_path, struct, fields)
     assert ctypes.sizeof(ctype) == size
     assert [getattr(ctype, f).offset for f in fields] == offsets
+
+
+def test_binding_constants_match_the_header():
+    """Every QUEST_* constant of the header that the binding mirrors has the header's value
+    (read from the header text, so no compiler is involved)."""
+    text = open(os.path.join(ROOT, "include", "quest.h")).read()
+    defines = dict(re.findall(r"#define (QUEST_[A-Z_]+) (\d+)", text))
+    mirrored = [n for n in dir(q) if n.startswith("QUEST_") and isinstance(getattr(q, n), int)]
+    assert len(mirrored) >= 15
+    for name in mirrored:
+        assert name in defines, name
+        assert int(defines[name]) == getattr(q, name), name
