@@ -27,6 +27,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "sparse decode µs/step & HBM GB/s (frac of roofline), 32K ctx, 2048 budget"
+PATH_NAMES = {1: "fused", 2: "chain", 3: "stream"}
 FLUSH_BYTES = 512 << 20
 PAGE = 16
 
@@ -39,11 +40,10 @@ def parse():
     ap.add_argument("--impl", default="quest", choices=["quest", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--decode-lag", type=int, default=0)
     ap.add_argument("--pages-per-split", type=int, default=0)
     ap.add_argument("--score-tile-pages", type=int, default=0)
     ap.add_argument("--trace", default="", help="write a fused-kernel timeline (npy) here")
-    ap.add_argument("--path", default="auto", choices=["auto", "fused", "chain"],
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "chain", "stream"],
                     help="quest_decode / quest_decode_step path (default: the library's choice)")
     ap.add_argument("--cluster-size", type=int, default=0,
                     help="CTAs per (sequence, kv head) cluster for --sweep / --layers (0: automatic)")
@@ -300,8 +300,8 @@ def run_quest(args):
     cnt = torch.empty((1, w.num_kv_heads), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
     path = {"auto": q.QUEST_PATH_AUTO, "fused": q.QUEST_PATH_FUSED,
-            "chain": q.QUEST_PATH_CHAIN}[args.path]
-    opts_main = q.opts(decode_lag=args.decode_lag, pages_per_split=args.pages_per_split,
+            "chain": q.QUEST_PATH_CHAIN, "stream": q.QUEST_PATH_STREAM}[args.path]
+    opts_main = q.opts(pages_per_split=args.pages_per_split,
                        score_tile_pages=args.score_tile_pages, path=path)
 
     def rewind():
@@ -325,12 +325,17 @@ def run_quest(args):
               f"status {rc}", flush=True)
         return
 
-    # warm-up
+    # warm-up: the same loop as the timed one (flush, events, step), so that nothing in the
+    # timed loop runs for the first time
     rewind()
+    wev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     for i in range(args.warmup):
         if i % w.steps == 0:
             rewind()
+        flush_l2()
+        wev[0].record()
         step(i % w.steps)
+        wev[1].record()
     torch.cuda.synchronize()
     rc, detail = q.read_status(ws)
     if rc != 0:
@@ -393,8 +398,8 @@ def run_quest(args):
     if args.trace:
         cap = 1 << 16
         tr = torch.zeros(1 + 2 * cap, dtype=torch.int64, device=dev)
-        o_tr = q.opts(decode_lag=args.decode_lag, pages_per_split=args.pages_per_split,
-                      score_tile_pages=args.score_tile_pages, trace=tr)
+        o_tr = q.opts(pages_per_split=args.pages_per_split,
+                      score_tile_pages=args.score_tile_pages, trace=tr, path=path)
         flush_l2()
         q.decode(cache, w.q[0], K, ws, o_tr, out=out, lse=lse)
         torch.cuda.synchronize()
@@ -478,7 +483,7 @@ def run_quest(args):
     peak, peak_kind = peaks()
     step_bytes = dec_bytes + append_bytes(1, w.num_kv_heads)
     achieved = dec_bytes / (dec_us * 1e-6) / 1e9
-    taken = "chain" if q.decode_path(cache, K, opts_main) == q.QUEST_PATH_CHAIN else "fused"
+    taken = PATH_NAMES[q.decode_path(cache, K, opts_main)]
     traffic = profiled_traffic(taken)
     line = {
         "metric": METRIC, "value": round(mean_step, 3), "unit": "us/step", "n_gpus": world,
@@ -493,9 +498,10 @@ def run_quest(args):
                    "replicas": world},
         "gbs": round(replicas.job_bytes_per_second(step_bytes, world, mean_step * 1e-6) / 1e9, 1),
         "roofline": {"bound": "hbm",
-                     "kernel": "quest_decode, chain: estimate_kernel + topk_kernel + "
-                               "decode_kernel" if taken == "chain"
-                     else "quest_decode, one launch: cluster_kernel",
+                     "kernel": {"chain": "quest_decode, chain: estimate_kernel + topk_kernel + "
+                                         "decode_kernel",
+                                "fused": "quest_decode, one launch: cluster_kernel",
+                                "stream": "quest_decode, one launch: stream_kernel"}[taken],
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
@@ -506,6 +512,8 @@ def run_quest(args):
         "gpu_launches": n * (3 if taken == "chain" else 1),
         "clocks": clk.summary(),
         "detail_us": {"step_mean": round(mean_step, 3), "step_p50": round(statistics.median(step_us), 3),
+                      "step_p90": round(sorted(step_us)[int(0.9 * (n - 1))], 3),
+                      "step_max": round(max(step_us), 3), "step_min": round(min(step_us), 3),
                       "quest_decode": round(dec_us, 3),
                       "quest_decode_l2_warm_back_to_back": round(dec_warm_us, 3),
                       "unfused_chain": round(chain_us, 3),

@@ -105,19 +105,17 @@ typedef struct quest_opts {
                                  items per (sequence, kv head), at least 16 pages; dense
                                  decode: at least 8)                                         */
     int32_t score_tile_pages; /* pages per scoring work item (default 128)                */
-    int32_t max_ctas;         /* fused kernel: cap on persistent CTAs (0 = all that fit)  */
+    int32_t max_ctas;         /* one-launch kernels: cap on persistent CTAs (cluster kernel:
+                                 clusters; stream kernel: CTAs) (0 = all that fit)          */
     int32_t debug_flags;      /* QUEST_DEBUG_* (0 in normal use)                          */
     int64_t wait_limit_ns;    /* bound on any inter-CTA wait (default 1e9 ns)             */
-    int32_t decode_lag;       /* fused kernel: a (b, g)'s decode items are queued after the
-                                 scoring items of the next decode_lag (b, g) pairs
-                                 (<= 0: default 16)                                         */
-    int32_t trace_capacity;   /* fused kernel: records `trace` can hold                   */
-    uint64_t* trace;          /* fused kernel: optional device timeline, NULL = off; zero
-                                 it before the call.  Record i is trace[1 + 2i] =
+    int32_t reserved;         /* must be 0                                                */
+    int32_t trace_capacity;   /* one-launch kernels: records `trace` can hold             */
+    uint64_t* trace;          /* one-launch kernels: optional device timeline, NULL = off;
+                                 zero it before the call.  Record i is trace[1 + 2i] =
                                  %globaltimer ns, trace[2 + 2i] = smid << 48 | cta << 32 |
-                                 event << 24 | item; unused records stay 0.  The cluster
-                                 kernel gives CTA c records [64c, 64c + 64); the queue
-                                 kernel appends and counts them in trace[0].              */
+                                 event << 24 | item; unused records stay 0.  CTA c owns
+                                 records [64c, 64c + 64).                                   */
     int32_t cluster_size;     /* fused kernel: CTAs per (sequence, kv head) cluster, 1..16;
                                  0: the largest size up to 8 at which every pair's cluster
                                  is resident at once (1 when there are more pairs than SMs
@@ -145,33 +143,39 @@ typedef struct quest_opts {
                                  workspace unless idx_out / count_out are given).           */
 } quest_opts_t;
 
-/* Values of quest_opts_t.path.  AUTO (0) takes the one-launch kernel for short rows
- * (max_pages below 1024) when every (sequence, kv head) pair of the call gets a cluster of
- * at least 2 CTAs, all resident at once with 2 CTAs per SM: there the step's fixed cost
- * dominates and one launch pays it once.  Otherwise (longer rows, more pairs, or a CTA
- * needing more than half an SM's shared memory) it takes the chain, whose scoring, top-K
- * and decode kernels spread over the whole GPU.  AUTO always takes the one-launch kernel
- * when cluster_size, trace or debug_flags is set, and the chain when no cluster of the
- * one-launch kernel fits in shared memory.  quest_decode_path() tells which one a call
- * takes. */
+/* Values of quest_opts_t.path.
+ *   FUSED  : one launch of the cluster kernel, a thread-block cluster per (sequence, kv
+ *            head) pair.
+ *   CHAIN  : separate estimate, top-K and sparse-decode kernels, back to back.
+ *   STREAM : one persistent launch of the stream kernel, one CTA per SM, every CTA working
+ *            on every pair: pairs are scored in order over the whole GPU, each pair is
+ *            selected as soon as its last page is scored while later pairs still stream,
+ *            and the kept pages of every pair are decoded by every CTA.  Needs every CTA
+ *            resident at once (cooperative launch), batch <= 1024 and top_k <= 2048.
+ * AUTO (0) takes the one-launch cluster kernel for short rows (max_pages below 1024) when
+ * every (sequence, kv head) pair of the call gets a cluster of at least 2 CTAs, all
+ * resident at once with 2 CTAs per SM: there the step's fixed cost dominates and one
+ * launch pays it once.  Otherwise (longer rows, more pairs, or a CTA needing more than
+ * half an SM's shared memory) it takes the chain, whose scoring, top-K and decode kernels
+ * spread over the whole GPU.  AUTO always takes the one-launch kernel when cluster_size,
+ * trace or debug_flags is set, and the chain when no cluster of the one-launch kernel fits
+ * in shared memory.  quest_decode_path() tells which one a call takes. */
 #define QUEST_PATH_AUTO 0
 #define QUEST_PATH_FUSED 1
 #define QUEST_PATH_CHAIN 2
+#define QUEST_PATH_STREAM 3
 
-/* The path (QUEST_PATH_FUSED or QUEST_PATH_CHAIN) that quest_decode / quest_decode_step
+/* The path (QUEST_PATH_FUSED, _CHAIN or _STREAM) that quest_decode / quest_decode_step
  * (n_layers = 1) or quest_decode_layers (n_layers layers) take for this cache, top_k and
  * opts, or minus a QUEST_ERR_* status on invalid arguments.  Queries the device's occupancy
  * for the one-launch kernel; launches nothing. */
 int quest_decode_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
                       int32_t n_layers);
 
-/* quest_decode only (one-launch path): never publish the selection, so that every decode
- * work item's bounded wait runs out and the call reports QUEST_ERR_TIMEOUT.  For testing
- * the timeout path; outputs are then unspecified. */
+/* quest_decode only (one-launch paths): never publish the selection, so that every
+ * decode work item's bounded wait runs out and the call reports QUEST_ERR_TIMEOUT.  For
+ * testing the timeout path; outputs are then unspecified. */
 #define QUEST_DEBUG_WITHHOLD_SELECTION 1
-/* quest_decode / quest_decode_step: run the work-queue variant of the fused kernel
- * (one persistent grid, global arrival counters) instead of the cluster variant. */
-#define QUEST_DEBUG_QUEUE_KERNEL 2
 
 /* Bytes of workspace the calls below need for this cache, top_k and opts; 0 if the
  * arguments are invalid (see quest_last_error). */

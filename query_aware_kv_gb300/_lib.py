@@ -31,8 +31,7 @@ QUEST_ERR_BAD_LENGTH = 7
 QUEST_ERR_BAD_SELECTION = 8
 QUEST_MAX_PAGES = 16384
 QUEST_DEBUG_WITHHOLD_SELECTION = 1
-QUEST_DEBUG_QUEUE_KERNEL = 2
-QUEST_PATH_AUTO, QUEST_PATH_FUSED, QUEST_PATH_CHAIN = 0, 1, 2
+QUEST_PATH_AUTO, QUEST_PATH_FUSED, QUEST_PATH_CHAIN, QUEST_PATH_STREAM = 0, 1, 2, 3
 HEAD_DIM = 128
 
 # Every symbol include/quest.h declares.
@@ -72,7 +71,7 @@ class QuestOpts(ctypes.Structure):
     _fields_ = [
         ("pages_per_split", ctypes.c_int32), ("score_tile_pages", ctypes.c_int32),
         ("max_ctas", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
-        ("wait_limit_ns", ctypes.c_int64), ("decode_lag", ctypes.c_int32),
+        ("wait_limit_ns", ctypes.c_int64), ("reserved", ctypes.c_int32),
         ("trace_capacity", ctypes.c_int32), ("trace", ctypes.c_void_p),
         ("cluster_size", ctypes.c_int32), ("sink_pages", ctypes.c_int32),
         ("local_pages", ctypes.c_int32), ("gqa_union", ctypes.c_int32),
@@ -156,20 +155,20 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
 
 
 def opts(pages_per_split: int = 0, score_tile_pages: int = 0, max_ctas: int = 0,
-         debug_flags: int = 0, wait_limit_ns: int = 0, decode_lag: int = 0,
-         trace: Optional[torch.Tensor] = None, cluster_size: int = 0, sink_pages: int = 0,
-         local_pages: int = 0, gqa_union: bool = False, path: int = 0) -> QuestOpts:
+         debug_flags: int = 0, wait_limit_ns: int = 0, trace: Optional[torch.Tensor] = None,
+         cluster_size: int = 0, sink_pages: int = 0, local_pages: int = 0,
+         gqa_union: bool = False, path: int = 0) -> QuestOpts:
     """Launch tuning (0 = default).  ``trace``: int64 CUDA tensor of 1 + 2n elements whose
-    first element is zero; receives up to n timeline records of the fused kernel.
+    first element is zero; receives up to n timeline records of a one-launch kernel.
     ``sink_pages`` / ``local_pages``: pages always kept at the start / end of a sequence
-    longer than top_k pages.  ``path``: QUEST_PATH_AUTO / _FUSED / _CHAIN for the decode
-    calls."""
+    longer than top_k pages.  ``path``: QUEST_PATH_AUTO / _FUSED / _CHAIN / _STREAM for the
+    decode calls."""
     cap, ptr = 0, None
     if trace is not None:
         _need(trace, "trace", torch.int64)
         cap, ptr = (trace.numel() - 1) // 2, trace.data_ptr()
     o = QuestOpts(pages_per_split, score_tile_pages, max_ctas, debug_flags, wait_limit_ns,
-                  decode_lag, cap, ptr, cluster_size, sink_pages, local_pages, int(gqa_union),
+                  0, cap, ptr, cluster_size, sink_pages, local_pages, int(gqa_union),
                   int(path))
     o._trace_ref = trace  # keep the buffer alive with the options
     return o
@@ -348,8 +347,8 @@ def decode(cache: PagedCache, q: torch.Tensor, top_k: int, ws: torch.Tensor,
            o: Optional[QuestOpts] = None, out=None, lse=None, want_lse: bool = True,
            idx_out: Optional[torch.Tensor] = None, count_out: Optional[torch.Tensor] = None,
            stream=None):
-    """Estimate + top-K + sparse decode: one launch of the cluster kernel or the chain of
-    three kernels (o.path; automatic by default, see decode_path)."""
+    """Estimate + top-K + sparse decode: one launch of the cluster or the stream kernel, or
+    the chain of three kernels (o.path; automatic by default, see decode_path)."""
     _need(q, "q", torch.float16, (cache.batch, cache.desc.num_q_heads, HEAD_DIM))
     out, lse = _out(cache, q, out, lse, want_lse)
     if idx_out is not None:
@@ -432,7 +431,7 @@ def dense_decode(cache: PagedCache, q: torch.Tensor, ws: torch.Tensor,
 
 def decode_path(cache: PagedCache, top_k: int, o: Optional[QuestOpts] = None,
                 n_layers: int = 1) -> int:
-    """QUEST_PATH_FUSED or QUEST_PATH_CHAIN: the path the decode calls take for this cache,
+    """QUEST_PATH_FUSED, _CHAIN or _STREAM: the path the decode calls take for this cache,
     top_k and options."""
     lib = load()
     r = lib.quest_decode_path(ctypes.byref(cache.desc), int(top_k), _opts_ref(o), int(n_layers))

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libquest.so")
 SOURCES = ["quest_api.cu", "quest_cache_kernels.cu", "quest_step_kernels.cu",
-           "quest_fused_kernel.cu", "quest_cluster_kernel.cu", "quest_static_scratch.cu"]
+           "quest_stream_kernel.cu", "quest_cluster_kernel.cu", "quest_static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

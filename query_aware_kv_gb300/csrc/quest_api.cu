@@ -100,6 +100,8 @@ Tiling make_tiling(const quest_cache_t* c, int top_k, const quest_opts_t* o) {
   t.pps_dense = (int)std::max<long long>(pps, cdiv(c->max_pages, 64));
   t.n_splits_dense = (int)cdiv(c->max_pages, t.pps_dense);
   t.max_splits = std::max(t.n_splits_sparse, t.n_splits_dense);
+  // the stream kernel writes one partial per decode piece of kStreamPiecePages kept pages
+  t.max_splits = std::max<int>(t.max_splits, (int)cdiv(kcap, kStreamPiecePages));
   return t;
 }
 
@@ -117,6 +119,7 @@ WsLayout make_layout(const quest_cache_t* c, const Tiling& t) {
   L.sel_count = off;     off = up256(off + nbg * 4);
   L.part_ml = off;       off = up256(off + nbh * t.max_splits * 2 * 4);
   L.part_acc = off;      off = up256(off + nbh * t.max_splits * kHeadDim * 4);
+  L.sel_pair = off;      off = up256(off + nbg * (size_t)t.topk_cap * 8);
   L.total = off;
   return L;
 }
@@ -138,9 +141,7 @@ Params make_params(const quest_cache_t* c, void* ws, const WsLayout& L, const Ti
   unsigned char* w = static_cast<unsigned char*>(ws);
   WsHeader* h = reinterpret_cast<WsHeader*>(w);
   p.status = &h->status;
-  p.ticket = &h->ticket;
   p.exited = &h->exited;
-  p.epoch = &h->epoch;
   p.score_arrive = reinterpret_cast<unsigned*>(w + L.score_arrive);
   p.ready = reinterpret_cast<unsigned*>(w + L.ready);
   p.decode_arrive = reinterpret_cast<unsigned*>(w + L.decode_arrive);
@@ -150,6 +151,8 @@ Params make_params(const quest_cache_t* c, void* ws, const WsLayout& L, const Ti
   p.sel_count = reinterpret_cast<int*>(w + L.sel_count);
   p.part_ml = reinterpret_cast<float*>(w + L.part_ml);
   p.part_acc = reinterpret_cast<float*>(w + L.part_acc);
+  p.sel_pair = reinterpret_cast<int*>(w + L.sel_pair);
+  p.started = &h->started;
   p.top_k = t.topk_cap;
   p.score_tile_pages = t.score_tile_pages;
   p.n_score_tiles = t.n_score_tiles;
@@ -358,19 +361,28 @@ int quest_sparse_decode(const quest_cache_t* cache, const void* q, const int32_t
                   "quest_sparse_decode");
 }
 
-// The path of a decode call (QUEST_PATH_* in quest.h): *chain on return.
+// The path of a decode call (QUEST_PATH_FUSED, _CHAIN or _STREAM in quest.h).
 static int decide_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
-                       int n_layers, bool* chain) {
+                       int n_layers, int* path_out) {
   const int cs = opts ? opts->cluster_size : 0;
   if (cs < 0 || cs > kMaxClusterSize)
     return fail(QUEST_ERR_INVALID_ARG, "cluster_size %d: use 0 (automatic) or 1..%d", cs,
                 kMaxClusterSize);
   const int path = opts ? opts->path : QUEST_PATH_AUTO;
-  if (path < QUEST_PATH_AUTO || path > QUEST_PATH_CHAIN)
-    return fail(QUEST_ERR_INVALID_ARG, "path %d: use QUEST_PATH_AUTO, _FUSED or _CHAIN", path);
+  if (path < QUEST_PATH_AUTO || path > QUEST_PATH_STREAM)
+    return fail(QUEST_ERR_INVALID_ARG, "path %d: use QUEST_PATH_AUTO, _FUSED, _CHAIN or _STREAM",
+                path);
   const int G = group_of(cache);
+  if (path == QUEST_PATH_STREAM) {
+    if (stream_slots(G, cache->page_size, cache->max_pages, top_k, cache->batch) <= 0)
+      return fail(QUEST_ERR_UNSUPPORTED,
+                  "the stream kernel does not fit this shape (batch %d, max_pages %d, top_k %d)",
+                  cache->batch, cache->max_pages, top_k);
+    *path_out = QUEST_PATH_STREAM;
+    return QUEST_OK;
+  }
   const bool fits = cluster_any_fits(G, cache->page_size, cache->max_pages, top_k);
-  *chain = path == QUEST_PATH_CHAIN;
+  *path_out = path == QUEST_PATH_CHAIN ? QUEST_PATH_CHAIN : QUEST_PATH_FUSED;
   if (path == QUEST_PATH_AUTO && cs == 0 && !(opts && (opts->trace || opts->debug_flags))) {
     bool fused = false;
     const long long nbg = (long long)n_layers * cache->batch * cache->num_kv_heads;
@@ -379,7 +391,7 @@ static int decide_path(const quest_cache_t* cache, int32_t top_k, const quest_op
                                                    &fused)
                                : cudaSuccess;
     if (e != cudaSuccess) return cuda_fail(e, "occupancy of the one-launch kernel");
-    *chain = !fused;
+    *path_out = fused ? QUEST_PATH_FUSED : QUEST_PATH_CHAIN;
   }
   return QUEST_OK;
 }
@@ -418,39 +430,36 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   p.dense = 0;
   p.k_new = static_cast<const __half*>(k_new);
   p.v_new = static_cast<const __half*>(v_new);
-  p.decode_lag = (opts && opts->decode_lag > 0) ? opts->decode_lag : kDefaultDecodeLag;
   p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
   p.trace_capacity = opts ? opts->trace_capacity : 0;
-  if (opts && (opts->debug_flags & QUEST_DEBUG_QUEUE_KERNEL)) {
-    const long long items = (long long)cache->batch * cache->num_kv_heads *
-                            ((long long)t.n_score_tiles + t.n_splits_sparse);
-    if (items > 0x7fffffffLL) return fail(QUEST_ERR_UNSUPPORTED, "too many work items");
-    return launched(launch_fused(p, group_of(cache), opts ? opts->max_ctas : 0,
-                                 static_cast<cudaStream_t>(stream)),
-                    what);
-  }
   const int cs = opts ? opts->cluster_size : 0;  // 0: the library picks
-  bool chain = false;
-  if ((rc = decide_path(cache, top_k, opts, 1, &chain))) return rc;
-  const bool fits = cluster_any_fits(group_of(cache), cache->page_size, cache->max_pages, top_k);
-  if (chain) {
+  const int G = group_of(cache);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int path = QUEST_PATH_FUSED;
+  if ((rc = decide_path(cache, top_k, opts, 1, &path))) return rc;
+  if (path == QUEST_PATH_STREAM) {
+    // one persistent launch over the whole GPU; the selection is written out only when asked
+    p.chain_append = p.k_new != nullptr ? 1 : 0;
+    p.n_splits = (int)cdiv(std::min(top_k, cache->max_pages), kStreamPiecePages);
+    p.sel_idx = idx_out;
+    p.sel_count = count_out;
+    const LayerPtrs lay{p.k_pool, p.v_pool, p.meta, p.q, p.k_new, p.v_new, p.out, p.lse};
+    return launched(launch_stream(p, lay, G, opts ? opts->max_ctas : 0, s), what);
+  }
+  if (path == QUEST_PATH_CHAIN) {
     // the same step as separate kernels: estimate (which also writes the new token's row
     // and widens its box), top-K, sparse decode (which advances the lengths at its end);
     // the selection goes to idx_out / count_out if given, else to the workspace
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int G = group_of(cache);
     p.chain_append = p.k_new != nullptr ? 1 : 0;
     cudaError_t e = launch_estimate(p, G, false, s);
     if (e == cudaSuccess) e = launch_topk(p, s);
     if (e == cudaSuccess) e = launch_decode(p, G, s);
     return launched(e, what);
   }
-  if (!fits)
+  if (!cluster_any_fits(G, cache->page_size, cache->max_pages, top_k))
     return fail(QUEST_ERR_UNSUPPORTED, "max_pages %d needs more shared memory than a CTA has",
                 cache->max_pages);
-  if (cs > 0 &&
-      cluster_smem_bytes(group_of(cache), cache->page_size, cache->max_pages, cs, top_k) >
-          kMaxSmem)
+  if (cs > 0 && cluster_smem_bytes(G, cache->page_size, cache->max_pages, cs, top_k) > kMaxSmem)
     return fail(QUEST_ERR_UNSUPPORTED, "cluster_size %d needs more shared memory than a CTA has",
                 cs);
   p.sel_idx = idx_out;     // the cluster kernel writes the selection only when asked
@@ -458,9 +467,7 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   LayerTable lt{};
   lt.n = 1;
   lt.l[0] = LayerPtrs{p.k_pool, p.v_pool, p.meta, p.q, p.k_new, p.v_new, p.out, p.lse};
-  return launched(launch_cluster(p, lt, group_of(cache), cs, opts ? opts->max_ctas : 0,
-                                 static_cast<cudaStream_t>(stream)),
-                  what);
+  return launched(launch_cluster(p, lt, G, cs, opts ? opts->max_ctas : 0, s), what);
 }
 
 int quest_decode_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
@@ -470,9 +477,9 @@ int quest_decode_path(const quest_cache_t* cache, int32_t top_k, const quest_opt
   if ((rc = check_topk(top_k))) return -rc;
   if (n_layers < 1 || n_layers > QUEST_MAX_LAYERS)
     return -fail(QUEST_ERR_INVALID_ARG, "n_layers %d: use 1..%d", n_layers, QUEST_MAX_LAYERS);
-  bool chain = false;
-  if ((rc = decide_path(cache, top_k, opts, n_layers, &chain))) return -rc;
-  return chain ? QUEST_PATH_CHAIN : QUEST_PATH_FUSED;
+  int path = QUEST_PATH_FUSED;
+  if ((rc = decide_path(cache, top_k, opts, n_layers, &path))) return -rc;
+  return path;
 }
 
 int quest_decode(const quest_cache_t* cache, const void* q, int32_t top_k, void* out, float* lse,
@@ -544,10 +551,34 @@ int quest_decode_layers(const quest_cache_t* cache, const quest_layer_t* layers,
   p.trace_capacity = opts ? opts->trace_capacity : 0;
   const int cs = opts ? opts->cluster_size : 0;
   const int G = group_of(cache);
-  bool chain = false;
-  if ((rc = decide_path(cache, top_k, opts, n_layers, &chain))) return rc;
+  int path = QUEST_PATH_FUSED;
+  if ((rc = decide_path(cache, top_k, opts, n_layers, &path))) return rc;
   const bool fits = cluster_any_fits(G, cache->page_size, cache->max_pages, top_k);
-  if (chain) {
+  if (path == QUEST_PATH_STREAM) {
+    // one stream launch per layer; every layer appends its token at the same position and
+    // only the last launch advances the lengths
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Params c = make_params(cache, ws, Lw, t, opts);
+    c.top_k = top_k;
+    c.dense = 0;
+    c.n_splits = (int)cdiv(std::min(top_k, cache->max_pages), kStreamPiecePages);
+    c.chain_append = append ? 1 : 0;
+    c.sel_idx = nullptr;
+    c.sel_count = nullptr;
+    c.trace = p.trace;
+    c.trace_capacity = p.trace_capacity;
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < n_layers && e == cudaSuccess; ++i) {
+      Params l = c;
+      l.k_pool = lt.l[i].k_pool;
+      l.v_pool = lt.l[i].v_pool;
+      l.meta = lt.l[i].meta;
+      l.hold_lengths = i + 1 < n_layers ? 1 : 0;
+      e = launch_stream(l, lt.l[i], G, opts ? opts->max_ctas : 0, s);
+    }
+    return launched(e, "quest_decode_layers");
+  }
+  if (path == QUEST_PATH_CHAIN) {
     // layer after layer as separate kernels: every layer's token row and box first (at the
     // same position), the lengths advanced once, then each layer's estimate, top-K and
     // sparse decode over the cache that holds the new token

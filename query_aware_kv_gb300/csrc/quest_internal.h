@@ -21,7 +21,6 @@ constexpr int kDefaultPagesPerSplit = 8;    // dense decode work items (at least
 constexpr int kMinSparsePagesPerSplit = 16;  // sparse decode work items, by default
 constexpr int kDefaultScoreTilePages = 128;
 constexpr long long kDefaultWaitNs = 1000000000LL;
-constexpr int kDefaultDecodeLag = 16;
 
 // Places in the code that record a device fault (third detail word).
 enum FaultSite : int {
@@ -33,10 +32,9 @@ enum FaultSite : int {
 struct WsHeader {
   int status;        // QUEST_OK or the first QUEST_ERR_* the device saw
   int detail[3];     // sequence, logical page, fault site
-  unsigned ticket;   // fused kernel: next work item
-  unsigned exited;   // fused kernel: CTAs that left the work loop
-  unsigned epoch;    // fused kernel: launches completed (selection flags carry epoch + 1)
-  unsigned pad[57];
+  unsigned exited;   // cluster kernel: CTAs that have left (the last advances the lengths)
+  unsigned started;  // stream kernel: CTAs that have read the lengths of an appending step
+  unsigned pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -55,6 +53,7 @@ struct WsLayout {
   size_t scores;                              // f32 [B*Hkv*max_pages]
   size_t sel_idx, sel_count;                  // i32 [B*Hkv*topk_cap], [B*Hkv]
   size_t part_ml, part_acc;                   // f32 [B*Hq*max_splits*2], [..*128]
+  size_t sel_pair;                            // i32x2 [B*Hkv*topk_cap] (logical, physical)
   size_t total;
 };
 
@@ -81,9 +80,7 @@ struct Params {
   int dense;             // decode every page instead of a selection
 
   int* status;           // -> WsHeader::status (detail follows it)
-  unsigned* ticket;
   unsigned* exited;
-  unsigned* epoch;
   unsigned* score_arrive;
   unsigned* ready;
   unsigned* decode_arrive;
@@ -95,13 +92,16 @@ struct Params {
   float qscale;          // log2(e) / sqrt(128)
 
   unsigned* seq_done;    // chain decode: kv heads of a sequence merged so far
-  int chain_append;      // chain: k_new is appended by the estimate kernel; every kernel
-                         // of the chain sees seq_lens + 1 (when there is room) and the
-                         // decode kernel advances seq_lens at its end
+  int chain_append;      // chain and stream kernel: the step appends k_new; every kernel
+                         // sees seq_lens + 1 (when there is room) and the last step of the
+                         // call advances seq_lens
+  int* sel_pair;         // stream kernel: [B][Hkv][top_k] (logical page, physical page)
+  unsigned* started;     // stream kernel: CTAs that have read the lengths
+  int hold_lengths;      // stream kernel: append, but leave seq_lens to a later launch
+                         // (every layer but the last of a multi-layer step)
   const __half* k_new;   // fused step: token appended per (b, g) before scoring, or null
   const __half* v_new;
-  int decode_lag;        // fused: (b, g)'s decode items follow the scoring of pair bg + lag
-  unsigned long long* trace;  // fused: optional timeline, trace[0] = records written
+  unsigned long long* trace;  // one-launch kernels: optional timeline (quest_opts_t.trace)
   int trace_capacity;
 };
 
@@ -125,7 +125,6 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
 
 // Dynamic shared memory of the decode-capable kernels (bytes), see quest_device.cuh.
 size_t decode_smem_bytes(int G, int P, int topk_keys, int score_tile_pages);
-size_t fused_smem_bytes(int G, int P, int max_pages);
 // Raise a kernel's dynamic shared-memory cap (once per device and kernel).
 // Per-layer tensors of a multi-layer fused step (the shape, block table and lengths are
 // shared by every layer).  Passed by value as a kernel parameter.
@@ -169,12 +168,18 @@ cudaError_t launch_prefill(const Params& p, const __half* k, const __half* v, in
 cudaError_t cluster_preferred(int G, int P, int max_pages, int top_k, int nbg, bool* out);
 cudaError_t launch_topk(const Params& p, cudaStream_t s);
 cudaError_t launch_decode(const Params& p, int G, cudaStream_t s);
-cudaError_t launch_fused(const Params& p, int G, int max_ctas, cudaStream_t s);
 size_t cluster_smem_bytes(int G, int P, int max_pages, int cs, int top_k);
 bool cluster_any_fits(int G, int P, int max_pages, int top_k);
 cudaError_t launch_cluster(const Params& p, const LayerTable& lt, int G, int cs, int max_clusters,
                            cudaStream_t s);
 constexpr int kMaxClusterSize = 16;
+// The stream kernel (one persistent launch, every CTA on every pair): ring slots for this
+// shape (0 if it does not fit), its shared memory, and its launch.
+int stream_slots(int G, int P, int max_pages, int top_k, int batch);
+size_t stream_smem_bytes(int G, int P, int max_pages, int top_k, int batch);
+cudaError_t launch_stream(const Params& p, const LayerPtrs& lay, int G, int max_ctas,
+                          cudaStream_t s);
+constexpr int kStreamPiecePages = 8;  // kept pages per decode piece of the stream kernel
 constexpr size_t kMaxSmem = 227 * 1024;  // dynamic shared memory of one CTA
 
 }  // namespace quest

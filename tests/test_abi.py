@@ -125,11 +125,25 @@ def test_calls_reject_bad_arguments_without_launching(lib):
 
 def test_decode_rejects_unknown_path(lib):
     d = desc()
-    o = q.opts(path=3)
+    o = q.opts(path=4)
     ws = ctypes.c_void_p(1 << 20)  # never dereferenced: the call fails before any launch
     assert lib.quest_decode(ctypes.byref(d), 16, 16, 16, 256, 256, 256, ws,
                             1 << 40, ctypes.byref(o), None) == q.QUEST_ERR_INVALID_ARG
     assert "path" in lib.quest_last_error().decode()
+
+
+def test_stream_path_is_chosen_on_request_and_bounded(lib):
+    """QUEST_PATH_STREAM is taken when asked for (no device query needed); shapes beyond its
+    on-chip tables (more than 1024 sequences, top_k above 2048) are refused."""
+    d = desc()
+    o = q.opts(path=q.QUEST_PATH_STREAM)
+    assert lib.quest_decode_path(ctypes.byref(d), 16, ctypes.byref(o), 1) == q.QUEST_PATH_STREAM
+    assert lib.quest_decode_path(ctypes.byref(d), 4096, ctypes.byref(o), 1) == \
+        -q.QUEST_ERR_UNSUPPORTED
+    big = desc(batch=2000, num_q_heads=1, num_kv_heads=1)
+    assert lib.quest_decode_path(ctypes.byref(big), 16, ctypes.byref(o), 1) == \
+        -q.QUEST_ERR_UNSUPPORTED
+    assert "stream" in lib.quest_last_error().decode()
 
 
 def test_decode_path_rejects_bad_arguments_without_querying(lib):

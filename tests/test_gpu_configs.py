@@ -24,8 +24,8 @@ import harness as H
 pytestmark = pytest.mark.gpu
 
 
-PATHS = [q.QUEST_PATH_AUTO, q.QUEST_PATH_FUSED]
-PATH_IDS = ["auto", "fused"]
+PATHS = [q.QUEST_PATH_AUTO, q.QUEST_PATH_FUSED, q.QUEST_PATH_STREAM]
+PATH_IDS = ["auto", "fused", "stream"]
 
 
 def _run(w, steps, check_needles=True, path=q.QUEST_PATH_AUTO):
@@ -36,11 +36,12 @@ def _run(w, steps, check_needles=True, path=q.QUEST_PATH_AUTO):
                                check_needles=check_needles, check_cache=(t == steps - 1))
 
 
-def test_longchat_32k_every_step():
+@pytest.mark.parametrize("path", [q.QUEST_PATH_AUTO, q.QUEST_PATH_STREAM], ids=["auto", "stream"])
+def test_longchat_32k_every_step(path):
     """The benchmark workload: 32768 prefilled tokens, then all 64 decode steps (each
     appends a token: 2049 -> 2052 pages), 32 MHA heads, budget 2048."""
     w = wl.longchat_32k(seed=0, device="cuda")
-    _run(w, w.steps)
+    _run(w, w.steps, path=path)
 
 
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)

@@ -166,12 +166,15 @@ def test_topk_sink_and_local_pages(sink, local):
     H.assert_status_ok(pair.ws)
 
 
-@pytest.mark.parametrize("cs", [0, 1, 8])
+@pytest.mark.parametrize("cs", [0, 1, 8, "stream"])
 def test_fused_step_with_sink_and_local_pages(cs):
     w = small(lens=(2500, 1, 700, 16 * 9), batch=4, steps=2, hq=8, hkv=4, budget=256,
               outliers=4)
     pair = H.on_device(w)
-    o = q.opts(cluster_size=cs, sink_pages=2, local_pages=2)
+    if cs == "stream":
+        o = q.opts(path=q.QUEST_PATH_STREAM, sink_pages=2, local_pages=2)
+    else:
+        o = q.opts(cluster_size=cs, sink_pages=2, local_pages=2)
     for t in range(w.steps):
         H.run_step_and_compare(pair, t, w.top_k, opts=o, one_launch=True, sink=2, local=2,
                                check_cache=(t == w.steps - 1))
@@ -306,12 +309,16 @@ def test_decode_steps_match_oracle(geom, fused):
         H.run_step_and_compare(pair, t, w.top_k, fused=fused)
 
 
-@pytest.mark.parametrize("path", [q.QUEST_PATH_FUSED, q.QUEST_PATH_CHAIN], ids=["fused", "chain"])
+ALL_PATHS = [q.QUEST_PATH_FUSED, q.QUEST_PATH_CHAIN, q.QUEST_PATH_STREAM]
+ALL_PATH_IDS = ["fused", "chain", "stream"]
+
+
+@pytest.mark.parametrize("path", ALL_PATHS, ids=ALL_PATH_IDS)
 @pytest.mark.parametrize("geom", GEOMS, ids=lambda g: f"hq{g['hq']}_hkv{g['hkv']}_p{g['P']}")
 def test_one_launch_step_matches_oracle(geom, path):
-    """quest_decode_step, as the one-launch kernel (append folded in) and as the chain of
-    separate kernels: boxes, pools, lengths, selection and attention all match the oracle
-    step after step (pages open and fill)."""
+    """quest_decode_step through each path (the cluster kernel and the stream kernel with
+    the append folded in, and the chain of separate kernels): boxes, pools, lengths,
+    selection and attention all match the oracle step after step (pages open and fill)."""
     w = small(lens=(1500, 1, 333, 0, 16 * 30 - 2), batch=5, steps=20, outliers=4, **geom)
     pair = H.on_device(w)
     o = q.opts(path=path)
@@ -362,24 +369,33 @@ def test_tiny_config():
     H.run_step_and_compare(pair, 0, w.top_k, one_launch=True, check_cache=True)
 
 
-def test_fused_queue_orders_agree():
-    """Any decode_lag (queue interleaving) and CTA count gives the same selection and the
-    same outputs up to split-merge rounding."""
+def test_stream_cta_counts_agree():
+    """The stream kernel with any number of CTAs (one CTA doing every pair's scoring,
+    selection, decode and merge; a few; one per SM) gives bit-identical selections and
+    outputs: each decode piece's partial and the merge order do not depend on which CTA
+    ran them."""
     w = small(lens=(4000, 2100, 5000), batch=3, hq=8, hkv=4, budget=512, outliers=4)
     pair = H.on_device(w)
     qd = w.q[0].cuda()
     idx0 = torch.empty((3, 4, w.top_k), dtype=torch.int32, device="cuda")
     cnt0 = torch.empty((3, 4), dtype=torch.int32, device="cuda")
-    base, base_lse = q.decode(pair.cache, qd, w.top_k, pair.ws, q.opts(debug_flags=q.QUEST_DEBUG_QUEUE_KERNEL),
-                              idx_out=idx0, count_out=cnt0)
-    for lag, ctas in [(1, 0), (2, 1), (3, 7), (100, 0), (5, 300)]:
+    o = q.opts(path=q.QUEST_PATH_STREAM)
+    base, base_lse = q.decode(pair.cache, qd, w.top_k, pair.ws, o, idx_out=idx0, count_out=cnt0)
+    H.assert_status_ok(pair.ws)
+    qh = w.q[0].numpy().astype(np.float32)
+    ref_scores = oracle.score(pair.ref, qh)
+    ri, rc = oracle.topk(pair.ref, ref_scores, w.top_k)
+    H.assert_selection(idx0.cpu().numpy(), cnt0.cpu().numpy(), ref_scores, ri, rc)
+    ro, rl = oracle.attend(pair.ref, qh, idx0.cpu().numpy(), cnt0.cpu().numpy())
+    H.assert_attention_close(base, base_lse, ro, rl)
+    for ctas in [1, 2, 3, 7, 300]:
         idx = torch.empty_like(idx0)
         cnt = torch.empty_like(cnt0)
         out, lse = q.decode(pair.cache, qd, w.top_k, pair.ws,
-                            q.opts(decode_lag=lag, max_ctas=ctas, debug_flags=q.QUEST_DEBUG_QUEUE_KERNEL),
+                            q.opts(path=q.QUEST_PATH_STREAM, max_ctas=ctas),
                             idx_out=idx, count_out=cnt)
-        assert torch.equal(idx, idx0) and torch.equal(cnt, cnt0)
-        assert torch.equal(out, base) and torch.equal(lse, base_lse)
+        assert torch.equal(idx, idx0) and torch.equal(cnt, cnt0), ctas
+        assert torch.equal(out, base) and torch.equal(lse, base_lse), ctas
     H.assert_status_ok(pair.ws)
 
 
@@ -393,16 +409,17 @@ def test_every_cluster_size_matches_oracle(cs):
                                check_cache=(t == w.steps - 1))
 
 
-def test_queue_variant_matches_cluster_variant():
+def test_stream_variant_matches_cluster_variant():
     w = small(lens=(4000, 2100, 5000), batch=3, hq=8, hkv=4, budget=512, outliers=4)
     pair = H.on_device(w)
     qd = w.q[0].cuda()
     idx0 = torch.empty((3, 4, w.top_k), dtype=torch.int32, device="cuda")
     cnt0 = torch.empty((3, 4), dtype=torch.int32, device="cuda")
-    base, base_lse = q.decode(pair.cache, qd, w.top_k, pair.ws, idx_out=idx0, count_out=cnt0)
+    base, base_lse = q.decode(pair.cache, qd, w.top_k, pair.ws, q.opts(path=q.QUEST_PATH_FUSED),
+                              idx_out=idx0, count_out=cnt0)
     idx = torch.empty_like(idx0)
     cnt = torch.empty_like(cnt0)
-    out, lse = q.decode(pair.cache, qd, w.top_k, pair.ws, q.opts(debug_flags=q.QUEST_DEBUG_QUEUE_KERNEL),
+    out, lse = q.decode(pair.cache, qd, w.top_k, pair.ws, q.opts(path=q.QUEST_PATH_STREAM),
                         idx_out=idx, count_out=cnt)
     H.assert_status_ok(pair.ws)
     assert torch.equal(idx, idx0) and torch.equal(cnt, cnt0)
@@ -410,16 +427,15 @@ def test_queue_variant_matches_cluster_variant():
     torch.testing.assert_close(lse, base_lse, atol=1e-4, rtol=0)
 
 
-@pytest.mark.parametrize("cs", [0, 1, 3, 16])
+@pytest.mark.parametrize("cs", [0, 1, 3, 16, "stream"])
 def test_fused_step_long_rows(cs):
-    """Rows of 1.2K-3.2K pages (the register-resident selection's larger size classes) in
-    the fused step, two decode steps."""
+    """Rows of 1.2K-3.2K pages in the one-launch steps, two decode steps."""
     w = small(lens=(33000, 20000, 51000), batch=3, hq=8, hkv=4, steps=2, budget=2048,
               outliers=4, needles_per_head=2)
     pair = H.on_device(w)
+    o = q.opts(path=q.QUEST_PATH_STREAM) if cs == "stream" else q.opts(cluster_size=cs)
     for t in range(w.steps):
-        H.run_step_and_compare(pair, t, w.top_k, opts=q.opts(cluster_size=cs), one_launch=True,
-                               check_needles=True)
+        H.run_step_and_compare(pair, t, w.top_k, opts=o, one_launch=True, check_needles=True)
 
 
 def test_trace_records_a_timeline():
@@ -439,6 +455,28 @@ def test_trace_records_a_timeline():
     # one selection and one merge per (b, g), by the leader of its cluster
     assert int((ev == 22).sum()) == w.batch * w.num_kv_heads
     assert int((ev == 26).sum()) == w.batch * w.num_kv_heads
+    assert (t.max() - t.min()) < 1e9
+
+
+def test_stream_trace_records_a_timeline():
+    """The stream kernel's timeline: every CTA starts and exits; one selection and one
+    merge per (b, g), each by some CTA's selector team."""
+    w = small(lens=(3000, 700), batch=2, budget=256)
+    pair = H.on_device(w)
+    cap = 64 * 160
+    tr = torch.zeros(1 + 2 * cap, dtype=torch.int64, device="cuda")
+    q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws,
+             q.opts(trace=tr, path=q.QUEST_PATH_STREAM))
+    H.assert_status_ok(pair.ws)
+    rec = tr[1:].view(cap, 2).cpu().numpy()
+    rec = rec[rec[:, 0] != 0]
+    t, info = rec[:, 0], rec[:, 1].astype(np.uint64)
+    ev = (info >> np.uint64(24)) & np.uint64(0xff)
+    ctas = (info >> np.uint64(32)) & np.uint64(0xffff)
+    n_ctas = len(set(int(c) for c in ctas[ev == 1]))
+    assert n_ctas >= 1 and int((ev == 2).sum()) == n_ctas
+    assert int((ev == 8).sum()) == w.batch * w.num_kv_heads    # selections done
+    assert int((ev == 10).sum()) == w.batch * w.num_kv_heads   # merges done
     assert (t.max() - t.min()) < 1e9
 
 
@@ -487,16 +525,22 @@ def test_workspace_reuse_many_calls():
     # the header counters are back to zero
     hdr = pair.ws[:32].view(torch.int32).cpu().tolist()
     assert hdr[4] == 0 and hdr[5] == 0
-    # so they are after one-launch steps, and after the queue variant (which also counts
-    # its launches in the epoch word)
+    # so they are after one-launch steps through the cluster kernel and the stream kernel
     for t in range(w.steps):
         H.run_step_and_compare(pair, t, w.top_k, one_launch=True)
-    qo = q.opts(debug_flags=q.QUEST_DEBUG_QUEUE_KERNEL)
+    so = q.opts(path=q.QUEST_PATH_STREAM)
     for _ in range(5):
-        q.decode(pair.cache, qd, w.top_k, pair.ws, qo)
+        out_s, _ = q.decode(pair.cache, qd, w.top_k, pair.ws, so)
+    for t in range(w.steps):
+        H.run_step_and_compare(pair, t, w.top_k, opts=so, one_launch=True)
     H.assert_status_ok(pair.ws)
     hdr = pair.ws[:32].view(torch.int32).cpu().tolist()
-    assert hdr[4] == 0 and hdr[5] == 0 and hdr[6] == 5
+    assert hdr[4] == 0 and hdr[5] == 0
+    # and so are the per-pair arrival counters and selection flags (the first three
+    # arrays after the header)
+    nbg = w.batch * w.num_kv_heads
+    ctr = pair.ws[256:256 + 3 * 256 + 4 * nbg].view(torch.int32).cpu().numpy()
+    assert not ctr.any()
 
 
 def test_planted_needles_selected_on_gpu():
@@ -508,18 +552,24 @@ def test_planted_needles_selected_on_gpu():
         H.run_step_and_compare(pair, t, w.top_k, check_needles=True)
 
 
-def test_empty_and_single_token_sequences():
+@pytest.mark.parametrize("path", ALL_PATHS, ids=ALL_PATH_IDS)
+def test_empty_and_single_token_sequences(path):
     w = small(lens=(0, 1, 0), steps=2)
     pair = H.on_device(w)
     qd = w.q[0].cuda()
-    out, lse = q.decode(pair.cache, qd, w.top_k, pair.ws)
+    o = q.opts(path=path)
+    idx = torch.empty((3, w.num_kv_heads, w.top_k), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((3, w.num_kv_heads), dtype=torch.int32, device="cuda")
+    out, lse = q.decode(pair.cache, qd, w.top_k, pair.ws, o, idx_out=idx, count_out=cnt)
     H.assert_status_ok(pair.ws)
     assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
-    phys = int(w.block_table[1, 0])
+    assert torch.all(cnt[0] == 0) and torch.all(idx[0] == -1) and torch.all(cnt[1] == 1)
     ro, rl = oracle.dense(pair.ref, w.q[0].numpy())
     H.assert_attention_close(out, lse, ro, rl)
     for t in range(w.steps):
-        H.run_step_and_compare(pair, t, w.top_k)
+        H.run_step_and_compare(pair, t, w.top_k, opts=o)
+    for t in range(w.steps):
+        H.run_step_and_compare(pair, t, w.top_k, opts=o, one_launch=True, check_cache=True)
 
 
 # ---------------------------------------------------------------- device-side faults
@@ -536,10 +586,11 @@ def test_bad_block_table_entry_is_reported():
     q.build_meta(pair.cache, pair.ws)
     rc, detail = q.read_status(pair.ws)
     assert rc == q.QUEST_ERR_BAD_PAGE and detail[0] == 1 and detail[1] == 3
-    q.workspace_init(pair.ws)
-    q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws)
-    rc, detail = q.read_status(pair.ws)
-    assert rc == q.QUEST_ERR_BAD_PAGE
+    for path in ALL_PATHS:
+        q.workspace_init(pair.ws)
+        q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws, q.opts(path=path))
+        rc, detail = q.read_status(pair.ws)
+        assert rc == q.QUEST_ERR_BAD_PAGE, path
 
 
 def test_bad_lengths_are_reported():
@@ -553,13 +604,14 @@ def test_bad_lengths_are_reported():
     assert rc == q.QUEST_ERR_BAD_LENGTH
     assert int(pair.cache.seq_lens[0]) == cap      # untouched
     pair.cache.seq_lens.fill_(cap + 1)             # beyond the row
-    q.workspace_init(pair.ws)
-    q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws)
-    rc, _ = q.read_status(pair.ws)
-    assert rc == q.QUEST_ERR_BAD_LENGTH
+    for path in ALL_PATHS:
+        q.workspace_init(pair.ws)
+        q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws, q.opts(path=path))
+        rc, _ = q.read_status(pair.ws)
+        assert rc == q.QUEST_ERR_BAD_LENGTH, path
 
 
-@pytest.mark.parametrize("path", [q.QUEST_PATH_FUSED, q.QUEST_PATH_CHAIN], ids=["fused", "chain"])
+@pytest.mark.parametrize("path", ALL_PATHS, ids=ALL_PATH_IDS)
 def test_step_without_room_or_page_is_reported(path):
     """A decode step whose token has no room (full row) or whose next page is unmapped
     reports it and leaves the length alone, through either path."""
@@ -598,14 +650,15 @@ def test_bad_selection_is_reported():
     assert rc == q.QUEST_ERR_BAD_SELECTION
 
 
-def test_withheld_selection_times_out_and_context_survives():
+@pytest.mark.parametrize("path", [q.QUEST_PATH_FUSED, q.QUEST_PATH_STREAM], ids=["fused", "stream"])
+def test_withheld_selection_times_out_and_context_survives(path):
     """A flag that nothing sets: every decode item's bounded wait runs out (20 ms), the
     call reports QUEST_ERR_TIMEOUT, and the next normal call works."""
     w = small(lens=(3000, 2000), batch=2, budget=256)
     pair = H.on_device(w)
-    o = q.opts(debug_flags=q.QUEST_DEBUG_WITHHOLD_SELECTION, wait_limit_ns=20_000_000)
+    o = q.opts(debug_flags=q.QUEST_DEBUG_WITHHOLD_SELECTION, wait_limit_ns=20_000_000, path=path)
     q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws, o)
     rc, detail = q.read_status(pair.ws)
     assert rc == q.QUEST_ERR_TIMEOUT
     q.workspace_init(pair.ws)
-    H.run_step_and_compare(pair, 0, w.top_k)
+    H.run_step_and_compare(pair, 0, w.top_k, opts=q.opts(path=path))
