@@ -115,7 +115,8 @@ typedef struct quest_opts {
                                  zero it before the call.  Record i is trace[1 + 2i] =
                                  %globaltimer ns, trace[2 + 2i] = smid << 48 | cta << 32 |
                                  event << 24 | item; unused records stay 0.  CTA c owns
-                                 records [64c, 64c + 64).                                   */
+                                 records [64c, 64c + 64) (cluster kernel) or
+                                 [256c, 256c + 256) (stream kernel).                        */
     int32_t cluster_size;     /* fused kernel: CTAs per (sequence, kv head) cluster, 1..16;
                                  0: the largest size up to 8 at which every pair's cluster
                                  is resident at once (1 when there are more pairs than SMs

@@ -383,6 +383,69 @@ def decode_step(cache: PagedCache, q: torch.Tensor, k_new: torch.Tensor, v_new: 
     return out, lse
 
 
+class DecodePlan:
+    """quest_decode / quest_decode_step bound to one cache, top_k, workspace, options, stream
+    and set of output buffers, for a decode loop.  Everything but the step's own tensors is
+    checked once, here; each call then only checks that q (and k_new, v_new) have the shape,
+    dtype and device fixed here and are contiguous, and goes straight to the C entry point
+    (the argument checks of ``decode`` / ``decode_step`` cost the host several microseconds
+    a call).  ``stream``: the stream every call is issued on (default: the current stream at
+    construction).  The outputs (``out``, ``lse``, ``idx_out``, ``count_out``) are
+    overwritten by every call and returned by it."""
+
+    def __init__(self, cache: PagedCache, top_k: int, ws: torch.Tensor,
+                 o: Optional[QuestOpts] = None, out=None, lse=None, want_lse: bool = True,
+                 idx_out: Optional[torch.Tensor] = None,
+                 count_out: Optional[torch.Tensor] = None, stream=None):
+        B, Hq, Hkv = cache.batch, cache.desc.num_q_heads, cache.num_kv_heads
+        self._qshape = torch.Size((B, Hq, HEAD_DIM))
+        self._kvshape = torch.Size((B, Hkv, HEAD_DIM))
+        self._dev = cache.k_pool.get_device()
+        probe = torch.empty(0, dtype=torch.float16, device=cache.k_pool.device)
+        self.out, self.lse = _out(cache, probe, out, lse, want_lse)
+        if idx_out is not None:
+            _need(idx_out, "idx_out", torch.int32, (B, Hkv, top_k))
+        if count_out is not None:
+            _need(count_out, "count_out", torch.int32, (B, Hkv))
+        _need(ws, "ws", torch.uint8)
+        self.idx_out, self.count_out = idx_out, count_out
+        self._keep = (cache, ws, o)  # alive as long as the plan
+        self._lib = load()
+        self._desc = ctypes.byref(cache.desc)
+        # the arguments after q (and k_new, v_new), in C order
+        self._tail = (int(top_k), self.out.data_ptr(), _ptr(self.lse), _ptr(idx_out),
+                      _ptr(count_out), ws.data_ptr(), ws.numel(), _opts_ref(o), _stream(stream))
+
+    def _ok(self, t, shape) -> bool:
+        return (type(t) is torch.Tensor and t.dtype is torch.float16 and t.shape == shape and
+                t.get_device() == self._dev and t.is_contiguous())
+
+    def decode(self, q: torch.Tensor):
+        """quest_decode of this step's queries; returns (out, lse)."""
+        if not self._ok(q, self._qshape):
+            _need(q, "q", torch.float16, self._qshape)
+            raise ValueError("q is on another device than the cache")
+        rc = self._lib.quest_decode(self._desc, q.data_ptr(), *self._tail)
+        if rc:
+            _check(rc)
+        return self.out, self.lse
+
+    def step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor):
+        """quest_decode_step: append (k_new, v_new), then decode q; returns (out, lse)."""
+        if not (self._ok(q, self._qshape) and self._ok(k_new, self._kvshape) and
+                self._ok(v_new, self._kvshape)):
+            _need(q, "q", torch.float16, self._qshape)
+            _need(k_new, "k_new", torch.float16, self._kvshape)
+            _need(v_new, "v_new", torch.float16, self._kvshape)
+            raise ValueError("q / k_new / v_new are on another device than the cache")
+        t = self._tail
+        rc = self._lib.quest_decode_step(self._desc, q.data_ptr(), k_new.data_ptr(),
+                                         v_new.data_ptr(), *t)
+        if rc:
+            _check(rc)
+        return self.out, self.lse
+
+
 def decode_layers(cache: PagedCache, layers: Sequence[PagedCache], q: Sequence[torch.Tensor],
                   top_k: int, ws: torch.Tensor, o: Optional[QuestOpts] = None,
                   k_new: Optional[Sequence[torch.Tensor]] = None,

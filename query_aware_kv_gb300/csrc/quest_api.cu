@@ -7,6 +7,9 @@
 #include <string>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "quest_internal.h"
 
@@ -114,6 +117,7 @@ WsLayout make_layout(const quest_cache_t* c, const Tiling& t) {
   L.ready = off;         off = up256(off + nbg * 4);
   L.decode_arrive = off; off = up256(off + nbg * 4);
   L.seq_done = off;      off = up256(off + (size_t)c->batch * 4);
+  L.skeys = off;         off = up256(off + nbg * c->max_pages * 4);
   L.scores = off;        off = up256(off + nbg * c->max_pages * 4);
   L.sel_idx = off;       off = up256(off + nbg * (size_t)t.topk_cap * 4);
   L.sel_count = off;     off = up256(off + nbg * 4);
@@ -152,6 +156,7 @@ Params make_params(const quest_cache_t* c, void* ws, const WsLayout& L, const Ti
   p.part_ml = reinterpret_cast<float*>(w + L.part_ml);
   p.part_acc = reinterpret_cast<float*>(w + L.part_acc);
   p.sel_pair = reinterpret_cast<int*>(w + L.sel_pair);
+  p.skeys = reinterpret_cast<unsigned*>(w + L.skeys);
   p.started = &h->started;
   p.top_k = t.topk_cap;
   p.score_tile_pages = t.score_tile_pages;
@@ -361,6 +366,35 @@ int quest_sparse_decode(const quest_cache_t* cache, const void* q, const int32_t
                   "quest_sparse_decode");
 }
 
+// The automatic choice between the one-launch cluster kernel and the chain depends only on
+// the device and the shape; it takes occupancy queries, so it is made once per device and
+// shape and remembered.
+static cudaError_t auto_path_fused(int G, int P, int max_pages, int top_k, int nbg,
+                                   bool* fused) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, int, int>, bool> memo;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_tuple(dev, G, P, max_pages, top_k, nbg);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = memo.find(key);
+    if (it != memo.end()) {
+      *fused = it->second;
+      return cudaSuccess;
+    }
+  }
+  bool f = false;
+  if (cluster_any_fits(G, P, max_pages, top_k) &&
+      (e = cluster_preferred(G, P, max_pages, top_k, nbg, &f)) != cudaSuccess)
+    return e;
+  std::lock_guard<std::mutex> lock(mu);
+  memo[key] = f;
+  *fused = f;
+  return cudaSuccess;
+}
+
 // The path of a decode call (QUEST_PATH_FUSED, _CHAIN or _STREAM in quest.h).
 static int decide_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
                        int n_layers, int* path_out) {
@@ -374,22 +408,20 @@ static int decide_path(const quest_cache_t* cache, int32_t top_k, const quest_op
                 path);
   const int G = group_of(cache);
   if (path == QUEST_PATH_STREAM) {
-    if (stream_slots(G, cache->page_size, cache->max_pages, top_k, cache->batch) <= 0)
+    if (stream_slots(G, cache->page_size, cache->max_pages, top_k, cache->batch,
+                     cache->num_q_heads) <= 0)
       return fail(QUEST_ERR_UNSUPPORTED,
                   "the stream kernel does not fit this shape (batch %d, max_pages %d, top_k %d)",
                   cache->batch, cache->max_pages, top_k);
     *path_out = QUEST_PATH_STREAM;
     return QUEST_OK;
   }
-  const bool fits = cluster_any_fits(G, cache->page_size, cache->max_pages, top_k);
   *path_out = path == QUEST_PATH_CHAIN ? QUEST_PATH_CHAIN : QUEST_PATH_FUSED;
   if (path == QUEST_PATH_AUTO && cs == 0 && !(opts && (opts->trace || opts->debug_flags))) {
     bool fused = false;
     const long long nbg = (long long)n_layers * cache->batch * cache->num_kv_heads;
-    const cudaError_t e = fits ? cluster_preferred(G, cache->page_size, cache->max_pages, top_k,
-                                                   (int)std::min<long long>(nbg, 0x7fffffff),
-                                                   &fused)
-                               : cudaSuccess;
+    const cudaError_t e = auto_path_fused(G, cache->page_size, cache->max_pages, top_k,
+                                          (int)std::min<long long>(nbg, 0x7fffffff), &fused);
     if (e != cudaSuccess) return cuda_fail(e, "occupancy of the one-launch kernel");
     *path_out = fused ? QUEST_PATH_FUSED : QUEST_PATH_CHAIN;
   }

@@ -168,9 +168,8 @@ struct CSmem {
   uint32_t* ranges;        // [2][CS][2] key range of each CTA's share
   int* sel;                // [2][kcap] kept pages, ascending
   float* parts;            // [2][CS][G * (128 + 2)] partials M[G], L[G], A[G][128]
-  int* hist;               // [2][kTopkBins], at the start of the ring: rank 0's ring is idle
+  int* hist;               // [kFastBins], at the start of the ring: rank 0's ring is idle
                            // while it selects
-  uint32_t* kept;          // [2][ceil(max_pages / 32)] selection bitmaps
 };
 
 constexpr int kLenCache = 1024;
@@ -199,8 +198,8 @@ __host__ __device__ inline size_t cluster_smem_layout(int G, int P, int max_page
   // streaming region
   size_t a = o;
   const size_t ring = a;     a = align_up(a + (size_t)kStages * 2 * P * kHeadDim * 2, 16);
-  static_assert((size_t)kStages * 2 * 16 * kHeadDim * 2 >= (size_t)2 * kTopkBins * 4,
-                "the ring holds the selection's histograms");
+  static_assert((size_t)kStages * 2 * 16 * kHeadDim * 2 >= (size_t)kFastBins * 4,
+                "the ring holds the selection's histogram");
   const size_t sdesc = a;    a = align_up(a + kStages * sizeof(StageInfo), 16);
   const size_t wsc = a;      a = align_up(a + (size_t)kConsumerWarps * G * P * 4, 16);
   const size_t st = a;       a = align_up(a + (size_t)kConsumerWarps * G * 3 * 4, 16);
@@ -212,7 +211,6 @@ __host__ __device__ inline size_t cluster_smem_layout(int G, int P, int max_page
   const size_t ranges = b;   b = align_up(b + (size_t)2 * S * 2 * 4, 16);
   const size_t sel = b;      b = align_up(b + (size_t)2 * kcap * 4, 16);
   const size_t parts = b;    b = align_up(b + (size_t)2 * S * part_floats * 4, 16);
-  const size_t kept = b;     b = align_up(b + (size_t)2 * ((max_pages + 31) / 32) * 4, 16);
   const size_t total = b;
   if (s) {
     s->full = reinterpret_cast<uint64_t*>(base + full);
@@ -235,7 +233,6 @@ __host__ __device__ inline size_t cluster_smem_layout(int G, int P, int max_page
     s->sel = reinterpret_cast<int*>(base + sel);
     s->parts = reinterpret_cast<float*>(base + parts);
     s->hist = reinterpret_cast<int*>(base + ring);
-    s->kept = reinterpret_cast<uint32_t*>(base + kept);
   }
   return total;
 }
@@ -606,12 +603,13 @@ __device__ void c_select(const Params& p, const CSmem& s, const Role& r, const P
     lo = min(lo, rg[2 * i]);
     hi = max(hi, rg[2 * i + 1]);
   }
-  // the histograms live in the ring, which bulk copies wrote last: clear them first
-  for (int i = tid; i < 2 * kTopkBins / 4; i += kConsumerThreads)
+  // the histogram lives in the ring, which bulk copies wrote last: clear it first
+  for (int i = tid; i < kFastBins / 4; i += kConsumerThreads)
     reinterpret_cast<int4*>(s.hist)[i] = make_int4(0, 0, 0, 0);
   bsync<kConsumerThreads, true>();
-  topk_keys<kConsumerThreads, true>(s.keys + (size_t)q.buf * keys_stride(p.max_pages), q.N,
-                                    q.count, lo, hi, sel, cnt_slot, s.hist, s.kept, s.scratch);
+  topk_fast<kConsumerThreads, true>(s.keys + (size_t)q.buf * keys_stride(p.max_pages), q.N,
+                                    q.count, lo, hi, sel, s.hist, s.scratch);
+  if (tid == 0) *cnt_slot = q.count;
   // the ring goes back to bulk copies (async proxy) after these generic writes
   fence_proxy_async_smem();
 }

@@ -2,7 +2,7 @@
 //
 //   score_tile    : criticality bound of a run of pages for one (sequence, kv head)
 //                   ("Guide to Quest", Solution step 2).
-//   topk_keys     : exact top-K of a row of score keys, ties to the lower page index
+//   topk_fast     : exact top-K of a row of score keys, ties to the lower page index
 //   topk_row        ("Guide to Quest", Solution step 3); topk_row loads the row first.
 //   decode_tile   : flash-decode over a run of kept pages, staged into shared memory by
 //                   1-D bulk copies (TMA) with an mbarrier ring; writes one split-K partial
@@ -148,7 +148,7 @@ __device__ __forceinline__ float2 h2f(uint32_t w) {
 }
 
 // First device fault wins; later ones are dropped.
-__device__ __forceinline__ void report(const Params& p, int code, int b, int page, int site) {
+static __device__ __noinline__ void report(const Params& p, int code, int b, int page, int site) {
   if (atomicCAS(p.status, 0, code) == 0) {
     p.status[1] = b;
     p.status[2] = page;
@@ -178,9 +178,9 @@ __device__ __forceinline__ int load_len_step(const Params& p, int b, int site,
 }
 
 // Bounded wait on an mbarrier phase; false (and a report) once wait_limit_ns has passed.
-__device__ __forceinline__ bool mbar_wait_bounded(const Params& p, uint64_t* bar,
-                                                  uint32_t parity, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The polling loop is out of line: every wait site shares one copy of it.
+static __device__ __noinline__ bool mbar_wait_slow(const Params& p, uint64_t* bar, uint32_t parity,
+                                            int site) {
   const long long t0 = global_ns();
   while (true) {
 #pragma unroll 1
@@ -192,11 +192,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(const Params& p, uint64_t* bar
     }
   }
 }
+__device__ __forceinline__ bool mbar_wait_bounded(const Params& p, uint64_t* bar,
+                                                  uint32_t parity, int site) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(p, bar, parity, site);
+}
 
 // Bounded wait until *flag == target (acquire).  Gives up early once another CTA timed out.
-__device__ __forceinline__ bool wait_flag_bounded(const Params& p, const unsigned* flag,
-                                                  unsigned target, int b, int site) {
-  if (ld_acquire_u32(flag) == target) return true;
+static __device__ __noinline__ bool wait_flag_slow(const Params& p, const unsigned* flag,
+                                            unsigned target, int b, int site) {
   const long long t0 = global_ns();
   while (true) {
     __nanosleep(100);
@@ -207,6 +210,10 @@ __device__ __forceinline__ bool wait_flag_bounded(const Params& p, const unsigne
       return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_flag_bounded(const Params& p, const unsigned* flag,
+                                                  unsigned target, int b, int site) {
+  return ld_acquire_u32(flag) == target || wait_flag_slow(p, flag, target, b, site);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -429,9 +436,9 @@ __device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, fl
 
 // ------------------------------------------------------------------------------------
 // top-K: "Guide to Quest", Solution step 3.  Scores become order-preserving unsigned keys
-// (sign flip), so the K largest scores are the K largest keys; see topk_keys below.
+// (sign flip), so the K largest scores are the K largest keys; see topk_fast below.
 // ------------------------------------------------------------------------------------
-constexpr int kTopkBins = 2048;
+constexpr int kFastBins = 4096;  // histogram bins of one selection level (12-bit digits)
 
 __device__ __forceinline__ uint32_t score_key(float s) {
   const uint32_t u = __float_as_uint(s + 0.0f);  // -0 -> +0
@@ -441,13 +448,11 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 // Shared memory of one selection over a row of up to max_pages scores.
 struct TopkSmem {
   uint32_t* keys;      // [max_pages]
-  int* hist;           // [2 * kTopkBins]
-  uint32_t* kept;      // [2][ceil(max_pages / 32)] bitmaps (kept keys; keys tied at the threshold)
+  int* hist;           // [kFastBins]
 };
 
 __host__ __device__ inline size_t topk_smem_bytes(int max_pages) {
-  return align_up((size_t)max_pages * 4, 16) + (size_t)2 * kTopkBins * 4 +
-         align_up((size_t)2 * ((max_pages + 31) / 32) * 4, 16);
+  return align_up((size_t)max_pages * 4, 16) + (size_t)kFastBins * 4;
 }
 
 __device__ inline TopkSmem topk_smem_at(unsigned char* base, int max_pages) {
@@ -455,8 +460,6 @@ __device__ inline TopkSmem topk_smem_at(unsigned char* base, int max_pages) {
   t.keys = reinterpret_cast<uint32_t*>(base);
   base += align_up((size_t)max_pages * 4, 16);
   t.hist = reinterpret_cast<int*>(base);
-  base += (size_t)2 * kTopkBins * 4;
-  t.kept = reinterpret_cast<uint32_t*>(base);
   return t;
 }
 
@@ -482,140 +485,160 @@ __device__ __forceinline__ int block_excl_sum(int v, int* tot) {
 
 
 // ------------------------------------------------------------------------------------
-// Exact selection over N <= 64 * NT keys in shared memory.  With d = key - lo (lo, hi: the
-// keys' range), the bits of d are resolved 11 at a time from the top, like a radix select
-// whose digits start at the span's leading bit: each level histograms the digit of the
-// keys still tied with the threshold (2048 bins), a block scan finds the bin holding the
-// K-th largest key, and the level ends when that bin is taken whole or d is exhausted
-// (at most 3 levels).  A last pass over the keys (the same loop, in marking mode) sets
-// two bitmaps: keys above the threshold, and keys equal to it (the lowest indices of those
-// are kept); one block scan of the per-thread counts then places the kept indices in
-// ascending order.  Running every
-// level and the marking pass through one loop keeps the code small: this routine runs once
-// per launch and its first pass waits for instruction fetches.
-// hist: 2 * kTopkBins ints, zero on entry (left zero); bits: 2 * ceil(N / 32) words;
-// scratch: 64 ints up to 8 warps, 128 with 16.  Called by threads 0..NT-1.
+// Exact selection of the K largest of N keys in shared memory ("Guide to Quest", Solution
+// step 3; ties to the lower index), the kept indices written in ascending order.  With
+// d = key - lo, the bits of d are resolved 12 at a time from the span's leading bit: each
+// level builds one 4096-bin histogram of the digit of the keys still tied with the
+// threshold, and one block scan from the top bin finds the bin that holds the K-th largest
+// key.  The search ends when that bin is taken whole, when d is exhausted, or when the bin
+// holds at most 32 keys: one warp gathers those and finds the K-th largest value among them
+// by counting.  Every step is a short pass with few barriers; a shared-memory histogram of
+// 4096 bins spreads the keys of a score row thinly, so its atomics rarely collide.
+// hist: kFastBins ints, zero on entry (left zero); scratch: 2 * (NT / 32) + 40 ints.
+// Called by threads 0..NT-1 with K < N < 65536.
 // ------------------------------------------------------------------------------------
-template <int NT, bool kNamed>
-__device__ __forceinline__ void topk_find_bin(const int* hist, int need, int* out3, int* sums) {
-  constexpr int kBPT = kTopkBins / NT;
-  const int tid = threadIdx.x;
-  const int low = kTopkBins - kBPT * (tid + 1);
-  int h[kBPT];
-#pragma unroll
-  for (int q = 0; q < kBPT / 4; ++q) {
-    const int4 v = reinterpret_cast<const int4*>(hist + low)[q];
-    h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
-  }
-  int local = 0;
-#pragma unroll
-  for (int j = 0; j < kBPT; ++j) local += h[j];
-  const int excl = block_excl_sum<NT, kNamed>(local, sums);
-  if (excl < need && need <= excl + local) {
-    int acc = excl;
-#pragma unroll
-    for (int j = kBPT - 1; j >= 0; --j) {
-      if (acc < need && acc + h[j] >= need) {
-        out3[0] = low + j;
-        out3[1] = acc;
-        out3[2] = h[j];
-      }
-      acc += h[j];
-    }
-  }
-  bsync<NT, kNamed>();
-}
+constexpr int kFewKeys = 32;  // a threshold bin this small is resolved by one warp
 
 template <int NT, bool kNamed>
-__device__ void topk_keys(const uint32_t* keys, int N, int K, uint32_t lo, uint32_t hi,
-                          int* idx_out, int* count_out, int* hist, uint32_t* bits,
-                          int* scratch) {
-  static_assert(NT % 32 == 0 && NT <= 512 && kTopkBins % (4 * NT) == 0, "up to 16 whole warps");
-  // scratch: [40, 48) bin search results; per-warp sums of the two alternating bin searches
-  // and of the final placement scan after them (within 64 ints up to 8 warps)
+__device__ void topk_fast(const uint32_t* keys, int N, int K, uint32_t lo, uint32_t hi,
+                          int* idx_out, int* hist, int* scratch) {
   constexpr int NW = NT / 32;
-  constexpr int kSums = NW <= 8 ? 16 : 48;
-  constexpr int kFinal = NW <= 8 ? 32 : 48 + 2 * NW;
-  const int tid = threadIdx.x;
-  const int nw = (N + 31) >> 5;
-  uint32_t* dbits = bits;
-  uint32_t* tbits = bits + nw;
-  for (int i = tid; i < 2 * nw; i += NT) bits[i] = 0u;
-  // level: the keys with (d >> top) == prefix are still tied with the threshold; this
-  // level resolves bits [sh, top) of d (at most 11)
+  constexpr int BPT = (kFastBins + NT - 1) / NT;  // bins per thread in the scan
+  static_assert(NT % 32 == 0 && NT <= 1024, "whole warps");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* found = scratch + 2 * NW;  // [0] bin, [1] keys above it, [2] keys in it, [3] gathered,
+                                  // [4] threshold key, [5] candidates above it
+  uint32_t* cand = reinterpret_cast<uint32_t*>(found + 8);  // [kFewKeys]
   const uint32_t span = hi - lo;
-  int sh = span >= (uint32_t)kTopkBins ? (32 - __clz(span)) - 11 : 0;
-  int top = sh + 11;
-  uint64_t prefix = 0;
-  int need = K;  // keys still to take among the tied ones
-  bool mark = false, whole = false;
-  for (int level = 0;; ++level) {
-    int* h = hist + (level & 1) * kTopkBins;
-#pragma unroll 4
+  int top = span ? 32 - __clz(span) : 0;  // bits of d below `top` are not resolved yet
+  uint32_t pref = 0;                      // d >> top of the keys tied with the threshold
+  int need = K;                           // keys still to take among those tied
+  bool whole = false, first = true;
+  while (top > 0) {
+    const int sh = top > 12 ? top - 12 : 0;
+    const uint32_t mask = (1u << (top - sh)) - 1u;
+#pragma unroll 1
     for (int i = tid; i < N; i += NT) {
-      const uint64_t d = keys[i] - lo;
-      if (!mark) {
-        if ((d >> top) == prefix) atomicAdd(&h[(int)((d >> sh) & (kTopkBins - 1))], 1);
-      } else {
-        // marking pass: above the threshold, or equal to it (only once d is exhausted,
-        // or when the whole threshold bin is taken)
-        const uint64_t v = d >> top;
-        if (v > prefix || (v == prefix && whole))
-          atomicOr(&dbits[i >> 5], 1u << (i & 31));
-        else if (v == prefix)
-          atomicOr(&tbits[i >> 5], 1u << (i & 31));
+      const uint32_t d = keys[i] - lo;
+      if (first || (d >> top) == pref) atomicAdd(&hist[(d >> sh) & mask], 1);
+    }
+    bsync<NT, kNamed>();
+    // thread t holds bins [low, low + BPT), low = kFastBins - (t + 1) * BPT (read, cleared)
+    const int low = kFastBins - (tid + 1) * BPT;
+    int c[BPT];
+    if constexpr (BPT % 4 == 0) {
+#pragma unroll
+      for (int q4 = 0; q4 < BPT / 4; ++q4) {
+        int4* h4 = reinterpret_cast<int4*>(hist + low) + q4;
+        const int4 x = *h4;
+        c[4 * q4] = x.x;
+        c[4 * q4 + 1] = x.y;
+        c[4 * q4 + 2] = x.z;
+        c[4 * q4 + 3] = x.w;
+        *h4 = make_int4(0, 0, 0, 0);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < BPT; ++k) {
+        c[k] = 0;
+        if (low + k >= 0) {
+          c[k] = hist[low + k];
+          hist[low + k] = 0;
+        }
       }
     }
-    if (mark) break;
-    bsync<NT, kNamed>();
-    int* f = scratch + 40 + 4 * (level & 1);
-    topk_find_bin<NT, kNamed>(h, need, f, scratch + kSums + NW * (level & 1));
-    const int bstar = f[0], above = f[1], bucket = f[2];
-    // clear this level's histogram for the level after next (the next one uses the other)
-    for (int i = tid; i < kTopkBins / 4; i += NT) reinterpret_cast<int4*>(h)[i] = make_int4(0, 0, 0, 0);
-    need -= above;
-    prefix = (prefix << (top - sh)) | (uint64_t)bstar;
-    top = sh;
-    whole = bucket == need;
-    if (whole || sh == 0) {
-      mark = true;  // next pass marks the kept keys
-    } else {
-      sh = sh > 11 ? sh - 11 : 0;
+    int tot = 0;
+#pragma unroll
+    for (int k = 0; k < BPT; ++k) tot += c[k];
+    const int excl = block_excl_sum<NT, kNamed>(tot, scratch);
+    if (excl < need && need <= excl + tot) {
+      int acc = excl;
+#pragma unroll
+      for (int k = BPT - 1; k >= 0; --k) {
+        if (acc < need && acc + c[k] >= need) {
+          found[0] = low + k;
+          found[1] = acc;
+          found[2] = c[k];
+        }
+        acc += c[k];
+      }
     }
+    if (tid == 0) found[3] = 0;
+    bsync<NT, kNamed>();
+    // (found[] is next written after the next level's histogram and its barrier)
+    const int bstar = found[0], above = found[1], cnt = found[2];
+    need -= above;
+    pref = (pref << (top - sh)) | (uint32_t)bstar;
+    top = sh;
+    first = false;
+    if (cnt == need) {
+      whole = true;
+      break;
+    }
+    if (top == 0) break;
+    if (cnt <= kFewKeys) {
+#pragma unroll 1
+      for (int i = tid; i < N; i += NT) {
+        const uint32_t v = keys[i];
+        if (((v - lo) >> top) == pref) cand[atomicAdd(&found[3], 1)] = v;
+      }
+      bsync<NT, kNamed>();
+      if (warp == 0) {
+        const uint32_t x = lane < cnt ? cand[lane] : 0u;
+        int gt = 0, eq = 0;
+        for (int q = 0; q < cnt; ++q) {
+          const uint32_t y = __shfl_sync(0xffffffffu, x, q);
+          gt += y > x;
+          eq += y == x;
+        }
+        if (lane < cnt && gt < need && need <= gt + eq) {  // x is the need-th largest value
+          found[4] = (int)x;
+          found[5] = gt;
+        }
+      }
+      bsync<NT, kNamed>();
+      need -= found[5];
+      pref = (uint32_t)found[4] - lo;
+      top = 0;
+      break;
+    }
+  }
+  // kept: (d >> top) > pref; tied: == pref, the `need` lowest indices of them (all if whole).
+  // Thread t takes indices [t*R, t*R + R) (R odd, so that a warp's 32 runs fall in 32
+  // different shared-memory banks): it counts its kept and tied keys, two block scans give
+  // its place in the output and its share of the ties, and a second look at its run writes
+  // them out in ascending order.  Short loops, no unrolling: this runs once per selection
+  // and its code is fetched cold.
+  const int R = ((N + NT - 1) / NT) | 1;
+  const int i0 = min(N, tid * R), i1 = min(N, i0 + R);
+  const uint32_t tsh = top >= 32 ? 31u : (uint32_t)top;  // top < 32 here; keeps the shift defined
+  int nk = 0, nt = 0;
+#pragma unroll 1
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t h = (keys[i] - lo) >> tsh;
+    nk += h > pref;
+    nt += h == pref;
+  }
+  // packed counts: both are below 2^16 (N < 65536)
+  const int pre = block_excl_sum<NT, kNamed>((nk << 16) | nt, scratch);
+  const int tie_before = pre & 0xffff;
+  int take = whole ? nt : max(0, min(nt, need - tie_before));
+  int pos = block_excl_sum<NT, kNamed>(nk + take, scratch + NW);
+#pragma unroll 1
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t h = (keys[i] - lo) >> tsh;
+    bool keep = h > pref;
+    if (h == pref && take > 0) {
+      keep = true;
+      --take;
+    }
+    if (keep) idx_out[pos++] = i;
   }
   bsync<NT, kNamed>();
-  // every thread writes the kept indices of its words, at offsets from one block scan of
-  // the (kept, tied) counts (packed in one int: both are below 2^16)
-  const int wpt = (nw + NT - 1) / NT;
-  const int w0 = min(nw, tid * wpt), w1 = min(nw, w0 + wpt);
-  int nd = 0, nt = 0;
-  for (int w = w0; w < w1; ++w) {
-    nd += __popc(dbits[w]);
-    nt += __popc(tbits[w]);
-  }
-  const int before = block_excl_sum<NT, kNamed>((nd << 16) | nt, scratch + kFinal);
-  int dcnt = before >> 16, tcnt = before & 0xffff;
-  for (int w = w0; w < w1; ++w) {
-    const uint32_t D = dbits[w], T = tbits[w];
-    uint32_t A = D | T;
-    while (A) {
-      const int b = __ffs(A) - 1;
-      A &= A - 1u;
-      const int i = w * 32 + b;
-      if ((D >> b) & 1u) {
-        idx_out[dcnt + min(tcnt, need)] = i;
-        ++dcnt;
-      } else {
-        if (tcnt < need) idx_out[dcnt + tcnt] = i;
-        ++tcnt;
-      }
-    }
-  }
-  if (tid == 0) *count_out = K;
 }
 
 // One row of N scores in global memory (possibly written by another CTA): keys into shared
-// memory with their range, then topk_keys.  N <= 64 * NT.  In a row longer than K, the
+// memory with their range, then topk_fast.  N <= 64 * NT.  In a row longer than K, the
 // first `sink` and last `local` pages get the largest key, so they are always kept.
 template <int NT, bool kNamed>
 __device__ void topk_row(const float* row, int N, int K, int sink, int local, int* idx_out,
@@ -657,7 +680,7 @@ __device__ void topk_row(const float* row, int N, int K, int sink, int local, in
     scratch[warp] = (int)lo;
     scratch[NW + warp] = (int)hi;
   }
-  for (int i = tid; i < 2 * kTopkBins / 4; i += NT)
+  for (int i = tid; i < kFastBins / 4; i += NT)
     reinterpret_cast<int4*>(t.hist)[i] = make_int4(0, 0, 0, 0);
   bsync<NT, kNamed>();
   lo = 0xffffffffu;
@@ -667,7 +690,8 @@ __device__ void topk_row(const float* row, int N, int K, int sink, int local, in
     lo = min(lo, (uint32_t)scratch[w]);
     hi = max(hi, (uint32_t)scratch[NW + w]);
   }
-  topk_keys<NT, kNamed>(t.keys, N, K, lo, hi, idx_out, count_out, t.hist, t.kept, scratch);
+  topk_fast<NT, kNamed>(t.keys, N, K, lo, hi, idx_out, t.hist, scratch);
+  if (tid == 0) *count_out = K;
 }
 
 

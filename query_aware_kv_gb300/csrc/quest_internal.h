@@ -50,6 +50,8 @@ struct Tiling {
 struct WsLayout {
   size_t score_arrive, ready, decode_arrive;  // u32 [B*Hkv] each
   size_t seq_done;                            // u32 [B]
+  size_t skeys;                               // u32 [B*Hkv*max_pages] stream kernel's key
+                                              // rows (0 = not written yet; kept zero)
   size_t scores;                              // f32 [B*Hkv*max_pages]
   size_t sel_idx, sel_count;                  // i32 [B*Hkv*topk_cap], [B*Hkv]
   size_t part_ml, part_acc;                   // f32 [B*Hq*max_splits*2], [..*128]
@@ -96,8 +98,11 @@ struct Params {
                          // sees seq_lens + 1 (when there is room) and the last step of the
                          // call advances seq_lens
   int* sel_pair;         // stream kernel: [B][Hkv][top_k] (logical page, physical page)
+  unsigned* skeys;       // stream kernel: [B][Hkv][max_pages] page keys, 0 until written
   unsigned* started;     // stream kernel: CTAs that have read the lengths
   int hold_lengths;      // stream kernel: append, but leave seq_lens to a later launch
+  int sel_ctas;          // stream kernel: the last sel_ctas CTAs of the grid select and merge
+  int ring_slots;        // stream kernel: stages in each streaming CTA's ring
                          // (every layer but the last of a multi-layer step)
   const __half* k_new;   // fused step: token appended per (b, g) before scoring, or null
   const __half* v_new;
@@ -175,8 +180,8 @@ cudaError_t launch_cluster(const Params& p, const LayerTable& lt, int G, int cs,
 constexpr int kMaxClusterSize = 16;
 // The stream kernel (one persistent launch, every CTA on every pair): ring slots for this
 // shape (0 if it does not fit), its shared memory, and its launch.
-int stream_slots(int G, int P, int max_pages, int top_k, int batch);
-size_t stream_smem_bytes(int G, int P, int max_pages, int top_k, int batch);
+int stream_slots(int G, int P, int max_pages, int top_k, int batch, int hq);
+size_t stream_smem_bytes(int G, int P, int max_pages, int top_k, int batch, int hq);
 cudaError_t launch_stream(const Params& p, const LayerPtrs& lay, int G, int max_ctas,
                           cudaStream_t s);
 constexpr int kStreamPiecePages = 8;  // kept pages per decode piece of the stream kernel

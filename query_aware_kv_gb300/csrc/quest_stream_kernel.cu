@@ -8,25 +8,27 @@
 // bounds before its top-K, its top-K before its pages are read), so a pair alone leaves
 // HBM idle while it selects.  Here every CTA (one per SM) works on every pair:
 //
-//   producer warp (12)     walks this CTA's share of the work in a fixed order and
-//       streams it into a shared-memory ring with 1-D bulk copies (TMA): first its scoring
-//       pieces (the boxes of up to P pages of one pair, "Guide to Quest", Solution
-//       step 1), then its decode pieces (the K and V chunks of up to 8 kept pages of one
-//       pair, once that pair's selection is published).  The query of the pair rides
-//       along in every stage.
-//   consumer warps (4..11) stage s belongs to consumer s mod 8.  Scoring stage: the
+//   producer warp (8)      walks this CTA's share of the work in a fixed order and
+//       streams it into a shared-memory ring: first its scoring pieces (the boxes of up
+//       to P pages of one pair, "Guide to Quest", Solution step 1, one 1-D bulk copy
+//       (TMA) each), then its decode pieces (the K and V chunks of up to 8 kept pages of
+//       one pair, once that pair's selection is published; scattered 4 KB chunks, which
+//       per-lane 16-byte asynchronous copies fetch faster than bulk copies).
+//   consumer warps (0..7)  stage s belongs to consumer s mod 8.  Scoring stage: the
 //       bound of each page (Solution step 2) becomes an order-preserving key in global
-//       memory; the warp then counts the piece on the pair's arrival counter, and the
-//       warp that completes a pair hands its selection to this CTA's selector team.
-//       Decode stage: flash-decode of one kept page (Tang 2024 summary: exact attention
-//       over the Top-K pages); the 8 warps' states of a piece are combined in shared
-//       memory into one split-K partial, and the warp that completes a pair's last piece
-//       hands its merge to the selector team.
-//   selector team (0..3)   runs the jobs handed to it: the exact top-K of a pair's keys
-//       (Solution step 3; ties to the lower page), published with the physical page of
-//       every kept page, or the log-sum-exp merge of a pair's partials into the output.
+//       memory, and the piece is counted on its pair (a release reduction).  Decode
+//       stage: flash-decode of one kept page (Tang 2024 summary: exact attention over the
+//       Top-K pages); the 8 warps' states of a piece are combined in shared memory into
+//       one split-K partial, which is counted on its pair.
+//   selector CTAs          the last few CTAs of the grid stream nothing: each owns every
+//       sel_ctas-th pair and, with 12 warps, takes the exact top-K of a pair's keys as
+//       soon as they are all in (Solution step 3; ties to the lower page), publishes it
+//       with the physical page of every kept page, and, once all of the pair's decode
+//       pieces are in, merges their partials by log-sum-exp into the output.  Selection is
+//       a chain of short dependent steps: on an SM of its own it is not slowed by the
+//       streaming warps.
 //
-// Work is split in global order over all CTAs (piece q goes to CTA q mod gridDim), pairs
+// Work is split in global order over the streaming CTAs (piece q goes to CTA q mod C), pairs
 // in order, so the GPU scores pair 0 first and pair 31 last: pairs complete, and are
 // selected, one after another while the boxes of later pairs still stream, and the
 // decode pieces (taken in the same pair order) find their selection published.  Every
@@ -39,27 +41,29 @@ namespace quest {
 
 namespace {
 
-constexpr int kSelWarps = 4;                       // selector team: warps 0..3
+constexpr int kSelWarps = 12;                      // a selector CTA's team: warps 0..11
 constexpr int kSelThreads = kSelWarps * 32;
-constexpr int kSWarps = kConsumerWarps;            // consumers: warps 4..11
+constexpr int kSWarps = kConsumerWarps;            // a streaming CTA's consumers: warps 0..7
 constexpr int kPiecePages = kStreamPiecePages;     // kept pages per decode piece
 static_assert(kPiecePages == kSWarps, "page i of a decode piece goes to consumer i");
-constexpr int kProducerWarp = kSelWarps + kSWarps;  // warp 12
-constexpr int kStreamThreads = (kProducerWarp + 1) * 32;
-constexpr int kJobs = 64;                          // job queue of the selector team
+constexpr int kProducerWarp = kSWarps;             // warp 8
+constexpr int kStreamThreads = (kSelWarps + 1) * 32;  // both roles launch 13 warps
 constexpr int kStreamMaxBatch = 1024;              // sequences whose lengths are kept on chip
 constexpr int kStreamMaxTopk = 2048;               // kept pages per pair (256 decode pieces)
-constexpr int kStreamTrace = 64;                   // timeline records per CTA
+constexpr int kStreamTrace = 256;                  // timeline records per CTA
+// record slots of a CTA: 0 start; streaming CTA: consumer w [8 + 24w, 32 + 24w), producer
+// [200, 255); selector CTA: [8, 255); 255 exit
+constexpr int kTrProducer = 200, kTrSelector = 8, kTrLast = kStreamTrace - 1;
 
 enum : int { kStEmpty = 0, kStScore = 1, kStDecode = 2 };
-enum : int { kJobSelect = 1, kJobMerge = 2 };
 // control words in shared memory
-enum : int { kCtlComb = 0, kCtlFree = 2, kCtlTail = 4, kCtlDone = 5, kCtlWords = 8 };
+enum : int { kCtlComb = 0, kCtlFree = 2, kCtlWords = 8 };
 
 enum StreamTraceEvent : int {
   kSeStart = 1, kSeExit = 2, kSeFirstScore = 3, kSeLastScore = 4, kSeFirstDecode = 5,
   kSeLastDecode = 6, kSeSelBegin = 7, kSeSelEnd = 8, kSeMergeBegin = 9, kSeMergeEnd = 10,
-  kSeIssueDecode = 11, kSeIssueLast = 12,
+  kSeIssueDecode = 11, kSeIssueLast = 12, kSeStageDone = 13, kSeIssue = 14, kSeSelLoaded = 15,
+  kSeStageLanded = 16, kSeSelTopk = 17, kSeSelWritten = 18, kSeSelFenced = 19,
 };
 
 struct SInfo {
@@ -67,6 +71,8 @@ struct SInfo {
   int j;     // pair
   int a;     // scoring: first page; decode: piece of the pair
   int n;     // scoring: boxes; decode: valid tokens of the page (0: nothing staged)
+  int b, g;  // the pair's sequence and kv head
+  int L, N;  // the sequence's tokens (after this step's append) and pages
 };
 
 struct SSmem {
@@ -76,84 +82,121 @@ struct SSmem {
   SInfo* info;          // [S]
   float* wsc;           // [kSWarps][G * P] logits, then weights, of the page in hand
   float* st;            // [kSWarps][G * 3] running max (log2 units), sum, rescale
-  float* cbuf;          // [2][kSWarps][G * (2 + 128)]: per warp m[G], l[G], acc[G][128]
+  float* cbuf;          // [nb][kSWarps][cbuf_floats(G)]: per warp acc[G][128], m[G], l[G]
   int* ctl;             // [kCtlWords]
-  int* jobs;            // [kJobs]
   int* lens;            // [B] tokens of each sequence in this step (after its append)
   int* sb;              // [B + 1] scoring pieces before sequence b (all its kv heads)
   int* db;              // [B + 1] decode pieces before sequence b
   uint32_t* keys;       // [keys_stride(max_pages)] selector: the pair's keys
-  int* hist;            // [2 * kTopkBins]
-  uint32_t* kept;       // [2 * ceil(max_pages / 32)]
+  int* hist;            // [kFastBins] selection histogram (zero between uses)
   int* scratch;         // [256]
   int* sel;             // [kcap] kept pages, ascending
   float* msc;           // [G][npc_max + 2] merge: scale of each partial, max, sum
+  int nb;               // combine buffers (decode piece k uses buffer k mod nb)
+  __half* qall;         // [B][Hq][128] every query, or null (each stage carries its own)
+  uint64_t* qbar;       // completes when qall has landed
 };
 
 __host__ __device__ inline int s_keys_stride(int max_pages) { return (max_pages + 3) & ~3; }
 
-__host__ __device__ inline size_t s_slot_bytes(int G, int P) {
-  return align_up((size_t)2 * P * kHeadDim * 2 + (size_t)G * kHeadDim * 2, 128);
+// Floats of one warp's state in the combine buffer: acc[G][128], then m[G] and l[G], padded
+// to whole 16-byte units so that every warp's acc starts on 16 bytes (float4 accesses).
+__host__ __device__ constexpr int cbuf_floats(int G) { return G * kHeadDim + ((2 * G + 3) & ~3); }
+
+// The queries of every pair (B * Hq * 256 bytes) are staged in shared memory once when they
+// fit in kQAllBytes; otherwise every stage carries its pair's query after its data.
+constexpr size_t kQAllBytes = 32 << 10;
+__host__ __device__ inline bool q_all(int batch, int hq) {
+  return (size_t)batch * hq * kHeadDim * 2 <= kQAllBytes;
+}
+__host__ __device__ inline size_t s_slot_bytes(int G, int P, bool qall) {
+  return align_up((size_t)2 * P * kHeadDim * 2 + (qall ? 0 : (size_t)G * kHeadDim * 2), 128);
 }
 
-// Everything but the ring, then as many ring slots as fit in `budget` bytes (0 if fewer
-// than kSWarps fit).  Writes the layout into s when given.
-__host__ __device__ inline size_t stream_smem_layout(int G, int P, int max_pages, int top_k,
-                                                     int batch, size_t budget, int* slots,
-                                                     SSmem* s, unsigned char* base) {
+// Bytes a selector CTA keeps in shared memory (in the space a streaming CTA gives its ring).
+__host__ __device__ inline size_t selector_bytes(int G, int max_pages, int kcap) {
+  const int npc = (kcap + kPiecePages - 1) / kPiecePages;
+  return align_up((size_t)s_keys_stride(max_pages) * 4, 16) + (size_t)kFastBins * 4 +
+         256 * 4 + align_up((size_t)kcap * 4, 16) + align_up((size_t)G * (npc + 2) * 4, 16);
+}
+
+// The fixed part, the ring barriers and descriptors, then one region that is the ring in a
+// streaming CTA and the selection buffers in a selector CTA; as many ring slots as fit in
+// `budget` bytes (a multiple of kSWarps; 0 if the shape does not fit).  Writes the layout
+// into s when given.
+__host__ __device__ inline size_t stream_smem_layout_nb(int G, int P, int max_pages, int top_k,
+                                                        int batch, int hq, size_t budget,
+                                                        int max_slots, int nb, int* slots, SSmem* s,
+                                                        unsigned char* base) {
   const int kcap = top_k < max_pages ? top_k : max_pages;
+  const bool qall = q_all(batch, hq);
   const int npc = (kcap + kPiecePages - 1) / kPiecePages;
   size_t o = 0;
   const size_t wsc = o;      o = align_up(o + (size_t)kSWarps * G * P * 4, 16);
   const size_t st = o;       o = align_up(o + (size_t)kSWarps * G * 3 * 4, 16);
-  const size_t cbuf = o;     o = align_up(o + (size_t)2 * kSWarps * G * (2 + kHeadDim) * 4, 16);
+  const size_t cbuf = o;     o = align_up(o + (size_t)nb * kSWarps * cbuf_floats(G) * 4, 16);
   const size_t ctl = o;      o = align_up(o + kCtlWords * 4, 16);
-  const size_t jobs = o;     o = align_up(o + kJobs * 4, 16);
   const size_t lens = o;     o = align_up(o + (size_t)batch * 4, 16);
   const size_t sb = o;       o = align_up(o + (size_t)(batch + 1) * 4, 16);
   const size_t db = o;       o = align_up(o + (size_t)(batch + 1) * 4, 16);
-  const size_t keys = o;     o = align_up(o + (size_t)s_keys_stride(max_pages) * 4, 16);
-  const size_t hist = o;     o = align_up(o + (size_t)2 * kTopkBins * 4, 16);
-  const size_t kept = o;     o = align_up(o + (size_t)2 * ((max_pages + 31) / 32) * 4, 16);
-  const size_t scr = o;      o = align_up(o + 256 * 4, 16);
-  const size_t sel = o;      o = align_up(o + (size_t)kcap * 4, 16);
-  const size_t msc = o;      o = align_up(o + (size_t)G * (npc + 2) * 4, 128);
+  const size_t qa = o;       o = align_up(o + (qall ? (size_t)batch * hq * kHeadDim * 2 : 0), 128);
+  const size_t qbar = o;     o += 16;
   const size_t fixed = o;
-  const size_t per_slot = s_slot_bytes(G, P) + 2 * 8 + sizeof(SInfo);
+  const size_t per_slot = s_slot_bytes(G, P, qall) + 2 * 8 + sizeof(SInfo);
   // a multiple of kSWarps: stage s sits in slot s mod S and belongs to consumer s mod 8, so
   // every slot keeps one consumer, which waits on its phases in order (a parity wait that
   // ran two phases ahead of the slot would be satisfied by the wrong phase)
   int S = 0;
-  if (budget > fixed + 256) S = (int)((budget - fixed - 256) / per_slot);
-  if (S > 64) S = 64;
+  if (budget > fixed + 512) S = (int)((budget - fixed - 512) / per_slot);
+  if (S > max_slots) S = max_slots;
   S -= S % kSWarps;
+  const size_t bars = fixed;
+  size_t e = bars + (size_t)S * 16;
+  const size_t infoo = e;    e = align_up(e + (size_t)S * sizeof(SInfo), 128);
+  const size_t region = e;
+  const size_t ring_bytes = (size_t)S * s_slot_bytes(G, P, qall);
+  const size_t sel_bytes = selector_bytes(G, max_pages, kcap);
+  e = region + (ring_bytes > sel_bytes ? ring_bytes : sel_bytes);
+  if (e > budget) S = 0;
   if (slots) *slots = S;
-  const size_t ring = align_up(fixed, 128);
-  size_t e = ring + (size_t)S * s_slot_bytes(G, P);
-  const size_t full = e;     e += (size_t)S * 8;
-  const size_t empty = e;    e += (size_t)S * 8;
-  const size_t infoo = e;    e = align_up(e + (size_t)S * sizeof(SInfo), 16);
   if (s) {
-    s->ring = base + ring;
-    s->full = reinterpret_cast<uint64_t*>(base + full);
-    s->empty = reinterpret_cast<uint64_t*>(base + empty);
+    s->ring = base + region;
+    s->full = reinterpret_cast<uint64_t*>(base + bars);
+    s->empty = s->full + S;
     s->info = reinterpret_cast<SInfo*>(base + infoo);
     s->wsc = reinterpret_cast<float*>(base + wsc);
     s->st = reinterpret_cast<float*>(base + st);
     s->cbuf = reinterpret_cast<float*>(base + cbuf);
     s->ctl = reinterpret_cast<int*>(base + ctl);
-    s->jobs = reinterpret_cast<int*>(base + jobs);
     s->lens = reinterpret_cast<int*>(base + lens);
     s->sb = reinterpret_cast<int*>(base + sb);
     s->db = reinterpret_cast<int*>(base + db);
-    s->keys = reinterpret_cast<uint32_t*>(base + keys);
-    s->hist = reinterpret_cast<int*>(base + hist);
-    s->kept = reinterpret_cast<uint32_t*>(base + kept);
-    s->scratch = reinterpret_cast<int*>(base + scr);
-    s->sel = reinterpret_cast<int*>(base + sel);
-    s->msc = reinterpret_cast<float*>(base + msc);
+    size_t r = region;
+    s->keys = reinterpret_cast<uint32_t*>(base + r);  r += align_up((size_t)s_keys_stride(max_pages) * 4, 16);
+    s->hist = reinterpret_cast<int*>(base + r);       r += (size_t)kFastBins * 4;
+    s->scratch = reinterpret_cast<int*>(base + r);    r += 256 * 4;
+    s->sel = reinterpret_cast<int*>(base + r);        r += align_up((size_t)kcap * 4, 16);
+    s->msc = reinterpret_cast<float*>(base + r);
+    (void)npc;
+    s->nb = nb;
+    s->qall = qall ? reinterpret_cast<__half*>(base + qa) : nullptr;
+    s->qbar = reinterpret_cast<uint64_t*>(base + qbar);
   }
   return e;
+}
+
+// The layout with two combine buffers (a piece's warps need not wait for the previous
+// piece's combine) if the ring still gets kSWarps slots, else with one.
+__host__ __device__ inline size_t stream_smem_layout(int G, int P, int max_pages, int top_k,
+                                                     int batch, int hq, size_t budget,
+                                                     int max_slots, int* slots, SSmem* s,
+                                                     unsigned char* base) {
+  int S = 0;
+  stream_smem_layout_nb(G, P, max_pages, top_k, batch, hq, budget, max_slots, 2, &S, nullptr,
+                        nullptr);
+  const int nb = S >= kSWarps ? 2 : 1;
+  return stream_smem_layout_nb(G, P, max_pages, top_k, batch, hq, budget, max_slots, nb, slots,
+                               s, base);
 }
 
 // ---------------------------------------------------------------- geometry of one call
@@ -172,6 +215,19 @@ __device__ __forceinline__ PairGeo pair_geo(const Params& p, const SSmem& s, int
   q.K = min(p.top_k, q.N);
   q.npc = (q.N + p.P - 1) / p.P;  // a scoring piece holds the boxes of P pages
   q.ndc = (q.K + kPiecePages - 1) / kPiecePages;
+  return q;
+}
+
+// The geometry a consumer needs, from its stage's descriptor (no division).
+__device__ __forceinline__ PairGeo geo_of(const Params& p, const SInfo& in) {
+  PairGeo q;
+  q.b = in.b;
+  q.g = in.g;
+  q.L = in.L;
+  q.N = in.N;
+  q.K = min(p.top_k, in.N);
+  q.npc = 0;
+  q.ndc = 0;
   return q;
 }
 
@@ -197,8 +253,8 @@ __device__ __forceinline__ void piece_of(const Params& p, const int* pre, int r,
   *j = b * p.Hkv + g;
 }
 
-__device__ __forceinline__ void strace(const Params& p, int* slot, int ev, int item) {
-  if (p.trace == nullptr || *slot >= kStreamTrace) return;
+// A timeline record (out of line: it is off the hot path unless a trace was asked for).
+__device__ __noinline__ void strace_rec(const Params& p, int* slot, int ev, int item) {
   const long long i = (long long)blockIdx.x * kStreamTrace + (*slot)++;
   if (i >= p.trace_capacity) return;
   unsigned smid;
@@ -208,185 +264,262 @@ __device__ __forceinline__ void strace(const Params& p, int* slot, int ev, int i
                        ((unsigned long long)(blockIdx.x & 0xffff) << 32) |
                        ((unsigned long long)(ev & 0xff) << 24) | (unsigned)(item & 0xffffff);
 }
-
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
+__device__ __forceinline__ void strace(const Params& p, int* slot, int limit, int ev, int item) {
+  if (p.trace != nullptr && *slot < limit) strace_rec(p, slot, ev, item);
 }
+
 __device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
+// 16-byte copy global -> shared through the load path (L2 only).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+// An arrival on `bar` once this thread's earlier cp.async copies have landed; the pending
+// count is raised by one now, so the phase cannot complete before that arrival.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ int ld_volatile_s32(const int* p) {
   return *reinterpret_cast<const volatile int*>(p);
 }
 
-// Hand a job to this CTA's selector team (one lane).
-__device__ void push_job(const Params& p, const SSmem& s, int kind, int j) {
-  const int slot = atomicAdd(&s.ctl[kCtlTail], 1) % kJobs;
-  // the slot's previous job (kJobs pushes ago) must have been taken
-  if (ld_volatile_s32(&s.jobs[slot]) != 0) {
-    const long long t0 = global_ns();
-    while (ld_volatile_s32(&s.jobs[slot]) != 0) {
-      __nanosleep(64);
-      if (global_ns() - t0 > p.wait_limit_ns) {
-        report(p, QUEST_ERR_TIMEOUT, -1, j, kSiteWaitSlot);
-        return;
-      }
-    }
-  }
-  __threadfence_block();
-  atomicExch(&s.jobs[slot], (kind << 28) | (j + 1));
+// True in every thread of the selector team if `pred` holds in any of them (named barrier 1).
+template <int NT>
+__device__ __forceinline__ bool bany(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, %2, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(NT)
+      : "memory");
+  return r != 0;
 }
 
 // ---------------------------------------------------------------- producer warp
+// The ring position of stage `stage`: slot and phase parity, advanced without a division.
+struct RingPos {
+  int slot;
+  uint32_t phase;
+  __device__ __forceinline__ void step(int by, int S) {
+    slot += by;
+    if (slot >= S) {
+      slot -= S;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Stages are issued in order, one lane at a time; each lane first works out, in parallel
+// with the others, where its stage's data comes from (the mapping of pieces to pairs takes
+// integer divisions: done serially they would make the producer the bottleneck).
 template <int G, int P>
-__device__ void s_produce(const Params& p, const LayerPtrs& lay, const SSmem& s, int S,
-                          int TS, int TD, int nS_pad) {
+__device__ void s_produce(const Params& p, const LayerPtrs& lay, const SSmem& s, int S, int C,
+                          int TS, int TD, int nS, int nS_pad) {
   constexpr uint32_t kChunk = (uint32_t)P * kHeadDim * 2;  // one page of K (or V), one kv head
   constexpr uint32_t kBox = 2 * kHeadDim * 2;              // one page's box (min, max)
-  constexpr uint32_t kQ = (uint32_t)G * kHeadDim * 2;
-  const size_t slot_bytes = s_slot_bytes(G, P);
+  const bool qall = s.qall != nullptr;
+  const uint32_t kQ = qall ? 0u : (uint32_t)G * kHeadDim * 2;
+  const size_t slot_bytes = s_slot_bytes(G, P, qall);
   const int lane = threadIdx.x & 31;
-  const int C = (int)gridDim.x, c = (int)blockIdx.x;
-  int tslot = kStreamTrace / 2;
-  uint32_t stage = 0;
-  auto slot_free = [&](uint32_t st_idx) -> bool {
-    const int sl = (int)(st_idx % (uint32_t)S);
-    return mbar_wait_bounded(p, &s.empty[sl], ((st_idx / (uint32_t)S) & 1u) ^ 1u, kSiteWaitSlot);
-  };
-  // ---- scoring pieces: the boxes of up to P pages of one pair (P boxes fill one stage)
-  if (lane == 0) {
-    for (int r = c; r < TS; r += C, ++stage) {
-      int j, u;
-      piece_of(p, s.sb, r, &j, &u);
-      const PairGeo q = pair_geo(p, s, j);
-      const int p0 = u * P;
-      const int n = min(P, q.N - p0);
-      const int sl = (int)(stage % (uint32_t)S);
-      const bool ok = slot_free(stage);
-      s.info[sl] = SInfo{kStScore, j, p0, ok ? n : 0};
-      if (ok) {
-        unsigned char* dst = s.ring + (size_t)sl * slot_bytes;
-        mbar_arrive_expect_tx(&s.full[sl], (uint32_t)n * kBox + kQ);
-        bulk_g2s(dst, lay.meta + box_offset(p, q.b, q.g, p0), (uint32_t)n * kBox, &s.full[sl]);
-        bulk_g2s(dst + 2 * kChunk, lay.q + ((size_t)q.b * p.Hq + (size_t)q.g * G) * kHeadDim, kQ,
-                 &s.full[sl]);
-      } else {
-        mbar_arrive(&s.full[sl]);
-      }
-    }
-    for (; stage < (uint32_t)nS_pad; ++stage) {  // round up to whole rounds of kSWarps
-      const int sl = (int)(stage % (uint32_t)S);
-      const bool ok = slot_free(stage);
-      s.info[sl] = SInfo{kStEmpty, 0, 0, 0};
-      (void)ok;
-      mbar_arrive(&s.full[sl]);
-    }
-    if (TS > c) strace(p, &tslot, kSeIssueLast, 0);
+  const int c = (int)blockIdx.x;
+  int tslot = kTrProducer;
+  RingPos pos{0, 0u};
+  if (qall && lane == 0) {  // every query of the call, once
+    const uint32_t qb = (uint32_t)((size_t)p.B * p.Hq * kHeadDim * 2);
+    mbar_arrive_expect_tx(s.qbar, qb);
+    bulk_g2s(s.qall, lay.q, qb, s.qbar);
   }
-  stage = __shfl_sync(0xffffffffu, stage, 0);
-  // ---- decode pieces: up to 8 kept pages of one pair, page i to consumer i
-  bool first = true;
-  for (int r = c; r < TD; r += C) {
-    int j, v;
-    piece_of(p, s.db, r, &j, &v);
-    const PairGeo q = pair_geo(p, s, j);
-    const int n = min(kPiecePages, q.K - v * kPiecePages);
-    bool ok = true;
-    if (lane == 0) ok = wait_flag_bounded(p, p.ready + j, 1u, q.b, kSiteWaitSelection);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (ok) (void)ld_acquire_u32(p.ready + j);  // every lane acquires the selection
-    if (first && lane == 0) strace(p, &tslot, kSeIssueDecode, j);
-    first = false;
-    // the selection's kept pages (written with their physical page by the selector); the
-    // appended token's row was written by a generic store: order it before the bulk copy
-    fence_proxy_async_global();
-    int nv = 0;
-    const __half* ksrc = nullptr;
-    const __half* vsrc = nullptr;
-    if (ok && lane < n) {
-      const int2 e = __ldcg(reinterpret_cast<const int2*>(p.sel_pair) +
-                            (size_t)j * p.top_k + v * kPiecePages + lane);
-      if (e.x >= 0 && e.x < q.N && e.y >= 0 && e.y < p.num_phys) {
-        nv = min(P, q.L - e.x * P);
-        const size_t off = ((size_t)e.y * p.Hkv + q.g) * (size_t)P * kHeadDim;
-        ksrc = lay.k_pool + off;
-        vsrc = lay.v_pool + off;
-      }
+  // ---- scoring pieces (the boxes of up to P pages of one pair fill one stage), then
+  // empty stages up to a whole round of kSWarps
+  for (int k0 = 0; k0 < nS_pad; k0 += 32) {
+    const int k = k0 + lane;
+    int j = 0, p0 = 0, n = 0;
+    PairGeo q{};
+    const __half* box = nullptr;
+    const __half* qsrc = nullptr;
+    if (k < nS) {
+      int u;
+      piece_of(p, s.sb, c + k * C, &j, &u);
+      q = pair_geo(p, s, j);
+      p0 = u * P;
+      n = min(P, q.N - p0);
+      box = lay.meta + box_offset(p, q.b, q.g, p0);
+      qsrc = lay.q + ((size_t)q.b * p.Hq + (size_t)q.g * G) * kHeadDim;
     }
-    for (int i = 0; i < kPiecePages; ++i) {
+    const int cnt = min(32, nS_pad - k0);
+#pragma unroll 1
+    for (int i = 0; i < cnt; ++i) {
       if (lane == i) {
-        const int sl = (int)(stage % (uint32_t)S);
-        const bool fr = slot_free(stage);
-        const int nvs = fr ? nv : 0;
-        s.info[sl] = SInfo{kStDecode, j, v, nvs};
-        if (nvs > 0) {
-          unsigned char* dst = s.ring + (size_t)sl * slot_bytes;
-          mbar_arrive_expect_tx(&s.full[sl], 2 * kChunk + kQ);
-          bulk_g2s(dst, ksrc, kChunk, &s.full[sl]);
-          bulk_g2s(dst + kChunk, vsrc, kChunk, &s.full[sl]);
-          bulk_g2s(dst + 2 * kChunk, lay.q + ((size_t)q.b * p.Hq + (size_t)q.g * G) * kHeadDim,
-                   kQ, &s.full[sl]);
+        const bool ok = mbar_wait_bounded(p, &s.empty[pos.slot], pos.phase ^ 1u, kSiteWaitSlot);
+        uint64_t* bar = &s.full[pos.slot];
+        strace(p, &tslot, kTrLast - 2, kSeIssue, k);
+        if (k < nS) {
+          s.info[pos.slot] = SInfo{kStScore, j, p0, ok ? n : 0, q.b, q.g, q.L, q.N};
+          if (ok) {
+            unsigned char* dst = s.ring + (size_t)pos.slot * slot_bytes;
+            mbar_arrive_expect_tx(bar, (uint32_t)n * kBox + kQ);
+            bulk_g2s(dst, box, (uint32_t)n * kBox, bar);
+            if (!qall) bulk_g2s(dst + 2 * kChunk, qsrc, kQ, bar);
+          } else {
+            mbar_arrive(bar);
+          }
         } else {
-          mbar_arrive(&s.full[sl]);
+          s.info[pos.slot] = SInfo{kStEmpty, 0, 0, 0, 0, 0, 0, 0};
+          mbar_arrive(bar);
         }
       }
-      ++stage;
+      pos.step(1, S);
       __syncwarp();
     }
   }
-  if (TD > c && lane == 0) strace(p, &tslot, kSeIssueLast, 1);
+  if (lane == 0 && TS > c) strace(p, &tslot, kTrLast, kSeIssueLast, 0);
+  // ---- decode pieces: up to 8 kept pages of one pair, page i to consumer i.  Lane l
+  // works out piece k0 + l's pair; the kept pages of the next piece are fetched while the
+  // current piece's copies are being issued, when its selection is already out.  A page's
+  // K and V chunks are scattered over the pool: the whole warp copies them, 16 bytes a lane
+  // per instruction, and the stage completes on its full barrier through the copies' own
+  // arrivals (each lane's, plus one plain arrival of lane 0).
+  bool first = true;
+  const int nD = c < TD ? (TD - 1 - c) / C + 1 : 0;
+  int2 e_next = make_int2(-1, -1);
+  bool have_next = false;
+  for (int k0 = 0; k0 < nD; k0 += 32) {
+    int dj = 0, dv = 0;
+    if (k0 + lane < nD) piece_of(p, s.db, c + (k0 + lane) * C, &dj, &dv);
+    const int cnt = min(32, nD - k0);
+#pragma unroll 1
+    for (int i = 0; i < cnt; ++i) {
+      const int j = __shfl_sync(0xffffffffu, dj, i), v = __shfl_sync(0xffffffffu, dv, i);
+      const PairGeo q = pair_geo(p, s, j);
+      const int n = min(kPiecePages, q.K - v * kPiecePages);
+      bool ok = true;
+      int2 e = make_int2(-1, -1);
+      if (have_next) {
+        e = e_next;
+      } else {
+        if (lane == 0) ok = wait_flag_bounded(p, p.ready + j, 1u, q.b, kSiteWaitSelection);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (ok) {
+          (void)ld_acquire_u32(p.ready + j);  // every lane acquires the selection
+          if (lane < n)
+            e = __ldcg(reinterpret_cast<const int2*>(p.sel_pair) + (size_t)j * p.top_k +
+                       v * kPiecePages + lane);
+        }
+      }
+      if (first && lane == 0) strace(p, &tslot, kTrLast, kSeIssueDecode, j);
+      first = false;
+      int nv = 0, ph = 0;
+      if (ok && lane < n && e.x >= 0 && e.x < q.N && e.y >= 0 && e.y < p.num_phys) {
+        nv = min(P, q.L - e.x * P);
+        ph = e.y;
+      }
+      // the next piece's kept pages, if its pair is already selected
+      have_next = false;
+      if (i + 1 < cnt || k0 + 32 < nD) {  // warp-uniform
+        int jn, vn;
+        if (i + 1 < cnt) {
+          jn = __shfl_sync(0xffffffffu, dj, i + 1);
+          vn = __shfl_sync(0xffffffffu, dv, i + 1);
+        } else {
+          int a = 0, b2 = 0;
+          if (lane == 0) piece_of(p, s.db, c + (k0 + 32) * C, &a, &b2);
+          jn = __shfl_sync(0xffffffffu, a, 0);
+          vn = __shfl_sync(0xffffffffu, b2, 0);
+        }
+        int rdy = 0;
+        if (lane == 0) rdy = ld_acquire_u32(p.ready + jn) == 1u;
+        rdy = __shfl_sync(0xffffffffu, rdy, 0);
+        if (rdy) {
+          const PairGeo qn = pair_geo(p, s, jn);
+          const int nn = min(kPiecePages, qn.K - vn * kPiecePages);
+          (void)ld_acquire_u32(p.ready + jn);  // every lane acquires the selection
+          if (lane < nn)
+            e_next = __ldcg(reinterpret_cast<const int2*>(p.sel_pair) + (size_t)jn * p.top_k +
+                            vn * kPiecePages + lane);
+          have_next = true;
+        }
+      }
+      const unsigned char* qsrc = reinterpret_cast<const unsigned char*>(
+          lay.q + ((size_t)q.b * p.Hq + (size_t)q.g * G) * kHeadDim);
+#pragma unroll 1
+      for (int t = 0; t < kPiecePages; ++t) {
+        const int nvt = __shfl_sync(0xffffffffu, nv, t);
+        const int pht = __shfl_sync(0xffffffffu, ph, t);
+        int fr = 1;
+        if (lane == 0) fr = mbar_wait_bounded(p, &s.empty[pos.slot], pos.phase ^ 1u, kSiteWaitSlot);
+        fr = __shfl_sync(0xffffffffu, fr, 0);
+        __syncwarp();  // the slot's last reads happen before any lane's copy into it
+        const int nvs = fr ? nvt : 0;
+        uint64_t* bar = &s.full[pos.slot];
+        if (lane == 0) s.info[pos.slot] = SInfo{kStDecode, j, v, nvs, q.b, q.g, q.L, q.N};
+        if (nvs > 0) {  // warp-uniform
+          unsigned char* dst = s.ring + (size_t)pos.slot * slot_bytes + 16 * lane;
+          const size_t off = (((size_t)pht * p.Hkv + q.g) * (size_t)P * kHeadDim) * 2 + 16 * lane;
+          const unsigned char* ks = reinterpret_cast<const unsigned char*>(lay.k_pool) + off;
+          const unsigned char* vs = reinterpret_cast<const unsigned char*>(lay.v_pool) + off;
+#pragma unroll
+          for (int u = 0; u < (int)kChunk / 512; ++u) cp_async16(dst + 512 * u, ks + 512 * u);
+#pragma unroll
+          for (int u = 0; u < (int)kChunk / 512; ++u)
+            cp_async16(dst + kChunk + 512 * u, vs + 512 * u);
+          if (!qall)  // the pair's G query rows, 16 G units of 16 bytes
+            for (int u = lane; u < (int)kQ / 16; u += 32)
+              cp_async16(dst - 16 * lane + 2 * kChunk + 16 * u, qsrc + 16 * u);
+          cp_async_arrive(bar);
+          __syncwarp();  // every lane's pending arrival is counted before lane 0's
+        }
+        if (lane == 0) mbar_arrive(bar);
+        pos.step(1, S);
+        __syncwarp();
+      }
+    }
+  }
+  if (TD > c && lane == 0) strace(p, &tslot, kTrLast, kSeIssueLast, 1);
 }
 
 // ---------------------------------------------------------------- consumer warps
-// Bound of every page of a scoring stage (half-warp per page); the keys go to global
-// memory.  The page of the step's new token first takes the token: its box opens or widens
-// in registers, is scored, and is written back with the token's K and V rows.
+// The query heads of a stage's pair: in the shared copy of every query, or after the data.
 template <int G, int P>
-__device__ void s_score_stage(const Params& p, const LayerPtrs& lay, const SSmem& s,
-                              const unsigned char* slot, const SInfo& in, const PairGeo& q) {
+__device__ __forceinline__ const __half* stage_q(const Params& p, const SSmem& s,
+                                                 const unsigned char* slot, const PairGeo& q) {
+  if (s.qall) return s.qall + ((size_t)q.b * p.Hq + (size_t)q.g * G) * kHeadDim;
+  return reinterpret_cast<const __half*>(slot + 2 * (size_t)P * kHeadDim * 2);
+}
+
+// Bound of every page of a scoring stage (half-warp per page); the keys go to the pair's
+// key row in global memory, where the pair's selector polls for them (a written key is
+// never 0).  The page of the step's new token first takes the token: its box opens or
+// widens (in the staged copy too), is written back with the token's K and V rows, and those
+// writes are made visible before any key of the stage (the selection that follows releases
+// the page to the decode pieces, which read the rows).  Returns true (in the whole warp) if
+// the stage wrote into its slot.
+template <int G, int P>
+__device__ bool s_score_stage(const Params& p, const LayerPtrs& lay, const SSmem& s,
+                              unsigned char* slot, const SInfo& in, const PairGeo& q) {
   const int lane = threadIdx.x & 31;
   const int hw = lane >> 4, c = lane & 15;
   QueryFrag<G> f;
-  load_query_frag<G>(reinterpret_cast<const __half*>(slot + 2 * (size_t)P * kHeadDim * 2), 0, 0,
-                     0, c, f);
-  // the appended token (tokens L-1 of a step that appends)
-  const bool appends = lay.k_new != nullptr && p.chain_append;  // set per call on the host
-  const int ap = appends && q.L > 0 ? (q.L - 1) / P : -1;
-  const bool mine = ap >= in.a && ap < in.a + in.n;
-  uint4 knew = make_uint4(0, 0, 0, 0), vnew = make_uint4(0, 0, 0, 0);
-  int aphys = -1;
-  if (mine) {
-    const size_t o = ((size_t)q.b * p.Hkv + q.g) * kHeadDim + 8 * c;
-    knew = *reinterpret_cast<const uint4*>(lay.k_new + o);
-    vnew = *reinterpret_cast<const uint4*>(lay.v_new + o);
-    const int ph = p.block_table[(size_t)q.b * p.max_pages + ap];
-    aphys = (ph >= 0 && ph < p.num_phys) ? ph : -1;
-  }
-  uint32_t* krow = reinterpret_cast<uint32_t*>(p.scores) + (size_t)(q.b * p.Hkv + q.g) * p.max_pages;
-  const bool windowed = q.N > q.K && (p.sink_pages > 0 || p.local_pages > 0);
-  for (int r0 = 0; r0 < in.n; r0 += 2) {
-    const int r = r0 + hw;
-    const int page = in.a + r;
-    uint4 mn = make_uint4(0, 0, 0, 0), mx = make_uint4(0, 0, 0, 0);
-    if (r < in.n) {
-      const unsigned char* rec = slot + (size_t)r * 2 * kHeadDim * 2;
-      mn = *reinterpret_cast<const uint4*>(rec + 16 * c);
-      mx = *reinterpret_cast<const uint4*>(rec + 2 * kHeadDim + 16 * c);
-    }
-    if (mine && r < in.n && page == ap) {
-      if (aphys >= 0) {
+  load_query_frag<G>(stage_q<G, P>(p, s, slot, q), 0, 0, 0, c, f);
+  const int ap = (lay.k_new != nullptr && p.chain_append && q.L > 0) ? (q.L - 1) / P : -1;
+  const bool takes_token = ap >= in.a && ap < in.a + in.n;  // warp-uniform
+  if (takes_token) {
+    if (hw == 0) {
+      const int ph = p.block_table[(size_t)q.b * p.max_pages + ap];
+      if (ph >= 0 && ph < p.num_phys) {
+        const size_t o = ((size_t)q.b * p.Hkv + q.g) * kHeadDim + 8 * c;
+        const uint4 knew = *reinterpret_cast<const uint4*>(lay.k_new + o);
+        const uint4 vnew = *reinterpret_cast<const uint4*>(lay.v_new + o);
         const int slot_a = (q.L - 1) % P;
-        if (slot_a == 0) {
-          mn = knew;
-          mx = knew;
-        } else {
-          const uint32_t a[4] = {mn.x, mn.y, mn.z, mn.w};
-          const uint32_t z[4] = {mx.x, mx.y, mx.z, mx.w};
+        unsigned char* rec = slot + (size_t)(ap - in.a) * 2 * kHeadDim * 2;
+        uint4 mn = knew, mx = knew;
+        if (slot_a != 0) {
+          const uint4 a0 = *reinterpret_cast<const uint4*>(rec + 16 * c);
+          const uint4 z0 = *reinterpret_cast<const uint4*>(rec + 2 * kHeadDim + 16 * c);
+          const uint32_t a[4] = {a0.x, a0.y, a0.z, a0.w};
+          const uint32_t z[4] = {z0.x, z0.y, z0.z, z0.w};
           const uint32_t nw[4] = {knew.x, knew.y, knew.z, knew.w};
           uint32_t ra[4], rz[4];
 #pragma unroll
@@ -400,33 +533,71 @@ __device__ void s_score_stage(const Params& p, const LayerPtrs& lay, const SSmem
           mn = make_uint4(ra[0], ra[1], ra[2], ra[3]);
           mx = make_uint4(rz[0], rz[1], rz[2], rz[3]);
         }
-        __half* box = lay.meta + box_offset(p, q.b, q.g, page);
+        *reinterpret_cast<uint4*>(rec + 16 * c) = mn;  // the staged box, for the scoring below
+        *reinterpret_cast<uint4*>(rec + 2 * kHeadDim + 16 * c) = mx;
+        __half* box = lay.meta + box_offset(p, q.b, q.g, ap);
         *reinterpret_cast<uint4*>(box + 8 * c) = mn;
         *reinterpret_cast<uint4*>(box + kHeadDim + 8 * c) = mx;
-        const size_t kv = (((size_t)aphys * p.Hkv + q.g) * P + slot_a) * kHeadDim + 8 * c;
+        const size_t kv = (((size_t)ph * p.Hkv + q.g) * P + slot_a) * kHeadDim + 8 * c;
         *reinterpret_cast<uint4*>(lay.k_pool + kv) = knew;
         *reinterpret_cast<uint4*>(lay.v_pool + kv) = vnew;
       } else if (c == 0) {
-        report(p, QUEST_ERR_BAD_PAGE, q.b, page, kSiteAppend);
+        report(p, QUEST_ERR_BAD_PAGE, q.b, ap, kSiteAppend);
       }
     }
-    float best = -CUDART_INF_F;
-#pragma unroll
-    for (int jh = 0; jh < G; ++jh) {
-      float sc = corner_dot<G>(f, jh, mn, mx);
-      sc += __shfl_xor_sync(0xffffffffu, sc, 8);
-      sc += __shfl_xor_sync(0xffffffffu, sc, 4);
-      sc += __shfl_xor_sync(0xffffffffu, sc, 2);
-      sc += __shfl_xor_sync(0xffffffffu, sc, 1);
-      best = fmaxf(best, sc);
-    }
-    if (c == 0 && r < in.n) {
-      // pages of the sink / local window of a long sequence get the largest key
-      const bool forced = windowed && (page < p.sink_pages || page >= q.N - p.local_pages);
-      __stcg(krow + page, forced ? 0xffffffffu : score_key(best));
-    }
+    __threadfence();  // the new rows and box, before this stage's keys
+    __syncwarp();
   }
-  if (mine) fence_proxy_async_global();  // the appended row, before the pair is released
+  unsigned* krow = p.skeys + (size_t)(q.b * p.Hkv + q.g) * p.max_pages;
+  const bool windowed = q.N > q.K && (p.sink_pages > 0 || p.local_pages > 0);
+  // half-warp hw scores boxes hw, hw + 2, ...: UB of them at a time, every load issued
+  // before any arithmetic and the half-warp sums interleaved, so that the stage is not one
+  // long chain of dependent steps
+  constexpr int UB = G <= 2 ? 4 : 2;
+#pragma unroll 1
+  for (int r0 = 0; 2 * r0 < in.n; r0 += UB) {
+    uint4 mn[UB], mx[UB];
+#pragma unroll
+    for (int u = 0; u < UB; ++u) {
+      const int r = 2 * (r0 + u) + hw;
+      mn[u] = make_uint4(0, 0, 0, 0);
+      mx[u] = make_uint4(0, 0, 0, 0);
+      if (r < in.n) {
+        const unsigned char* rec = slot + (size_t)r * 2 * kHeadDim * 2;
+        mn[u] = *reinterpret_cast<const uint4*>(rec + 16 * c);
+        mx[u] = *reinterpret_cast<const uint4*>(rec + 2 * kHeadDim + 16 * c);
+      }
+    }
+    float sc[UB][G];
+#pragma unroll
+    for (int u = 0; u < UB; ++u)
+#pragma unroll
+      for (int jh = 0; jh < G; ++jh) sc[u][jh] = corner_dot<G>(f, jh, mn[u], mx[u]);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+      for (int u = 0; u < UB; ++u)
+#pragma unroll
+        for (int jh = 0; jh < G; ++jh) sc[u][jh] += __shfl_xor_sync(0xffffffffu, sc[u][jh], o);
+    // lane c < UB of half-warp hw writes the key of box 2 (r0 + c) + hw: the warp's keys
+    // of this group are one contiguous run
+    uint32_t key = 0u;
+#pragma unroll
+    for (int u = 0; u < UB; ++u) {
+      float best = sc[u][0];
+#pragma unroll
+      for (int jh = 1; jh < G; ++jh) best = fmaxf(best, sc[u][jh]);
+      const int page = in.a + 2 * (r0 + u) + hw;
+      // pages of the sink / local window of a long sequence get the largest key; no score
+      // key is 0 (that would take a NaN with every bit set), so 0 can mean "not written"
+      const bool forced = windowed && (page < p.sink_pages || page >= q.N - p.local_pages);
+      const uint32_t k = forced ? 0xffffffffu : max(score_key(best), 1u);
+      if (c == u) key = k;
+    }
+    const int r = 2 * (r0 + c) + hw;
+    if (c < UB && r < in.n) __stcg(krow + in.a + r, key);
+  }
+  return takes_token;
 }
 
 // Flash-decode of the one kept page of a decode stage; this warp's state of the piece goes
@@ -451,7 +622,7 @@ __device__ void s_decode_stage(const Params& p, const SSmem& s, const unsigned c
   __syncwarp();
   if (in.n > 0) {
     const __half* Ks = reinterpret_cast<const __half*>(slot);
-    const __half* qs = Ks + 2 * P * kHeadDim;
+    const __half* qs = stage_q<G, P>(p, s, slot, geo_of(p, in));
     float qf[G][4];
 #pragma unroll
     for (int jh = 0; jh < G; ++jh) {
@@ -466,7 +637,7 @@ __device__ void s_decode_stage(const Params& p, const SSmem& s, const unsigned c
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(empty_bar);
-  // the combine buffer of this piece's parity must be done with piece k - 2
+  // the combine buffer of this piece must be done with piece k - nb
   if (ld_volatile_s32(free_word) != k) {
     const long long t0 = global_ns();
     while (ld_volatile_s32(free_word) != k) {
@@ -477,14 +648,14 @@ __device__ void s_decode_stage(const Params& p, const SSmem& s, const unsigned c
       }
     }
   }
-  // this warp's state: m[G], l[G], acc[G][128]
+  // this warp's state: acc[G][128], m[G], l[G]
   if (lane < G) {
-    cb[lane] = st[lane * 3 + 0];
-    cb[G + lane] = st[lane * 3 + 1];
+    cb[G * kHeadDim + lane] = st[lane * 3 + 0];
+    cb[G * kHeadDim + G + lane] = st[lane * 3 + 1];
   }
 #pragma unroll
   for (int jh = 0; jh < G; ++jh)
-    *reinterpret_cast<float4*>(cb + 2 * G + jh * kHeadDim + 4 * lane) =
+    *reinterpret_cast<float4*>(cb + jh * kHeadDim + 4 * lane) =
         make_float4(acc[jh][0], acc[jh][1], acc[jh][2], acc[jh][3]);
 }
 
@@ -492,24 +663,25 @@ __device__ void s_decode_stage(const Params& p, const SSmem& s, const unsigned c
 template <int G>
 __device__ void s_combine(const Params& p, const float* cbase, const PairGeo& q, int v) {
   const int lane = threadIdx.x & 31;
-  constexpr int WF = 2 * G + G * kHeadDim;  // floats per warp state
+  constexpr int WF = cbuf_floats(G);  // floats per warp state
+  constexpr int MO = G * kHeadDim;    // offset of m[G]; l[G] follows
 #pragma unroll
   for (int jh = 0; jh < G; ++jh) {
     float M = -CUDART_INF_F;
 #pragma unroll
-    for (int w = 0; w < kSWarps; ++w) M = fmaxf(M, cbase[w * WF + jh]);
+    for (int w = 0; w < kSWarps; ++w) M = fmaxf(M, cbase[w * WF + MO + jh]);
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
     float Ls = 0.f;
 #pragma unroll
     for (int w = 0; w < kSWarps; ++w) {
-      const float m = cbase[w * WF + jh];
+      const float m = cbase[w * WF + MO + jh];
       const float f = (m == -CUDART_INF_F) ? 0.f : exp2f(m - M);
-      const float4 a = *reinterpret_cast<const float4*>(cbase + w * WF + 2 * G + jh * kHeadDim + 4 * lane);
+      const float4 a = *reinterpret_cast<const float4*>(cbase + w * WF + jh * kHeadDim + 4 * lane);
       A.x = fmaf(a.x, f, A.x);
       A.y = fmaf(a.y, f, A.y);
       A.z = fmaf(a.z, f, A.z);
       A.w = fmaf(a.w, f, A.w);
-      Ls = fmaf(cbase[w * WF + G + jh], f, Ls);
+      Ls = fmaf(cbase[w * WF + MO + G + jh], f, Ls);
     }
     const size_t slotp = ((size_t)q.b * p.Hq + (size_t)q.g * G + jh) * p.n_splits + v;
     *reinterpret_cast<float4*>(p.part_acc + slotp * kHeadDim + 4 * lane) = A;
@@ -524,34 +696,30 @@ template <int G, int P>
 __device__ void s_consume(const Params& p, const LayerPtrs& lay, const SSmem& s, int S,
                           int total_stages, int nS_pad) {
   const int lane = threadIdx.x & 31;
-  const int w = (threadIdx.x >> 5) - kSelWarps;
-  const size_t slot_bytes = s_slot_bytes(G, P);
-  constexpr int WF = 2 * G + G * kHeadDim;
-  int tslot = 1 + 2 * w;
-  bool first_score = true, first_decode = true;
-  for (int stg = w; stg < total_stages; stg += kSWarps) {
-    const int sl = stg % S;
-    const bool ok = mbar_wait_bounded(p, &s.full[sl], (uint32_t)(stg / S) & 1u, kSiteWaitStage);
+  const int w = threadIdx.x >> 5;
+  const size_t slot_bytes = s_slot_bytes(G, P, s.qall != nullptr);
+  constexpr int WF = cbuf_floats(G);
+  if (s.qall) mbar_wait_bounded(p, s.qbar, 0u, kSiteWaitStage);  // the queries have landed
+  static_assert(WF % 4 == 0, "each warp's state starts on 16 bytes");
+  int tslot = 8 + 24 * w;
+  RingPos pos{w, 0u};  // S is a multiple of kSWarps: this warp's slots are w, w + 8, ...
+  for (int stg = w; stg < total_stages; stg += kSWarps, pos.step(kSWarps, S)) {
+    const int sl = pos.slot;
+    const bool ok = mbar_wait_bounded(p, &s.full[sl], pos.phase, kSiteWaitStage);
+    if (lane == 0) strace(p, &tslot, 32 + 24 * w, kSeStageLanded, stg);
     SInfo in = s.info[sl];
     if (!ok) in.n = 0;
-    const unsigned char* slot = s.ring + (size_t)sl * slot_bytes;
+    unsigned char* slot = s.ring + (size_t)sl * slot_bytes;
     if (in.kind == kStScore) {
-      if (first_score && lane == 0 && w == 0) strace(p, &tslot, kSeFirstScore, in.j);
-      first_score = false;
-      const PairGeo q = pair_geo(p, s, in.j);
-      if (in.n > 0) s_score_stage<G, P>(p, lay, s, slot, in, q);
+      const PairGeo q = geo_of(p, in);
+      // a stage that took the new token wrote into its slot: generic writes, ordered before
+      // the slot goes back to bulk copies (the other stages only read their slot)
+      if (in.n > 0 && s_score_stage<G, P>(p, lay, s, slot, in, q)) fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&s.empty[sl]);
-        // the piece is counted on the pair; the warp that completes the pair selects it
-        const unsigned old = atom_add_acq_rel(p.score_arrive + in.j, 1u);
-        if (old + 1u == (unsigned)q.npc) push_job(p, s, kJobSelect, in.j);
-      }
+      if (lane == 0) mbar_arrive(&s.empty[sl]);
     } else if (in.kind == kStDecode) {
-      if (first_decode && lane == 0 && w == 0) strace(p, &tslot, kSeFirstDecode, in.j);
-      first_decode = false;
       const int k = (stg - nS_pad) / kSWarps;  // this CTA's decode piece
-      const int par = k & 1;
+      const int par = k % s.nb;
       float* cbase = s.cbuf + (size_t)par * kSWarps * WF;
       s_decode_stage<G, P>(p, s, slot, in, w, &s.empty[sl], cbase + w * WF,
                            &s.ctl[kCtlFree + par], k);
@@ -564,60 +732,72 @@ __device__ void s_consume(const Params& p, const LayerPtrs& lay, const SSmem& s,
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
         __threadfence_block();
-        const PairGeo q = pair_geo(p, s, in.j);
+        const PairGeo q = geo_of(p, in);
         s_combine<G>(p, cbase, q, in.a);
         __syncwarp();
         if (lane == 0) {
           s.ctl[kCtlComb + par] = 0;
           __threadfence_block();
-          atomicExch(&s.ctl[kCtlFree + par], k + 2);
-          const unsigned old = atom_add_acq_rel(p.decode_arrive + in.j, 1u);
-          if (old + 1u == (unsigned)q.ndc) push_job(p, s, kJobMerge, in.j);
+          atomicExch(&s.ctl[kCtlFree + par], k + s.nb);
+          red_add_release(p.decode_arrive + in.j, 1u);  // after the partial
         }
       }
-      if (lane == 0 && stg + kSWarps >= total_stages && w == 0)
-        strace(p, &tslot, kSeLastDecode, in.j);
     } else {
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.empty[sl]);
     }
-  }
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence_block();
-    atomicAdd(&s.ctl[kCtlDone], 1);
+    if (lane == 0 && in.kind != kStEmpty)
+      strace(p, &tslot, 32 + 24 * w, kSeStageDone, (stg & 0xfffff) | (in.kind << 20));
   }
 }
 
 // ---------------------------------------------------------------- selector team
 // Exact top-K of pair j's keys; the kept pages (ascending) go out with their physical
-// pages, then the pair is released to the decode pieces.
+// pages, then the pair is released to the decode pieces.  The keys arrive in the pair's
+// key row from every CTA's consumers: the row is read until none of its N keys is 0 (not
+// written yet), then cleared for the next call.
 __device__ void s_select(const Params& p, const SSmem& s, const PairGeo& q, int j) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int* sel = s.sel;
-  int* cnt_slot = s.scratch + 200;
-  if (q.N <= q.K) {
-    for (int r = tid; r < q.K; r += kSelThreads) sel[r] = r;
-  } else {
-    const uint32_t* krow = reinterpret_cast<const uint32_t*>(p.scores) + (size_t)j * p.max_pages;
-    uint32_t lo = 0xffffffffu, hi = 0u;
-    for (int i0 = 0; i0 < q.N; i0 += 16 * kSelThreads) {
-      uint32_t v[16];
+  unsigned* krow = p.skeys + (size_t)j * p.max_pages;
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  const long long t0 = global_ns();
+  while (true) {
+    int missing = 0;
+    lo = 0xffffffffu;
+    hi = 0u;
+#pragma unroll 1
+    for (int i0 = 0; i0 < q.N; i0 += 4 * kSelThreads) {
+      uint32_t v[4];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
+      for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * kSelThreads + tid;
-        v[u] = i < q.N ? __ldcg(krow + i) : 0u;
+        v[u] = i < q.N ? __ldcg(krow + i) : 1u;
       }
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
+      for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * kSelThreads + tid;
         if (i < q.N) {
           s.keys[i] = v[u];
+          missing |= v[u] == 0u;
           lo = min(lo, v[u]);
           hi = max(hi, v[u]);
         }
       }
     }
+    if (!bany<kSelThreads>(missing != 0)) break;
+    // thread 0 decides when to give up, for the whole team
+    if (bany<kSelThreads>(tid == 0 && global_ns() - t0 > p.wait_limit_ns)) {
+      if (tid == 0) report(p, QUEST_ERR_TIMEOUT, q.b, -1, kSiteWaitSelection);
+      break;
+    }
+    __nanosleep(200);
+  }
+  // the keys are in shared memory: clear the row for the next call
+  for (int i = tid; i < q.N; i += kSelThreads) __stcg(krow + i, 0u);
+  if (q.N <= q.K) {
+    for (int r = tid; r < q.K; r += kSelThreads) sel[r] = r;
+  } else {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
@@ -625,7 +805,7 @@ __device__ void s_select(const Params& p, const SSmem& s, const PairGeo& q, int 
     }
     if (lane == 0) {
       s.scratch[100 + warp] = (int)lo;
-      s.scratch[110 + warp] = (int)hi;
+      s.scratch[120 + warp] = (int)hi;
     }
     bsync<kSelThreads, true>();
     lo = 0xffffffffu;
@@ -633,10 +813,14 @@ __device__ void s_select(const Params& p, const SSmem& s, const PairGeo& q, int 
 #pragma unroll
     for (int w = 0; w < kSelWarps; ++w) {
       lo = min(lo, (uint32_t)s.scratch[100 + w]);
-      hi = max(hi, (uint32_t)s.scratch[110 + w]);
+      hi = max(hi, (uint32_t)s.scratch[120 + w]);
     }
-    topk_keys<kSelThreads, true>(s.keys, q.N, q.K, lo, hi, sel, cnt_slot, s.hist, s.kept,
-                                 s.scratch);
+    if (tid == 0) {
+      int* ts = s.scratch + 250;  // the team's trace slot, kept by the team's loop
+      strace(p, ts, kTrLast, kSeSelLoaded, j);
+    }
+    topk_fast<kSelThreads, true>(s.keys, q.N, q.K, lo, hi, sel, s.hist, s.scratch);
+    if (tid == 0) strace(p, s.scratch + 250, kTrLast, kSeSelTopk, j);
   }
   bsync<kSelThreads, true>();
   // kept pages with their physical page, for the decode producers; the caller's copy
@@ -655,12 +839,12 @@ __device__ void s_select(const Params& p, const SSmem& s, const PairGeo& q, int 
   if (idx_row)
     for (int r = q.K + tid; r < p.top_k; r += kSelThreads) idx_row[r] = -1;
   if (tid == 0 && p.sel_count) p.sel_count[j] = q.K;
+  if (tid == 0) strace(p, s.scratch + 250, kTrLast, kSeSelWritten, j);
   __threadfence();
   bsync<kSelThreads, true>();
-  if (tid == 0) {
-    p.score_arrive[j] = 0u;  // every piece of the pair has arrived: ready for the next call
-    if (!(p.debug_flags & QUEST_DEBUG_WITHHOLD_SELECTION)) st_release_u32(p.ready + j, 1u);
-  }
+  if (tid == 0) strace(p, s.scratch + 250, kTrLast, kSeSelFenced, j);
+  if (tid == 0 && !(p.debug_flags & QUEST_DEBUG_WITHHOLD_SELECTION))
+    st_release_u32(p.ready + j, 1u);
 }
 
 // Log-sum-exp merge of pair j's piece partials into out / lse.
@@ -734,56 +918,38 @@ __device__ void s_empty_pair(const Params& p, const LayerPtrs& lay, const PairGe
   if (tid == 0 && p.sel_count) p.sel_count[j] = 0;
 }
 
+// Selector CTA sc of Cs owns pairs sc, sc + Cs, ...: pairs finish scoring roughly in
+// order, so consecutive pairs go to different selector CTAs and are selected side by side.
+// For each of its pairs, in order, the team waits until all of the pair's keys are in and
+// selects; then, pair by pair again, it waits until every decode piece has been combined
+// (counted by the streaming CTAs' consumers with release reductions, polled with acquire
+// loads; all CTAs are resident, so every count completes) and merges.
 template <int G>
-__device__ void s_selector(const Params& p, const LayerPtrs& lay, const SSmem& s, int NP) {
+__device__ void s_selector(const Params& p, const LayerPtrs& lay, const SSmem& s, int NP,
+                           int sc, int Cs) {
   const int tid = threadIdx.x;
-  int tslot = kStreamTrace / 2 + 8;
-  // pairs without a token are finished here
-  for (int j = (int)blockIdx.x; j < NP; j += (int)gridDim.x) {
+  int* tslot = s.scratch + 250;  // the team's next trace record (thread 0 only)
+  if (tid == 0) *tslot = kTrSelector;
+  for (int j = sc; j < NP; j += Cs) {
     const PairGeo q = pair_geo(p, s, j);
-    if (q.N == 0) s_empty_pair<G>(p, lay, q, j);
+    if (q.N == 0) {
+      s_empty_pair<G>(p, lay, q, j);
+      continue;
+    }
+    if (tid == 0) strace(p, tslot, kTrLast, kSeSelBegin, j);
+    s_select(p, s, q, j);
+    if (tid == 0) strace(p, tslot, kTrLast, kSeSelEnd, j);
+    bsync<kSelThreads, true>();
   }
-  int* bc = s.scratch + 240;  // broadcast of the job
-  for (int head = 0;; ++head) {
-    const int sl = head % kJobs;
-    if (tid == 0) {
-      int job = ld_volatile_s32(&s.jobs[sl]);
-      const long long t0 = global_ns();
-      while (job == 0) {
-        if (ld_volatile_s32(&s.ctl[kCtlDone]) == kSWarps) {
-          job = ld_volatile_s32(&s.jobs[sl]);  // a job pushed before the last warp finished
-          if (job == 0) job = -1;
-          break;
-        }
-        __nanosleep(64);
-        job = ld_volatile_s32(&s.jobs[sl]);
-        if (global_ns() - t0 > 4 * p.wait_limit_ns) {
-          report(p, QUEST_ERR_TIMEOUT, -1, -1, kSiteWaitSelection);
-          job = -1;
-          break;
-        }
-      }
-      if (job > 0) {
-        s.jobs[sl] = 0;
-        __threadfence();  // acquire side of the pair's completion, for the whole team
-      }
-      *bc = job;
-    }
-    bsync<kSelThreads, true>();
-    const int job = *bc;
-    bsync<kSelThreads, true>();
-    if (job < 0) break;
-    const int kind = job >> 28, j = (job & 0x0fffffff) - 1;
+  for (int j = sc; j < NP; j += Cs) {
     const PairGeo q = pair_geo(p, s, j);
-    if (kind == kJobSelect) {
-      if (tid == 0) strace(p, &tslot, kSeSelBegin, j);
-      s_select(p, s, q, j);
-      if (tid == 0) strace(p, &tslot, kSeSelEnd, j);
-    } else {
-      if (tid == 0) strace(p, &tslot, kSeMergeBegin, j);
-      s_merge<G>(p, lay, s, q, j);
-      if (tid == 0) strace(p, &tslot, kSeMergeEnd, j);
-    }
+    if (q.N == 0) continue;
+    if (tid == 0) wait_flag_bounded(p, p.decode_arrive + j, (unsigned)q.ndc, q.b, kSiteWaitSlot);
+    bsync<kSelThreads, true>();
+    (void)ld_acquire_u32(p.decode_arrive + j);  // every thread acquires the pair's partials
+    if (tid == 0) strace(p, tslot, kTrLast, kSeMergeBegin, j);
+    s_merge<G>(p, lay, s, q, j);
+    if (tid == 0) strace(p, tslot, kTrLast, kSeMergeEnd, j);
     bsync<kSelThreads, true>();
   }
 }
@@ -798,18 +964,22 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   extern __shared__ __align__(128) unsigned char smem[];
   SSmem s;
   int S = 0;  // ring slots: the host launched with the same layout
-  stream_smem_layout(G, P, p.max_pages, p.top_k, p.B, kMaxSmem, &S, &s, smem);
+  stream_smem_layout(G, P, p.max_pages, p.top_k, p.B, p.Hq, kMaxSmem, p.ring_slots, &S, &s,
+                     smem);
   const int tid = threadIdx.x;
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
+    mbar_init(s.qbar, 1);
     fence_mbar_init();
   }
+  const int Cs = p.sel_ctas, C = (int)gridDim.x - Cs, c = (int)blockIdx.x;
+  const bool selector = c >= C;  // the last Cs CTAs select and merge, the others stream
   if (tid < kCtlWords) s.ctl[tid] = (tid == kCtlFree + 1) ? 1 : 0;
-  if (tid < kJobs) s.jobs[tid] = 0;
-  for (int i = tid; i < 2 * kTopkBins; i += blockDim.x) s.hist[i] = 0;
+  if (selector)
+    for (int i = tid; i < kFastBins; i += blockDim.x) s.hist[i] = 0;
   pdl_wait();
   // this step's length of every sequence (the new token counts when there is room)
   const long long cap = (long long)p.max_pages * p.P;
@@ -866,38 +1036,37 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   }
   __syncthreads();
   const int TS = s.sb[p.B], TD = s.db[p.B];
-  const int C = (int)gridDim.x, c = (int)blockIdx.x;
-  const int nS = c < TS ? (TS - 1 - c) / C + 1 : 0;
-  const int nD = c < TD ? (TD - 1 - c) / C + 1 : 0;
+  const int nS = !selector && c < TS ? (TS - 1 - c) / C + 1 : 0;
+  const int nD = !selector && c < TD ? (TD - 1 - c) / C + 1 : 0;
   const int nS_pad = (nS + kSWarps - 1) / kSWarps * kSWarps;
   const int total = nS_pad + nD * kSWarps;
   if (tid == 0) {
     int t0 = 0;
-    strace(p, &t0, kSeStart, TS);
+    strace(p, &t0, 1, kSeStart, TS);
   }
   const int warp = tid >> 5;
-  if (warp == kProducerWarp) {
-    s_produce<G, P>(p, lay, s, S, TS, TD, nS_pad);
-  } else if (warp >= kSelWarps) {
+  if (selector) {
+    if (warp < kSelWarps) s_selector<G>(p, lay, s, p.B * p.Hkv, c - C, Cs);
+  } else if (warp == kProducerWarp) {
+    s_produce<G, P>(p, lay, s, S, C, TS, TD, nS, nS_pad);
+  } else if (warp < kSWarps) {
     s_consume<G, P>(p, lay, s, S, total, nS_pad);
-  } else {
-    s_selector<G>(p, lay, s, p.B * p.Hkv);
   }
   __syncthreads();
   // a wait that gave up may leave copies in flight: let them land before the CTA leaves
-  if (tid == kProducerWarp * 32 && ld_relaxed_s32(p.status) != QUEST_OK) {
+  if (!selector && tid == kProducerWarp * 32 && ld_relaxed_s32(p.status) != QUEST_OK) {
     const int last = total;
     for (int st = max(0, last - S); st < last; ++st)
       mbar_wait_bounded(p, &s.full[st % S], (uint32_t)(st / S) & 1u, kSiteWaitStage);
   }
   if (tid == 0) {
     int tl = kStreamTrace - 1;
-    strace(p, &tl, kSeExit, 0);
+    strace(p, &tl, kStreamTrace, kSeExit, 0);
   }
   // With an appended token, CTA 0 advances the lengths once every CTA has read them.
   if (p.chain_append && !p.hold_lengths && c == 0 && tid < 32) {
     bool ok = true;
-    if (tid == 0) ok = wait_flag_bounded(p, p.started, (unsigned)C, -1, kSiteWaitSlot);
+    if (tid == 0) ok = wait_flag_bounded(p, p.started, gridDim.x, -1, kSiteWaitSlot);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (ok) {
       for (int b = tid; b < p.B; b += 32) {
@@ -932,11 +1101,18 @@ static const void* pick_stream(int G, int P) {
   }
 }
 
+// Ring slots at most (the shared memory left after the rest usually holds fewer: ~24 slots
+// of 8 KB at page 16; a shallower ring measured no faster).
+constexpr int kStreamMaxSlots = 64;
+
 // Ring slots of the stream kernel for this shape (0: it does not fit).
-int stream_slots(int G, int P, int max_pages, int top_k, int batch) {
-  if (batch > kStreamMaxBatch || top_k > kStreamMaxTopk) return 0;
+int stream_slots(int G, int P, int max_pages, int top_k, int batch, int hq) {
+  // (the selection packs per-thread counts of keys in 16 bits)
+  if (batch > kStreamMaxBatch || top_k > kStreamMaxTopk || max_pages >= 65536)
+    return 0;
   int S = 0;
-  stream_smem_layout(G, P, max_pages, top_k, batch, kMaxSmem, &S, nullptr, nullptr);
+  stream_smem_layout(G, P, max_pages, top_k, batch, hq, kMaxSmem, kStreamMaxSlots, &S,
+                     nullptr, nullptr);
   return S;
 }
 
@@ -972,39 +1148,46 @@ cudaError_t device_info(DevInfo* out) {
 
 }  // namespace
 
-size_t stream_smem_bytes(int G, int P, int max_pages, int top_k, int batch) {
-  return stream_smem_layout(G, P, max_pages, top_k, batch, kMaxSmem, nullptr, nullptr, nullptr);
+size_t stream_smem_bytes(int G, int P, int max_pages, int top_k, int batch, int hq) {
+  const int S = stream_slots(G, P, max_pages, top_k, batch, hq);
+  return stream_smem_layout(G, P, max_pages, top_k, batch, hq, kMaxSmem, S, nullptr, nullptr,
+                            nullptr);
 }
 
-// CTAs of a stream launch: one per SM, fewer for a small step (about 64 KB of stream per
-// CTA at least), at most max_ctas when given.
-cudaError_t stream_grid(const Params& p, int max_ctas, int* ctas) {
+// CTAs of a stream launch: selector CTAs, one for every two pairs (at most 16, at most a
+// quarter of the grid, at least one), and streaming CTAs, one per remaining SM, fewer for a
+// small step (about 64 KB of stream per CTA at least).  max_ctas, when given, caps the
+// whole grid (which keeps at least one CTA of each kind).
+cudaError_t stream_grid(const Params& p, int max_ctas, int* ctas, int* sel_ctas) {
   DevInfo d;
   cudaError_t e = device_info(&d);
   if (e != cudaSuccess) return e;
   if (!d.coop) return cudaErrorNotSupported;
   const long long kcap = std::min<long long>(p.top_k, p.max_pages);
-  const long long bytes = (long long)p.B * p.Hkv *
-                          ((long long)p.max_pages * 2 * kHeadDim * 2 + kcap * p.P * kHeadDim * 4);
-  long long n = (bytes + (64 << 10) - 1) / (64 << 10);
+  const long long pairs = (long long)p.B * p.Hkv;
+  const long long bytes =
+      pairs * ((long long)p.max_pages * 2 * kHeadDim * 2 + kcap * p.P * kHeadDim * 4);
+  const long long want_sel = std::max<long long>(1, std::min<long long>(16, (pairs + 1) / 2));
+  long long n = (bytes + (64 << 10) - 1) / (64 << 10) + want_sel;
   if (n > d.sms) n = d.sms;
-  if (n < 1) n = 1;
   if (max_ctas > 0 && n > max_ctas) n = max_ctas;
+  if (n < 2) n = 2;
+  const long long sel = std::max<long long>(1, std::min<long long>(want_sel, n / 4));
   *ctas = (int)n;
+  *sel_ctas = (int)sel;
   return cudaSuccess;
 }
 
 cudaError_t launch_stream(const Params& p, const LayerPtrs& lay, int G, int max_ctas,
                           cudaStream_t s) {
-  const int S = stream_slots(G, p.P, p.max_pages, p.top_k, p.B);
+  const int S = stream_slots(G, p.P, p.max_pages, p.top_k, p.B, p.Hq);
   if (S < kSWarps) return cudaErrorInvalidConfiguration;
-  const size_t smem = stream_smem_layout(G, p.P, p.max_pages, p.top_k, p.B, kMaxSmem, nullptr,
-                                         nullptr, nullptr);
+  const size_t smem = stream_smem_bytes(G, p.P, p.max_pages, p.top_k, p.B, p.Hq);
   const void* fn = pick_stream(G, p.P);
   cudaError_t e = ensure_smem(fn, smem);
   if (e != cudaSuccess) return e;
-  int ctas = 0;
-  if ((e = stream_grid(p, max_ctas, &ctas)) != cudaSuccess) return e;
+  int ctas = 0, sel = 0;
+  if ((e = stream_grid(p, max_ctas, &ctas, &sel)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kStreamThreads);
@@ -1016,6 +1199,8 @@ cudaError_t launch_stream(const Params& p, const LayerPtrs& lay, int G, int max_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   Params pp = p;
+  pp.sel_ctas = sel;
+  pp.ring_slots = S;
   LayerPtrs ll = lay;
   void* args[] = {&pp, &ll};
   return cudaLaunchKernelExC(&cfg, fn, args);

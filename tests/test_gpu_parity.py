@@ -463,7 +463,7 @@ def test_stream_trace_records_a_timeline():
     merge per (b, g), each by some CTA's selector team."""
     w = small(lens=(3000, 700), batch=2, budget=256)
     pair = H.on_device(w)
-    cap = 64 * 160
+    cap = 256 * 160  # 256 records per CTA, at most one CTA per SM
     tr = torch.zeros(1 + 2 * cap, dtype=torch.int64, device="cuda")
     q.decode(pair.cache, w.q[0].cuda(), w.top_k, pair.ws,
              q.opts(trace=tr, path=q.QUEST_PATH_STREAM))
@@ -662,3 +662,34 @@ def test_withheld_selection_times_out_and_context_survives(path):
     assert rc == q.QUEST_ERR_TIMEOUT
     q.workspace_init(pair.ws)
     H.run_step_and_compare(pair, 0, w.top_k, opts=q.opts(path=path))
+
+
+@pytest.mark.parametrize("path", [q.QUEST_PATH_AUTO, q.QUEST_PATH_STREAM], ids=["auto", "stream"])
+def test_decode_plan_matches_calls(path):
+    """A DecodePlan (arguments checked once) issues the same C calls as decode_step /
+    decode: two copies of one workload stepped side by side give bit-identical outputs,
+    selections, boxes and lengths; a q of the wrong shape is refused before any launch."""
+    w = small(lens=(3000, 700, 1), batch=3, hq=8, hkv=4, budget=256, outliers=4, steps=3)
+    a, b = H.on_device(w), H.on_device(w)
+    o = q.opts(path=path)
+    shape_i, shape_c = (3, 4, w.top_k), (3, 4)
+    ia = torch.empty(shape_i, dtype=torch.int32, device="cuda")
+    ca = torch.empty(shape_c, dtype=torch.int32, device="cuda")
+    ib = torch.empty_like(ia)
+    cb = torch.empty_like(ca)
+    plan = q.DecodePlan(b.cache, w.top_k, b.ws, o, idx_out=ib, count_out=cb)
+    for t in range(w.steps):
+        qd, kn, vn = w.q[t].cuda(), w.k_new[t].cuda(), w.v_new[t].cuda()
+        oa, la = q.decode_step(a.cache, qd, kn, vn, w.top_k, a.ws, o, idx_out=ia, count_out=ca)
+        ob, lb = plan.step(qd, kn, vn)
+        assert torch.equal(oa, ob) and torch.equal(la, lb), t
+        assert torch.equal(ia, ib) and torch.equal(ca, cb), t
+    oa, la = q.decode(a.cache, w.q[0].cuda(), w.top_k, a.ws, o)
+    ob, lb = plan.decode(w.q[0].cuda())
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+    H.assert_status_ok(a.ws)
+    H.assert_status_ok(b.ws)
+    assert torch.equal(a.cache.meta, b.cache.meta)
+    assert torch.equal(a.cache.seq_lens, b.cache.seq_lens)
+    with pytest.raises(ValueError):
+        plan.decode(torch.zeros((3, 4, 128), dtype=torch.float16, device="cuda"))
