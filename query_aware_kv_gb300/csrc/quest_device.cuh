@@ -115,6 +115,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 16-byte copy global -> shared through the load path (L2 only).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+// An arrival on `bar` once this thread's earlier cp.async copies have landed; the pending
+// count is raised by one now, so the phase cannot complete before that arrival.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ uint4 ld_stream_v4(const void* ptr) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -335,31 +345,69 @@ __device__ __forceinline__ float corner_dot(const QueryFrag<G>& f, int j, const 
   return s;
 }
 
+// The step's new token into page ap of (b, g), by the 16 threads c = 0..15 of one half-warp
+// (16 bytes of the row each): its K / V rows go to slot `aslot` of physical page `aphys`
+// (-1: unmapped, reported, nothing written) and its box opens (slot 0) or widens with the
+// new key.
+__device__ __forceinline__ void append_token_box(const Params& p, int b, int g, int ap,
+                                                 int aslot, int aphys, int c) {
+  if (aphys < 0) {
+    if (c == 0) report(p, QUEST_ERR_BAD_PAGE, b, ap, kSiteAppend);
+    return;
+  }
+  const size_t o = ((size_t)b * p.Hkv + g) * kHeadDim + 8 * c;
+  const uint4 knew = *reinterpret_cast<const uint4*>(p.k_new + o);
+  const uint4 vnew = *reinterpret_cast<const uint4*>(p.v_new + o);
+  __half* box = p.meta + box_offset(p, b, g, ap) + 8 * c;
+  uint4 mn = knew, mx = knew;
+  if (aslot != 0) {
+    const uint4 a0 = __ldcg(reinterpret_cast<const uint4*>(box));
+    const uint4 z0 = __ldcg(reinterpret_cast<const uint4*>(box + kHeadDim));
+    const uint32_t a[4] = {a0.x, a0.y, a0.z, a0.w};
+    const uint32_t z[4] = {z0.x, z0.y, z0.z, z0.w};
+    const uint32_t n[4] = {knew.x, knew.y, knew.z, knew.w};
+    uint32_t ra[4], rz[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const __half2 hn = *reinterpret_cast<const __half2*>(&n[w]);
+      const __half2 l2 = __hmin2(*reinterpret_cast<const __half2*>(&a[w]), hn);
+      const __half2 h2 = __hmax2(*reinterpret_cast<const __half2*>(&z[w]), hn);
+      ra[w] = *reinterpret_cast<const uint32_t*>(&l2);
+      rz[w] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    mn = make_uint4(ra[0], ra[1], ra[2], ra[3]);
+    mx = make_uint4(rz[0], rz[1], rz[2], rz[3]);
+  }
+  *reinterpret_cast<uint4*>(box) = mn;
+  *reinterpret_cast<uint4*>(box + kHeadDim) = mx;
+  const size_t kv = (((size_t)aphys * p.Hkv + g) * p.P + aslot) * kHeadDim + 8 * c;
+  *reinterpret_cast<uint4*>(p.k_pool + kv) = knew;
+  *reinterpret_cast<uint4*>(p.v_pool + kv) = vnew;
+}
+
 // Scores of pages [p0, p0 + n_live) of (b, g) into dst.  The boxes of those pages are
 // contiguous (logical page order).  Half-warp per page, 16 B of the min row and 16 B of the
 // max row per lane, 4 pages in flight per half-warp.  Called by the whole block.
 // PerHead: dst is query head (g * G)'s row of a [B][Hq][max_pages] array and every head of
 // the group writes its own bound (rows `stride` floats apart) instead of the group maximum.
 // Append (a chain step, not PerHead): page ap, if in this tile, first takes the step's new
-// token: its K / V rows go to slot `aslot` of physical page `aphys` (-1: unmapped,
-// reported, nothing written) and its box opens (slot 0) or widens with the new key in
-// registers before it is scored, as in the one-launch kernel.  A variant of its own, so
-// that the plain estimate keeps its registers.
+// token (append_token_box, by the block's first half-warp, before a block barrier), and the
+// boxes are then read through L2 (the read-only path may not see a box written during the
+// kernel), so the page is scored with its new box, as in the one-launch kernels.
 template <int G, bool PerHead = false, bool Append = false>
 __device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, float* dst,
                            size_t stride = 0, int ap = -1, int aslot = 0, int aphys = -1) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int hw = tid >> 4, c = tid & 15, nhw = nthr >> 4;
+  if constexpr (Append && !PerHead) {
+    if (ap >= p0 && ap < p0 + n_live) {  // block-uniform
+      if (tid < 16) append_token_box(p, b, g, ap, aslot, aphys, c);
+      __syncthreads();
+    }
+  }
   QueryFrag<G> f;
   load_query_frag<G>(p, b, g, c, f);
   const __half* box0 = p.meta + box_offset(p, b, g, p0) + 8 * c;
-  const bool has_append = Append && !PerHead && ap >= p0 && ap < p0 + n_live;
-  uint4 knew = make_uint4(0, 0, 0, 0), vnew = make_uint4(0, 0, 0, 0);
-  if (has_append) {
-    const size_t o = ((size_t)b * p.Hkv + g) * kHeadDim + 8 * c;
-    knew = *reinterpret_cast<const uint4*>(p.k_new + o);
-    vnew = *reinterpret_cast<const uint4*>(p.v_new + o);
-  }
   constexpr int U = 4;
   for (int base = 0; base < n_live; base += U * nhw) {
     uint4 mn[U], mx[U];
@@ -370,45 +418,12 @@ __device__ void score_tile(const Params& p, int b, int g, int p0, int n_live, fl
       mx[u] = make_uint4(0, 0, 0, 0);
       if (r < n_live) {
         const __half* src = box0 + (size_t)r * 2 * kHeadDim;
-        mn[u] = ld_stream_v4(src);
-        mx[u] = ld_stream_v4(src + kHeadDim);
-      }
-    }
-    if constexpr (Append && !PerHead) {
-      if (has_append) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int r = base + u * nhw + hw;
-          if (r >= n_live || p0 + r != ap) continue;
-          if (aphys < 0) {
-            if (c == 0) report(p, QUEST_ERR_BAD_PAGE, b, ap, kSiteAppend);
-            continue;
-          }
-          if (aslot == 0) {
-            mn[u] = knew;
-            mx[u] = knew;
-          } else {
-            const uint32_t a[4] = {mn[u].x, mn[u].y, mn[u].z, mn[u].w};
-            const uint32_t z[4] = {mx[u].x, mx[u].y, mx[u].z, mx[u].w};
-            const uint32_t n[4] = {knew.x, knew.y, knew.z, knew.w};
-            uint32_t ra[4], rz[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const __half2 hn = *reinterpret_cast<const __half2*>(&n[w]);
-              const __half2 l2 = __hmin2(*reinterpret_cast<const __half2*>(&a[w]), hn);
-              const __half2 h2 = __hmax2(*reinterpret_cast<const __half2*>(&z[w]), hn);
-              ra[w] = *reinterpret_cast<const uint32_t*>(&l2);
-              rz[w] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
-            mn[u] = make_uint4(ra[0], ra[1], ra[2], ra[3]);
-            mx[u] = make_uint4(rz[0], rz[1], rz[2], rz[3]);
-          }
-          __half* box = p.meta + box_offset(p, b, g, ap) + 8 * c;
-          *reinterpret_cast<uint4*>(box) = mn[u];
-          *reinterpret_cast<uint4*>(box + kHeadDim) = mx[u];
-          const size_t kv = (((size_t)aphys * p.Hkv + g) * p.P + aslot) * kHeadDim + 8 * c;
-          *reinterpret_cast<uint4*>(p.k_pool + kv) = knew;
-          *reinterpret_cast<uint4*>(p.v_pool + kv) = vnew;
+        if constexpr (Append && !PerHead) {
+          mn[u] = __ldcg(reinterpret_cast<const uint4*>(src));
+          mx[u] = __ldcg(reinterpret_cast<const uint4*>(src + kHeadDim));
+        } else {
+          mn[u] = ld_stream_v4(src);
+          mx[u] = ld_stream_v4(src + kHeadDim);
         }
       }
     }
@@ -849,46 +864,57 @@ __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap&
     for (int k = 0; k < 4; ++k) acc[j][k] = 0.f;
 
   if (warp == kConsumerWarps) {
-    // ---- producer warp: resolve pages 32 at a time, then issue their copies in order
+    // ---- producer warp: resolve pages 32 at a time, then fill their stages in order.  A
+    // page's K and V chunks lie anywhere in the pool: the whole warp copies them, 16 bytes a
+    // lane per instruction (scattered 4-8 KB chunks come in faster through the load path
+    // than as bulk copies), and the stage completes on its full barrier through the copies'
+    // own arrivals (each lane's, plus one plain arrival of lane 0).
     const size_t chunk_elems = (size_t)P * kHeadDim;
     for (int base = 0; base < n_tile; base += 32) {
       const int r = base + lane;
-      int nv = 0;
-      const __half* ksrc = nullptr;
-      const __half* vsrc = nullptr;
+      int nv = 0, phys = 0;
       if (r < n_tile) {
         const int lp = sel_row ? __ldcg(sel_row + r0 + r) : r0 + r;
         if (lp < 0 || lp >= N_b) {
           report(p, QUEST_ERR_BAD_SELECTION, b, lp, kSiteSelection);
         } else {
-          const int phys = p.block_table[(size_t)b * p.max_pages + lp];
+          phys = p.block_table[(size_t)b * p.max_pages + lp];
           if (phys < 0 || phys >= p.num_phys) {
             report(p, QUEST_ERR_BAD_PAGE, b, lp, kSiteDecode);
+            phys = 0;
           } else {
             nv = min(P, L - lp * P);
-            const size_t off = ((size_t)phys * p.Hkv + g) * chunk_elems;
-            ksrc = p.k_pool + off;
-            vsrc = p.v_pool + off;
           }
         }
       }
       const int cnt = min(32, n_tile - base);
+#pragma unroll 1
       for (int j = 0; j < cnt; ++j) {
-        if (lane == j) {
-          const uint32_t k = pc + (uint32_t)r;
-          const int stage = (int)(k % kStages);
-          const uint32_t par = ((k / kStages) & 1u) ^ 1u;
-          const bool ok = mbar_wait_bounded(p, &empty[stage], par, kSiteWaitSlot);
-          nvalid_s[stage] = ok ? nv : 0;
-          if (ok && nv > 0) {
-            unsigned char* dst = ring + (size_t)stage * 2 * kChunk;
-            mbar_arrive_expect_tx(&full[stage], 2 * kChunk);
-            bulk_g2s(dst, ksrc, kChunk, &full[stage]);
-            bulk_g2s(dst + kChunk, vsrc, kChunk, &full[stage]);
-          } else {
-            mbar_arrive(&full[stage]);
-          }
+        const int nvj = __shfl_sync(0xffffffffu, nv, j);
+        const int phj = __shfl_sync(0xffffffffu, phys, j);
+        const uint32_t k = pc + (uint32_t)(base + j);
+        const int stage = (int)(k % kStages);
+        const uint32_t par = ((k / kStages) & 1u) ^ 1u;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait_bounded(p, &empty[stage], par, kSiteWaitSlot);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();  // the stage's last reads happen before any lane's copy into it
+        const int nvs = ok ? nvj : 0;
+        if (lane == 0) nvalid_s[stage] = nvs;
+        if (nvs > 0) {  // warp-uniform
+          const size_t off = (((size_t)phj * p.Hkv + g) * chunk_elems) * 2 + 16 * lane;
+          const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_pool) + off;
+          const unsigned char* vs = reinterpret_cast<const unsigned char*>(p.v_pool) + off;
+          unsigned char* dst = ring + (size_t)stage * 2 * kChunk + 16 * lane;
+#pragma unroll
+          for (int u = 0; u < (int)kChunk / 512; ++u) cp_async16(dst + 512 * u, ks + 512 * u);
+#pragma unroll
+          for (int u = 0; u < (int)kChunk / 512; ++u)
+            cp_async16(dst + kChunk + 512 * u, vs + 512 * u);
+          cp_async_arrive(&full[stage]);
+          __syncwarp();  // every lane's pending arrival is counted before lane 0's
         }
+        if (lane == 0) mbar_arrive(&full[stage]);
         __syncwarp();
       }
     }

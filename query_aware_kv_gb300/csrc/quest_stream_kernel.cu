@@ -271,16 +271,6 @@ __device__ __forceinline__ void strace(const Params& p, int* slot, int limit, in
 __device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// 16-byte copy global -> shared through the load path (L2 only).
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
-// An arrival on `bar` once this thread's earlier cp.async copies have landed; the pending
-// count is raised by one now, so the phase cannot complete before that arrival.
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 __device__ __forceinline__ int ld_volatile_s32(const int* p) {
   return *reinterpret_cast<const volatile int*>(p);
 }
