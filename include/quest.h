@@ -352,12 +352,15 @@ int quest_dense_decode(const quest_cache_t* cache, const void* q, void* out, flo
  * array in the library's own device memory (present on every GPU that loads the library,
  * until the process exits); a cache / top_k whose quest_workspace_size() exceeds 16 MiB is
  * rejected with QUEST_ERR_WORKSPACE.  Nothing is allocated.
- * - The first call on each device looks up that array's device address (with the device
- *   current); make that first call before any stream capture.
+ * - Every call looks up that array's address on the current device (not a stream
+ *   operation), so a device reset that rebuilds the context leaves no stale address.
  * - Every call, on every stream, shares the one array: calls that may overlap on the GPU
  *   race and give wrong results.  Each call clears the part that must start at zero.
  * - status_out (nullable, device int32[4]) receives the device status word and its three
- *   detail words (see quest_read_status) once the call's work is done, in stream order.
+ *   detail words (see quest_read_status) once the call's work is done, in stream order
+ *   (QUEST_OK and zeros for batch 0).  The array is private to the library and the next
+ *   call clears it: with status_out NULL a device-side error (an unmapped page, a wait
+ *   that ran out) of this call is lost.
  */
 int quest_decode_static(const quest_cache_t* cache, const void* q, int32_t top_k, void* out,
                         float* lse, int32_t* idx_out, int32_t* count_out, int32_t* status_out,

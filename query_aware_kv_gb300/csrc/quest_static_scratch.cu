@@ -11,7 +11,6 @@
 // the query and the output buffers; nothing here calls cudaMalloc, cudaFree or any other
 // routine that allocates.
 #include <cstdio>
-#include <mutex>
 
 #include "quest_internal.h"
 
@@ -23,26 +22,15 @@ constexpr size_t kStaticScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 // In host code `g_static_scratch` names a host-side stand-in, not device memory: its
-// device address must be looked up, once per device, with that device current.
-constexpr int kMaxDevices = 64;
-std::mutex g_lookup_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
+// device address (on the current device) is looked up on every call, so that a context
+// torn down and rebuilt (which reloads the module) never leaves a stale address behind.
+// The lookup is not a stream operation and costs well under a microsecond.
 int scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return quest::set_last_error(QUEST_ERR_CUDA, cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices)
-    return quest::set_last_error(QUEST_ERR_UNSUPPORTED, "device ordinal beyond 63");
-  std::lock_guard<std::mutex> lock(g_lookup_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess || !p)
-      return quest::set_last_error(QUEST_ERR_CUDA, "cudaGetSymbolAddress(static scratch) failed");
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess || !p)
+    return quest::set_last_error(QUEST_ERR_CUDA, "cudaGetSymbolAddress(static scratch) failed");
+  *out = p;
   return QUEST_OK;
 }
 
@@ -54,7 +42,14 @@ extern "C" int quest_decode_static(const quest_cache_t* cache, const void* q, in
   size_t need = 0, zeroed = 0;
   int rc = quest::decode_workspace_requirement(cache, top_k, &need, &zeroed);
   if (rc) return rc;
-  if (cache->batch == 0) return QUEST_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cache->batch == 0) {  // nothing to do: the status reads OK, as after any good call
+    if (status_out) {
+      const cudaError_t e = cudaMemsetAsync(status_out, 0, 4 * sizeof(int32_t), s);
+      if (e != cudaSuccess) return quest::set_last_error(QUEST_ERR_CUDA, cudaGetErrorString(e));
+    }
+    return QUEST_OK;
+  }
   if (need > kStaticScratchBytes) {
     char msg[160];
     snprintf(msg, sizeof(msg),
@@ -64,7 +59,6 @@ extern "C" int quest_decode_static(const quest_cache_t* cache, const void* q, in
   }
   void* ws = nullptr;
   if ((rc = scratch_address(&ws))) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The array keeps whatever the previous call left: clear the status word, the work
   // queue, the counters and the selection flags before this call uses them.
   cudaError_t e = cudaMemsetAsync(ws, 0, zeroed, s);

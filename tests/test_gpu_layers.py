@@ -88,36 +88,86 @@ def test_layers_match_oracle_and_single_calls(append, path):
     H.assert_status_ok(ws)
 
 
-@pytest.mark.parametrize("path", [q.QUEST_PATH_AUTO, q.QUEST_PATH_FUSED], ids=["auto", "fused"])
-def test_layers_of_the_128k_model(path):
-    """Four layers of the 128K-context shape (8192 pages per head), through the automatic
-    choice (the layers as separate kernels here) and in one launch; every head's needle
-    page must be in the oracle's selection and the outputs must match."""
-    n = 4
-    ws_ = [wl.yarn_128k_layer(layer, seed=0, device="cuda", budget=2048) for layer in range(n)]
-    w0 = ws_[0]
-    K = w0.top_k
+def _on_block_table(w, bt0):
+    """w's pools laid out under the block table bt0: logical page p of sequence b goes to
+    physical page bt0[b, p] (the layers of a model share one block table; each layer's
+    workload draws its own)."""
+    src, dst = w.block_table.long(), bt0.long()
+    m = (src >= 0) & (dst >= 0)
+    k = torch.zeros_like(w.k_pool)
+    v = torch.zeros_like(w.v_pool)
+    k[dst[m]] = w.k_pool[src[m]]
+    v[dst[m]] = w.v_pool[src[m]]
+    return k, v
+
+
+N_LAYERS_128K = 32
+BUDGETS_128K = (1024, 2048)
+
+
+@pytest.fixture(scope="module")
+def model_128k():
+    """The 32 layers of the 128K-context model (1 sequence of 131 072 tokens, 32 MHA heads,
+    8192 pages of 16 per head, one needle page per head and layer) on one shared block table,
+    with the oracle's selection and attention of every layer at both budgets."""
     dev = torch.device("cuda")
-    base = q.PagedCache.allocate_meta(w0.k_pool, w0.v_pool, w0.block_table, w0.seq_lens.clone(),
-                                      w0.num_q_heads)
-    layers = [base] + [q.PagedCache.allocate_meta(w.k_pool, w.v_pool, base.block_table,
-                                                   base.seq_lens, w.num_q_heads)
-                       for w in ws_[1:]]
-    ws = q.workspace(base, K)
+    w0 = wl.yarn_128k_layer(0, seed=0, device="cuda", budget=2048)
+    bt0, sl0 = w0.block_table, w0.seq_lens
+    Hq = w0.num_q_heads
+    base = q.PagedCache.allocate_meta(w0.k_pool, w0.v_pool, bt0, sl0.clone(), Hq)
+    layers, qs, needles = [base], [w0.q[0]], [w0.needles]
+    for i in range(1, N_LAYERS_128K):
+        w = wl.yarn_128k_layer(i, seed=0, device="cuda", budget=2048)
+        k, v = _on_block_table(w, bt0)
+        layers.append(q.PagedCache.allocate_meta(k, v, base.block_table, base.seq_lens, Hq))
+        qs.append(w.q[0])
+        needles.append(w.needles)
+        del w, k, v
+    ws = {b: q.workspace(base, b // 16) for b in BUDGETS_128K}
     for lay in layers:
-        q.build_meta(lay, ws)
-    qs = [w.q[0] for w in ws_]
-    outs, lses = q.decode_layers(base, layers, qs, K, ws, q.opts(path=path))
+        q.build_meta(lay, ws[BUDGETS_128K[0]])
+    torch.cuda.synchronize()
+    bt, sl = bt0.cpu().numpy(), sl0.cpu().numpy()
+    ref = {}
+    for i, lay in enumerate(layers):
+        r = oracle.Cache.from_arrays(lay.k_pool.cpu().numpy(), lay.v_pool.cpu().numpy(), bt, sl,
+                                     Hq)
+        oracle.build_meta(r)
+        qh = qs[i].cpu().numpy().astype(np.float32)
+        rs = oracle.score(r, qh)
+        for budget in BUDGETS_128K:
+            ri, rc = oracle.topk(r, rs, budget // 16)
+            for (b, g, p, slot) in needles[i]:  # the workload plants what the method must find
+                assert p in ri[b, g, :rc[b, g]].tolist(), ("oracle misses a needle", i, g)
+            ref[(i, budget)] = oracle.attend(r, qh, ri, rc)
+        del r
+    return dict(base=base, layers=layers, qs=qs, needles=needles, ws=ws, ref=ref, dev=dev)
+
+
+@pytest.mark.parametrize("budget", BUDGETS_128K)
+@pytest.mark.parametrize("path", [q.QUEST_PATH_AUTO, q.QUEST_PATH_FUSED], ids=["auto", "fused"])
+def test_layers_of_the_128k_model(model_128k, path, budget):
+    """All 32 layers of the 128K-context model in one quest_decode_layers call (1024
+    (layer, kv head) pairs), through the automatic choice and in one launch of the cluster
+    kernel (more pairs than resident clusters: every cluster loops over pairs).  Every
+    layer's outputs must match the oracle's attention over the oracle's selection, and in
+    every layer every head's needle page must be among the pages the GPU selects: the
+    selection is read from a single-layer quest_decode of the same layer (its scores and
+    top-K are the same arithmetic as the multi-layer call's; the outputs of the two agree)."""
+    m = model_128k
+    base, layers, qs, ws = m["base"], m["layers"], m["qs"], m["ws"][budget]
+    K = budget // 16
+    o = q.opts(path=path)
+    outs, lses = q.decode_layers(base, layers, qs, K, ws, o)
     H.assert_status_ok(ws)
-    bt = w0.block_table.cpu().numpy()
-    sl = w0.seq_lens.cpu().numpy()
-    for i, w in enumerate(ws_):
-        ref = oracle.Cache.from_arrays(w.k_pool.cpu().numpy(), w.v_pool.cpu().numpy(), bt, sl,
-                                       w.num_q_heads)
-        oracle.build_meta(ref)
-        qh = w.q[0].cpu().numpy().astype(np.float32)
-        rs = oracle.score(ref, qh)
-        ri, rc = oracle.topk(ref, rs, K)
-        out_ref, lse_ref = oracle.attend(ref, qh, ri, rc)
+    idx = torch.empty((1, 32, K), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((1, 32), dtype=torch.int32, device="cuda")
+    for i, lay in enumerate(layers):
+        out_ref, lse_ref = m["ref"][(i, budget)]
         H.assert_attention_close(outs[i], lses[i], out_ref, lse_ref)
-        del ref
+        one, one_lse = q.decode(lay, qs[i], K, ws, o, idx_out=idx, count_out=cnt)
+        gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+        for (b, g, p, slot) in m["needles"][i]:
+            assert p in gi[b, g, :gc[b, g]].tolist(), ("needle page not selected", i, g, p)
+        torch.testing.assert_close(one.float(), outs[i].float(), atol=2e-3, rtol=0)
+    H.assert_status_ok(ws)

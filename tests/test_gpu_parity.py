@@ -693,3 +693,32 @@ def test_decode_plan_matches_calls(path):
     assert torch.equal(a.cache.seq_lens, b.cache.seq_lens)
     with pytest.raises(ValueError):
         plan.decode(torch.zeros((3, 4, 128), dtype=torch.float16, device="cuda"))
+
+
+@pytest.mark.parametrize("cs", [1, 2])
+@pytest.mark.parametrize("ctas", [1, 3])
+def test_cluster_pair_loop_with_few_clusters(cs, ctas):
+    """The one-launch cluster kernel is persistent over pairs.  With max_ctas capping the
+    grid at 1 or 3 clusters of 1 or 2 CTAs, the 12 (sequence, kv head) pairs run through
+    each cluster's pair loop: two appending steps match the oracle (selection, attention,
+    and on the last step boxes, rows and lengths), and the capped launch gives the same
+    selections and outputs, bit for bit, as the uncapped one."""
+    w = small(lens=(3000, 700, 1), batch=3, hq=8, hkv=4, budget=256, outliers=4, steps=2)
+    a, b = H.on_device(w), H.on_device(w)
+    o_cap = q.opts(path=q.QUEST_PATH_FUSED, cluster_size=cs, max_ctas=ctas)
+    o_all = q.opts(path=q.QUEST_PATH_FUSED, cluster_size=cs)
+    for t in range(w.steps):
+        H.run_step_and_compare(a, t, w.top_k, opts=o_cap, one_launch=True,
+                               check_cache=(t == w.steps - 1))
+        H.run_step_and_compare(b, t, w.top_k, opts=o_all, one_launch=True)
+    assert torch.equal(a.cache.meta, b.cache.meta)
+    assert torch.equal(a.cache.seq_lens, b.cache.seq_lens)
+    qd = w.q[0].cuda()
+    ia = torch.empty((3, 4, w.top_k), dtype=torch.int32, device="cuda")
+    ca = torch.empty((3, 4), dtype=torch.int32, device="cuda")
+    ib, cb = torch.empty_like(ia), torch.empty_like(ca)
+    oa, la = q.decode(a.cache, qd, w.top_k, a.ws, o_cap, idx_out=ia, count_out=ca)
+    ob, lb = q.decode(b.cache, qd, w.top_k, b.ws, o_all, idx_out=ib, count_out=cb)
+    H.assert_status_ok(a.ws)
+    assert torch.equal(ia, ib) and torch.equal(ca, cb)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
