@@ -568,8 +568,10 @@ def run_quest(args):
                    "replicas": world},
         "gbs": round(replicas.job_bytes_per_second(step_bytes, world, mean_step * 1e-6) / 1e9, 1),
         "roofline": {"bound": "hbm",
-                     "kernel": {"chain": "quest_decode, chain: estimate_kernel + topk_kernel + "
-                                         "decode_kernel",
+                     "kernel": {"chain": "quest_decode, chain: estimate_kernel + " +
+                                         ("decode_kernel (top-K in every decode work item)"
+                                          if q.decode_launches(cache, K, opts_main) == 2 else
+                                          "topk_kernel + decode_kernel"),
                                 "fused": "quest_decode, one launch: cluster_kernel",
                                 "stream": "quest_decode, one launch: stream_kernel"}[taken],
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -579,7 +581,7 @@ def run_quest(args):
                      "traffic": traffic},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": n * (3 if taken == "chain" else 1),
+        "gpu_launches": n * q.decode_launches(cache, K, opts_main),
         "clocks": clk.summary(),
         "detail_us": {"step_mean": round(mean_step, 3),
                       "step_l2_flushed_mean": round(sum(fl) / len(fl), 3),
@@ -676,6 +678,16 @@ def run_sweep(args):
         # the library's own choice between the one-launch kernel and the chain
         auto_us = timed(lambda: q.decode(cache, qv, K, ws, None, out=out, lse=lse, idx_out=idx,
                                          count_out=cnt), reps)
+        # the chain forced, and the stream kernel where its shape fits
+        oc = q.opts(path=q.QUEST_PATH_CHAIN)
+        chain_path_us = timed(lambda: q.decode(cache, qv, K, ws, oc, out=out, lse=lse), reps)
+        os_ = q.opts(path=q.QUEST_PATH_STREAM)
+        try:
+            q.decode_path(cache, K, os_)
+            stream_us = round(timed(lambda: q.decode(cache, qv, K, ws, os_, out=out, lse=lse),
+                                    reps), 2)
+        except q.QuestError:
+            stream_us = None
         L = [int(x) for x in cache.seq_lens.cpu().tolist()]
         tok = selected_tokens(idx, cnt, L, P)
         nbytes = decode_bytes(L, tok, B, Hq, Hkv, page=P)
@@ -725,6 +737,7 @@ def run_sweep(args):
             "num_kv_heads": Hkv,
             "page_size": P, "top_k_pages": K, "seq_lens_mean": round(sum(L) / len(L), 1),
             "quest_decode_us": round(fused, 2), "quest_decode_auto_us": round(auto_us, 2),
+            "quest_decode_chain_us": round(chain_path_us, 2), "quest_decode_stream_us": stream_us,
             "algorithmic_bytes": nbytes,
             "gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
             "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),

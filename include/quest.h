@@ -137,17 +137,21 @@ typedef struct quest_opts {
                                  pages; the fused calls answer QUEST_ERR_UNSUPPORTED.        */
     int32_t path;             /* quest_decode*: QUEST_PATH_* (quest_decode_layers: see there).
                                  The chain
-                                 computes the same step as separate estimate, top-K and
-                                 sparse-decode kernels; the estimate writes the new token's
-                                 row and box as it scores that page, and the sparse decode
-                                 advances the lengths at its end (selection kept in the
-                                 workspace unless idx_out / count_out are given).           */
+                                 computes the same step as separate kernels: estimate, top-K
+                                 and sparse decode, or, when the decode's work items fit on
+                                 the GPU about twice over, estimate and a sparse decode whose
+                                 work items each take their pair's top-K; the estimate writes
+                                 the new token's row and box as it scores that page, and the
+                                 sparse decode advances the lengths at its end (selection
+                                 kept in the workspace unless idx_out / count_out are
+                                 given).                                                     */
 } quest_opts_t;
 
 /* Values of quest_opts_t.path.
  *   FUSED  : one launch of the cluster kernel, a thread-block cluster per (sequence, kv
  *            head) pair.
- *   CHAIN  : separate estimate, top-K and sparse-decode kernels, back to back.
+ *   CHAIN  : separate estimate, top-K and sparse-decode kernels, back to back (with few
+ *            pairs the top-K runs inside the sparse decode's work items instead).
  *   STREAM : one persistent launch of the stream kernel, one CTA per SM, every CTA working
  *            on every pair: pairs are scored in order over the whole GPU, each pair is
  *            selected as soon as its last page is scored while later pairs still stream,
@@ -172,6 +176,12 @@ typedef struct quest_opts {
  * for the one-launch kernel; launches nothing. */
 int quest_decode_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
                       int32_t n_layers);
+
+/* Kernel launches of one quest_decode or quest_decode_step call for this cache, top_k and
+ * opts: 1 on the one-launch paths; on the chain 3 (estimate, top-K, sparse decode), or 2
+ * when the sparse decode's work items take the top-K themselves (few pairs: see
+ * QUEST_PATH_CHAIN).  Minus a QUEST_ERR_* status on invalid arguments; launches nothing. */
+int quest_decode_launches(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts);
 
 /* quest_decode only (one-launch paths): never publish the selection, so that every
  * decode work item's bounded wait runs out and the call reports QUEST_ERR_TIMEOUT.  For

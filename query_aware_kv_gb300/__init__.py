@@ -10,7 +10,7 @@ from ._lib import (  # noqa: F401
     QUEST_ERR_TIMEOUT, QUEST_ERR_UNSUPPORTED, QUEST_ERR_WORKSPACE, QUEST_MAX_PAGES, QUEST_OK,
     QUEST_PATH_AUTO, QUEST_PATH_CHAIN, QUEST_PATH_FUSED, QUEST_PATH_STREAM,
     DecodePlan, PagedCache, QuestCacheDesc, QuestError, QuestLayer, QuestOpts, append, build_meta, decode,
-    decode_layers, decode_path, decode_step,
+    decode_launches, decode_layers, decode_path, decode_step,
     dense_decode, estimate, estimate_heads, load, opts, prefill, read_status, sparse_decode, topk, workspace,
     workspace_init, workspace_size,
 )

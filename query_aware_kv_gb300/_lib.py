@@ -39,7 +39,7 @@ EXPORTS = (
     "quest_workspace_size", "quest_workspace_init", "quest_build_meta", "quest_append",
     "quest_prefill",
     "quest_estimate", "quest_estimate_heads", "quest_topk", "quest_sparse_decode",
-    "quest_decode", "quest_decode_layers", "quest_decode_path",
+    "quest_decode", "quest_decode_layers", "quest_decode_path", "quest_decode_launches",
     "quest_decode_step", "quest_dense_decode", "quest_decode_static", "quest_read_status",
     "quest_last_error", "quest_status_string", "quest_version",
 )
@@ -112,6 +112,7 @@ def load() -> ctypes.CDLL:
             "quest_decode_layers": (ctypes.c_int, [C, ctypes.POINTER(QuestLayer), I32, I32, V,
                                                    SZ, O, V]),
             "quest_decode_path": (ctypes.c_int, [C, I32, O, I32]),
+            "quest_decode_launches": (ctypes.c_int, [C, I32, O]),
             "quest_dense_decode": (ctypes.c_int, [C, V, V, V, V, SZ, O, V]),
             "quest_read_status": (ctypes.c_int, [V, SZ, V, ctypes.POINTER(I32)]),
             "quest_last_error": (ctypes.c_char_p, []),
@@ -498,6 +499,15 @@ def decode_path(cache: PagedCache, top_k: int, o: Optional[QuestOpts] = None,
     top_k and options."""
     lib = load()
     r = lib.quest_decode_path(ctypes.byref(cache.desc), int(top_k), _opts_ref(o), int(n_layers))
+    if r < 0:
+        raise QuestError(-r, lib.quest_last_error().decode())
+    return int(r)
+
+
+def decode_launches(cache: PagedCache, top_k: int, o: Optional[QuestOpts] = None) -> int:
+    """Kernel launches of one decode / decode_step call for this cache, top_k and options."""
+    lib = load()
+    r = lib.quest_decode_launches(ctypes.byref(cache.desc), int(top_k), _opts_ref(o))
     if r < 0:
         raise QuestError(-r, lib.quest_last_error().decode())
     return int(r)

@@ -395,6 +395,26 @@ static cudaError_t auto_path_fused(int G, int P, int max_pages, int top_k, int n
   return cudaSuccess;
 }
 
+// Where a chain decode call selects its pages.  While the decode kernel's work items fit on
+// the GPU about twice over, every work item takes its pair's top-K itself (the redundant
+// selections run on SMs that would otherwise idle, and the top-K kernel, its launch and the
+// selection's round trip through global memory drop out of the step); with more work items
+// the top-K kernel selects once per pair and also resolves every kept page's physical page
+// for the decode kernel.
+static void set_chain_selection(Params& p) {
+  static std::mutex mu;
+  static int sms[64] = {};
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!sms[dev & 63]) cudaDeviceGetAttribute(&sms[dev & 63], cudaDevAttrMultiProcessorCount, dev);
+    n = sms[dev & 63];
+  }
+  const long long items = (long long)p.B * p.Hkv * p.n_splits;
+  p.chain_select = (n > 0 && items <= 2LL * n) ? 1 : 0;
+  p.chain_pairs = 1 - p.chain_select;
+}
+
 // The path of a decode call (QUEST_PATH_FUSED, _CHAIN or _STREAM in quest.h).
 static int decide_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
                        int n_layers, int* path_out) {
@@ -480,11 +500,13 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   }
   if (path == QUEST_PATH_CHAIN) {
     // the same step as separate kernels: estimate (which also writes the new token's row
-    // and widens its box), top-K, sparse decode (which advances the lengths at its end);
-    // the selection goes to idx_out / count_out if given, else to the workspace
+    // and widens its box), top-K (its own kernel, or inside every decode work item: see
+    // set_chain_selection), sparse decode (which advances the lengths at its end); the
+    // selection goes to idx_out / count_out if given, else to the workspace
     p.chain_append = p.k_new != nullptr ? 1 : 0;
+    set_chain_selection(p);
     cudaError_t e = launch_estimate(p, G, false, s);
-    if (e == cudaSuccess) e = launch_topk(p, s);
+    if (e == cudaSuccess && !p.chain_select) e = launch_topk(p, s);
     if (e == cudaSuccess) e = launch_decode(p, G, s);
     return launched(e, what);
   }
@@ -500,6 +522,22 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   lt.n = 1;
   lt.l[0] = LayerPtrs{p.k_pool, p.v_pool, p.meta, p.q, p.k_new, p.v_new, p.out, p.lse};
   return launched(launch_cluster(p, lt, G, cs, opts ? opts->max_ctas : 0, s), what);
+}
+
+int quest_decode_launches(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts) {
+  int rc = check_cache(cache);
+  if (rc) return -rc;
+  if ((rc = check_topk(top_k))) return -rc;
+  int path = QUEST_PATH_FUSED;
+  if ((rc = decide_path(cache, top_k, opts, 1, &path))) return -rc;
+  if (path != QUEST_PATH_CHAIN) return 1;
+  const Tiling t = make_tiling(cache, top_k, opts);
+  Params p{};
+  p.B = cache->batch;
+  p.Hkv = cache->num_kv_heads;
+  p.n_splits = t.n_splits_sparse;
+  set_chain_selection(p);
+  return p.chain_select ? 2 : 3;
 }
 
 int quest_decode_path(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts,
@@ -620,6 +658,7 @@ int quest_decode_layers(const quest_cache_t* cache, const quest_layer_t* layers,
     c.pps = t.pps_sparse;
     c.n_splits = t.n_splits_sparse;
     c.dense = 0;
+    set_chain_selection(c);
     auto at = [&](int i) {
       Params l = c;
       l.k_pool = lt.l[i].k_pool;
@@ -639,7 +678,7 @@ int quest_decode_layers(const quest_cache_t* cache, const quest_layer_t* layers,
     for (int i = 0; i < n_layers && e == cudaSuccess; ++i) {
       const Params l = at(i);
       e = launch_estimate(l, G, false, s);
-      if (e == cudaSuccess) e = launch_topk(l, s);
+      if (e == cudaSuccess && !l.chain_select) e = launch_topk(l, s);
       if (e == cudaSuccess) e = launch_decode(l, G, s);
     }
     return launched(e, "quest_decode_layers");

@@ -167,13 +167,22 @@ static __device__ __noinline__ void report(const Params& p, int code, int b, int
 }
 
 // Tokens present in sequence b, or 0 (and a report) if seq_lens[b] is out of range.
-__device__ __forceinline__ int load_len(const Params& p, int b, int site) {
-  const int L = p.seq_lens[b];
+__device__ __forceinline__ int check_len(const Params& p, int b, int L, int site) {
   if (L < 0 || (long long)L > (long long)p.max_pages * p.P) {
     report(p, QUEST_ERR_BAD_LENGTH, b, -1, site);
     return 0;
   }
   return L;
+}
+__device__ __forceinline__ int load_len(const Params& p, int b, int site) {
+  return check_len(p, b, p.seq_lens[b], site);
+}
+// The step's length of sequence b from its stored length L0 (already loaded): with an
+// appending chain step the new token counts if the sequence has room for it.
+__device__ __forceinline__ int step_len(const Params& p, int b, int L0, int site) {
+  const int L = check_len(p, b, L0, site);
+  const bool app = p.chain_append && (long long)L + 1 <= (long long)p.max_pages * p.P && L == L0;
+  return app ? L + 1 : L;
 }
 
 // load_len for the kernels of a chain step: when the step appends (p.chain_append), the new
@@ -470,6 +479,12 @@ __host__ __device__ inline size_t topk_smem_bytes(int max_pages) {
   return align_up((size_t)max_pages * 4, 16) + (size_t)kFastBins * 4;
 }
 
+// Ints of the decode ring's region that a selection inside the decode kernel needs: its
+// keys and histogram, then 256 ints of scratch.
+__host__ __device__ inline int select_ring_ints(int max_pages) {
+  return (int)((topk_smem_bytes(max_pages) + 256 * 4) / 4);
+}
+
 __device__ inline TopkSmem topk_smem_at(unsigned char* base, int max_pages) {
   TopkSmem t;
   t.keys = reinterpret_cast<uint32_t*>(base);
@@ -620,7 +635,7 @@ __device__ void topk_fast(const uint32_t* keys, int N, int K, uint32_t lo, uint3
   }
   // kept: (d >> top) > pref; tied: == pref, the `need` lowest indices of them (all if whole).
   // Thread t takes indices [t*R, t*R + R) (R odd, so that a warp's 32 runs fall in 32
-  // different shared-memory banks): it counts its kept and tied keys, two block scans give
+  // different shared-memory banks): it counts its kept and tied keys, one block scan gives
   // its place in the output and its share of the ties, and a second look at its run writes
   // them out in ascending order.  Short loops, no unrolling: this runs once per selection
   // and its code is fetched cold.
@@ -634,11 +649,12 @@ __device__ void topk_fast(const uint32_t* keys, int N, int K, uint32_t lo, uint3
     nk += h > pref;
     nt += h == pref;
   }
-  // packed counts: both are below 2^16 (N < 65536)
+  // packed counts: both are below 2^16 (N < 65536).  Ties are taken in index order, so the
+  // threads before this one took min(their ties, need) of them: one scan places everything.
   const int pre = block_excl_sum<NT, kNamed>((nk << 16) | nt, scratch);
   const int tie_before = pre & 0xffff;
   int take = whole ? nt : max(0, min(nt, need - tie_before));
-  int pos = block_excl_sum<NT, kNamed>(nk + take, scratch + NW);
+  int pos = (pre >> 16) + (whole ? tie_before : min(tie_before, need));
 #pragma unroll 1
   for (int i = i0; i < i1; ++i) {
     const uint32_t h = (keys[i] - lo) >> tsh;
@@ -874,11 +890,19 @@ __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap&
       const int r = base + lane;
       int nv = 0, phys = 0;
       if (r < n_tile) {
-        const int lp = sel_row ? __ldcg(sel_row + r0 + r) : r0 + r;
+        int lp;
+        if (p.chain_pairs) {  // the top-K kernel resolved the physical page already
+          const int2 e = __ldcg(reinterpret_cast<const int2*>(p.sel_pair) +
+                                ((size_t)b * p.Hkv + g) * p.top_k + r0 + r);
+          lp = e.x;
+          phys = e.y;
+        } else {
+          lp = sel_row ? sel_row[r0 + r] : r0 + r;  // (global, or this CTA's shared memory)
+        }
         if (lp < 0 || lp >= N_b) {
           report(p, QUEST_ERR_BAD_SELECTION, b, lp, kSiteSelection);
         } else {
-          phys = p.block_table[(size_t)b * p.max_pages + lp];
+          if (!p.chain_pairs) phys = p.block_table[(size_t)b * p.max_pages + lp];
           if (phys < 0 || phys >= p.num_phys) {
             report(p, QUEST_ERR_BAD_PAGE, b, lp, kSiteDecode);
             phys = 0;

@@ -97,7 +97,9 @@ struct Params {
   int chain_append;      // chain and stream kernel: the step appends k_new; every kernel
                          // sees seq_lens + 1 (when there is room) and the last step of the
                          // call advances seq_lens
-  int* sel_pair;         // stream kernel: [B][Hkv][top_k] (logical page, physical page)
+  int* sel_pair;         // stream kernel and chain: [B][Hkv][top_k] (logical, physical page)
+  int chain_pairs;       // chain: topk_kernel also writes sel_pair, decode_kernel reads it
+  int chain_select;      // chain: every decode work item takes its pair's top-K itself
   unsigned* skeys;       // stream kernel: [B][Hkv][max_pages] page keys, 0 until written
   unsigned* started;     // stream kernel: CTAs that have read the lengths
   int hold_lengths;      // stream kernel: append, but leave seq_lens to a later launch

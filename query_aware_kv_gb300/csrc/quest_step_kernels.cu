@@ -76,16 +76,43 @@ __global__ void __launch_bounds__(kConsumerThreads) estimate_kernel(Params p) {
 // per scheduler to hide each other's waits.
 constexpr int kTopkThreads = 512;
 
+// chain_pairs (a chain decode call): the kept pages also go out with their physical pages
+// ((logical, physical) in sel_pair, physical -1 if unmapped), so that the decode kernel
+// starts its copies one dependent load earlier; the block table row is read into shared
+// memory alongside the length and the scores.  Dynamic smem: topk_smem_bytes(max_pages)
+// + 256 ints, + max_pages + top_k ints with chain_pairs.
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(Params p) {
   extern __shared__ __align__(16) unsigned char sm[];
   pdl_wait();
   const int bg = blockIdx.x, b = bg / p.Hkv;
-  const int L = load_len_step(p, b, kSiteTopk);
+  const int tid = threadIdx.x;
+  int* scratch = reinterpret_cast<int*>(sm + topk_smem_bytes(p.max_pages));  // [256]
+  int* bt_s = scratch + 256;                                                  // [max_pages]
+  int* sel_s = bt_s + p.max_pages;                                            // [top_k]
+  const int L0 = p.seq_lens[b];
+  if (p.chain_pairs)
+    for (int i = tid; i < p.max_pages; i += kTopkThreads)
+      bt_s[i] = p.block_table[(size_t)b * p.max_pages + i];
+  const int L = step_len(p, b, L0, kSiteTopk);
   const int N = (L + p.P - 1) / p.P;
-  int* scratch = reinterpret_cast<int*>(sm + topk_smem_bytes(p.max_pages));
+  int* idx_g = p.sel_idx + (size_t)bg * p.top_k;
   topk_row<kTopkThreads, false>(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
-                                    p.sink_pages, p.local_pages, p.sel_idx + (size_t)bg * p.top_k, p.sel_count + bg,
-                                    topk_smem_at(sm, p.max_pages), scratch);
+                                p.sink_pages, p.local_pages, p.chain_pairs ? sel_s : idx_g,
+                                p.sel_count + bg, topk_smem_at(sm, p.max_pages), scratch);
+  if (p.chain_pairs) {
+    __syncthreads();  // the selection and the block table row are in shared memory
+    int2* pr = reinterpret_cast<int2*>(p.sel_pair) + (size_t)bg * p.top_k;
+    for (int r = tid; r < p.top_k; r += kTopkThreads) {
+      const int lp = sel_s[r];
+      int ph = -1;
+      if (lp >= 0 && lp < N) {
+        ph = bt_s[lp];
+        if (ph < 0 || ph >= p.num_phys) ph = -1;
+      }
+      idx_g[r] = lp;
+      pr[r] = make_int2(lp, ph);
+    }
+  }
 }
 
 // Group-level selection, union form ("Guide to Quest", Best Practices step 2): each query
@@ -150,17 +177,40 @@ __global__ void __launch_bounds__(kConsumerThreads) topk_union_kernel(Params p, 
 template <int G, int P>
 __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const SmemMap m = make_smem_map(G, P, 0, 0);
+  const SmemMap m = make_smem_map(G, P, p.chain_select ? select_ring_ints(p.max_pages) : 0, 0);
   init_ring(smem, m);
   pdl_wait();
   const int split = blockIdx.x, bg = blockIdx.y;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
-  const int L = load_len_step(p, b, kSiteDecode);
+  // the length and the selection's count are independent: both loads go out together
+  const int L0 = p.seq_lens[b];
+  const int c0 = (p.dense || p.chain_select) ? 0 : p.sel_count[bg];
+  const int L = step_len(p, b, L0, kSiteDecode);
   const int N = (L + P - 1) / P;
   int count = N;
   const int* sel_row = nullptr;
-  if (!p.dense) {
-    count = p.sel_count[bg];
+  if (p.chain_select) {
+    // A chain step without a top-K kernel: every work item of the pair takes the pair's
+    // top-K over the scores itself (the same arithmetic, so the same pages in every one),
+    // in the ring's space before the ring is used, and keeps the kept pages in shared
+    // memory; work item 0 also writes the caller's copy.
+    int* sel_s = reinterpret_cast<int*>(smem + m.total);  // [top_k]
+    int* cnt_s = reinterpret_cast<int*>(smem + m.misc) + 8;
+    unsigned char* ring = smem + m.ring;
+    topk_row<kDecodeThreads, false>(p.scores + (size_t)bg * p.max_pages, N, p.top_k,
+                                    p.sink_pages, p.local_pages, sel_s, cnt_s,
+                                    topk_smem_at(ring, p.max_pages),
+                                    reinterpret_cast<int*>(ring + topk_smem_bytes(p.max_pages)));
+    __syncthreads();
+    count = *cnt_s;
+    sel_row = sel_s;
+    if (split == 0) {
+      for (int r = threadIdx.x; r < p.top_k; r += kDecodeThreads)
+        p.sel_idx[(size_t)bg * p.top_k + r] = sel_s[r];
+      if (threadIdx.x == 0) p.sel_count[bg] = count;
+    }
+  } else if (!p.dense) {
+    count = c0;
     const int cap = min(p.top_k, N);
     if (count < 0 || count > cap) {
       if (threadIdx.x == 0 && split == 0) report(p, QUEST_ERR_BAD_SELECTION, b, count, kSiteSelection);
@@ -253,7 +303,8 @@ cudaError_t launch_topk_union(const Params& p, int row_cap, cudaStream_t s) {
 
 cudaError_t launch_topk(const Params& p, cudaStream_t s) {
   const void* fn = (const void*)topk_kernel;
-  const size_t smem = topk_smem_bytes(p.max_pages) + 256 * 4;
+  const size_t smem = topk_smem_bytes(p.max_pages) + 256 * 4 +
+                      (p.chain_pairs ? ((size_t)p.max_pages + p.top_k) * 4 : 0);
   cudaError_t e = ensure_smem(fn, smem);
   if (e != cudaSuccess) return e;
   Params pp = p;
@@ -263,7 +314,9 @@ cudaError_t launch_topk(const Params& p, cudaStream_t s) {
 
 cudaError_t launch_decode(const Params& p, int G, cudaStream_t s) {
   const void* fn = pick_decode(G, p.P);
-  const size_t smem = decode_smem_bytes(G, p.P, 0, 0);
+  const size_t smem = p.chain_select ? decode_smem_bytes(G, p.P, select_ring_ints(p.max_pages), 0) +
+                                           align_up((size_t)p.top_k * 4, 16)
+                                     : decode_smem_bytes(G, p.P, 0, 0);
   cudaError_t e = ensure_smem(fn, smem);
   if (e != cudaSuccess) return e;
   Params pp = p;

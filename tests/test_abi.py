@@ -217,3 +217,16 @@ def test_binding_constants_match_the_header():
     for name in mirrored:
         assert name in defines, name
         assert int(defines[name]) == getattr(q, name), name
+
+
+def test_decode_launches_without_a_device_query(lib):
+    """One launch on the one-launch paths (asked for: no device query); bad arguments are
+    refused as by quest_decode_path."""
+    d = desc()
+    for path in (q.QUEST_PATH_STREAM, q.QUEST_PATH_FUSED):
+        o = q.opts(path=path)
+        assert lib.quest_decode_launches(ctypes.byref(d), 16, ctypes.byref(o)) == 1
+    assert lib.quest_decode_launches(ctypes.byref(d), 0, None) == -q.QUEST_ERR_INVALID_ARG
+    o = q.opts(path=7)
+    assert lib.quest_decode_launches(ctypes.byref(d), 16, ctypes.byref(o)) == \
+        -q.QUEST_ERR_INVALID_ARG

@@ -722,3 +722,16 @@ def test_cluster_pair_loop_with_few_clusters(cs, ctas):
     H.assert_status_ok(a.ws)
     assert torch.equal(ia, ib) and torch.equal(ca, cb)
     assert torch.equal(oa, ob) and torch.equal(la, lb)
+
+
+def test_chain_launch_count_follows_the_work_item_rule():
+    """On the chain, a call with few decode work items selects inside the sparse decode (two
+    launches), one with many keeps the top-K kernel (three); both match the oracle."""
+    few = small(lens=(3000, 700), batch=2, hq=8, hkv=4, budget=256, outliers=4, steps=1)
+    many = wl.build("many_pairs", batch=8, num_q_heads=64, num_kv_heads=64, page_size=16,
+                    prefill_lens=[2000 + 37 * i for i in range(8)], steps=1, budget=1024, seed=3)
+    o = q.opts(path=q.QUEST_PATH_CHAIN)
+    for w, launches in ((few, 2), (many, 3)):
+        pair = H.on_device(w)
+        assert q.decode_launches(pair.cache, w.top_k, o) == launches
+        H.run_step_and_compare(pair, 0, w.top_k, opts=o, one_launch=True, check_cache=True)
