@@ -138,9 +138,10 @@ typedef struct quest_opts {
     int32_t path;             /* quest_decode*: QUEST_PATH_* (quest_decode_layers: see there).
                                  The chain
                                  computes the same step as separate kernels: estimate, top-K
-                                 and sparse decode, or, when the decode's work items fit on
-                                 the GPU about twice over, estimate and a sparse decode whose
-                                 work items each take their pair's top-K; the estimate writes
+                                 and sparse decode, or, for MHA rows of at most 4096 pages
+                                 whose decode work items fit on the GPU about twice over,
+                                 estimate and a sparse decode whose work items each take
+                                 their pair's top-K; the estimate writes
                                  the new token's row and box as it scores that page, and the
                                  sparse decode advances the lengths at its end (selection
                                  kept in the workspace unless idx_out / count_out are
@@ -150,8 +151,8 @@ typedef struct quest_opts {
 /* Values of quest_opts_t.path.
  *   FUSED  : one launch of the cluster kernel, a thread-block cluster per (sequence, kv
  *            head) pair.
- *   CHAIN  : separate estimate, top-K and sparse-decode kernels, back to back (with few
- *            pairs the top-K runs inside the sparse decode's work items instead).
+ *   CHAIN  : separate estimate, top-K and sparse-decode kernels, back to back (for short
+ *            MHA rows with few pairs the top-K runs inside the sparse decode's work items).
  *   STREAM : one persistent launch of the stream kernel, one CTA per SM, every CTA working
  *            on every pair: pairs are scored in order over the whole GPU, each pair is
  *            selected as soon as its last page is scored while later pairs still stream,

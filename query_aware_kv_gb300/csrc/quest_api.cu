@@ -395,12 +395,16 @@ static cudaError_t auto_path_fused(int G, int P, int max_pages, int top_k, int n
   return cudaSuccess;
 }
 
-// Where a chain decode call selects its pages.  While the decode kernel's work items fit on
-// the GPU about twice over, every work item takes its pair's top-K itself (the redundant
-// selections run on SMs that would otherwise idle, and the top-K kernel, its launch and the
-// selection's round trip through global memory drop out of the step); with more work items
-// the top-K kernel selects once per pair and also resolves every kept page's physical page
-// for the decode kernel.
+// Where a chain decode call selects its pages.  For MHA rows of at most 4096 pages whose
+// decode work items fit on the GPU about twice over, every work item takes its pair's top-K
+// itself (the redundant selections run on SMs that would otherwise idle, and the top-K
+// kernel, its launch and the selection's round trip through global memory drop out of the
+// step); otherwise the top-K kernel selects once per pair, with 16 warps, and also resolves
+// every kept page's physical page for the decode kernel.  Measured on GB300 (quest_decode,
+// L2 flushed): 32K MHA 31.5 against 32.2 us, 8 ragged 8K-32K sequences at budget 256 54.0
+// against 56.4; but the 128K row (8192 pages) 54.1 against 50.9 and GQA-4 at page 32 62.8
+// against 60.7, where the longer selection or the heavier decode work item makes the
+// redundant top-K the longer path.
 static void set_chain_selection(Params& p) {
   static std::mutex mu;
   static int sms[64] = {};
@@ -411,7 +415,7 @@ static void set_chain_selection(Params& p) {
     n = sms[dev & 63];
   }
   const long long items = (long long)p.B * p.Hkv * p.n_splits;
-  p.chain_select = (n > 0 && items <= 2LL * n) ? 1 : 0;
+  p.chain_select = (n > 0 && items <= 2LL * n && p.Hq == p.Hkv && p.max_pages <= 4096) ? 1 : 0;
   p.chain_pairs = 1 - p.chain_select;
 }
 
@@ -534,7 +538,9 @@ int quest_decode_launches(const quest_cache_t* cache, int32_t top_k, const quest
   const Tiling t = make_tiling(cache, top_k, opts);
   Params p{};
   p.B = cache->batch;
+  p.Hq = cache->num_q_heads;
   p.Hkv = cache->num_kv_heads;
+  p.max_pages = cache->max_pages;
   p.n_splits = t.n_splits_sparse;
   set_chain_selection(p);
   return p.chain_select ? 2 : 3;

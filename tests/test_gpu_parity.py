@@ -725,13 +725,15 @@ def test_cluster_pair_loop_with_few_clusters(cs, ctas):
 
 
 def test_chain_launch_count_follows_the_work_item_rule():
-    """On the chain, a call with few decode work items selects inside the sparse decode (two
-    launches), one with many keeps the top-K kernel (three); both match the oracle."""
-    few = small(lens=(3000, 700), batch=2, hq=8, hkv=4, budget=256, outliers=4, steps=1)
+    """On the chain, a call on short MHA rows with few decode work items selects inside the
+    sparse decode (two launches); GQA, or many work items, keep the top-K kernel (three).
+    All match the oracle."""
+    few = small(lens=(3000, 700), batch=2, hq=4, hkv=4, budget=256, outliers=4, steps=1)
+    gqa = small(lens=(3000, 700), batch=2, hq=8, hkv=4, budget=256, outliers=4, steps=1)
     many = wl.build("many_pairs", batch=8, num_q_heads=64, num_kv_heads=64, page_size=16,
                     prefill_lens=[2000 + 37 * i for i in range(8)], steps=1, budget=1024, seed=3)
     o = q.opts(path=q.QUEST_PATH_CHAIN)
-    for w, launches in ((few, 2), (many, 3)):
+    for w, launches in ((few, 2), (gqa, 3), (many, 3)):
         pair = H.on_device(w)
         assert q.decode_launches(pair.cache, w.top_k, o) == launches
         H.run_step_and_compare(pair, 0, w.top_k, opts=o, one_launch=True, check_cache=True)
