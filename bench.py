@@ -256,6 +256,44 @@ def run_reference(args):
 # ------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------
+class _Driver:
+    """Asynchronous copies and event calls through the CUDA driver (libcuda), for the
+    end-to-end loop: plain cuMemcpyHtoDAsync / cuMemcpyDtoHAsync, one per copy."""
+
+    def __init__(self):
+        import ctypes
+        lib = ctypes.CDLL("libcuda.so.1")
+        V, SZ = ctypes.c_void_p, ctypes.c_size_t
+        U64 = ctypes.c_uint64
+        self._h2d = lib.cuMemcpyHtoDAsync_v2
+        self._h2d.argtypes = [U64, V, SZ, V]
+        self._d2h = lib.cuMemcpyDtoHAsync_v2
+        self._d2h.argtypes = [V, U64, SZ, V]
+        self._rec = lib.cuEventRecord
+        self._rec.argtypes = [V, V]
+        self._wait = lib.cuStreamWaitEvent
+        self._wait.argtypes = [V, V, ctypes.c_uint]
+        for f in (self._h2d, self._d2h, self._rec, self._wait):
+            f.restype = ctypes.c_int
+
+    @staticmethod
+    def _ok(rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what} failed with CUresult {rc}")
+
+    def h2d(self, dst, src, n, stream):
+        self._ok(self._h2d(dst, src, n, stream), "cuMemcpyHtoDAsync")
+
+    def d2h(self, dst, src, n, stream):
+        self._ok(self._d2h(dst, src, n, stream), "cuMemcpyDtoHAsync")
+
+    def record(self, event, stream):
+        self._ok(self._rec(event, stream), "cuEventRecord")
+
+    def wait(self, stream, event):
+        self._ok(self._wait(stream, event, 0), "cuStreamWaitEvent")
+
+
 def run_quest(args):
     import types
 
@@ -347,14 +385,14 @@ def run_quest(args):
         t = (i // ncopy) % steps_per_copy
         c.plan.step(c.qs[t], c.kns[t], c.vns[t])
 
-    host_issue = [0.0]  # host seconds spent issuing the timed calls (last timed_steps)
+    host_issue = [0.0, 0]  # host seconds spent issuing calls, and those calls (last timed_steps)
 
     def timed_steps(count, fn):
         """`count` calls of fn(i) back to back, in segments of at most `seg` calls (the copies
         are rewound between segments, outside the timed intervals).  Returns total ms."""
         total = 0.0
         done = 0
-        host_issue[0] = 0.0
+        host_issue[0], host_issue[1] = 0.0, 0
         while done < count:
             m = min(seg, count - done)
             rewind_all()
@@ -362,10 +400,16 @@ def run_quest(args):
             if world > 1:
                 dist.barrier()
             t0.record()
+            # host time to issue the first (up to) 128 calls of the segment: later calls can
+            # wait for room in the launch queue once the GPU falls behind
+            h_n = min(m, 128)
             h0 = time.perf_counter()
-            for i in range(m):
+            for i in range(h_n):
                 fn(i)
             host_issue[0] += time.perf_counter() - h0
+            host_issue[1] += h_n
+            for i in range(h_n, m):
+                fn(i)
             t1.record()
             torch.cuda.synchronize()
             if world > 1:
@@ -407,7 +451,7 @@ def run_quest(args):
         total_ms = timed_steps(n, step)
         wall = time.perf_counter() - wall0
     mean_step = 1e3 * total_ms / n
-    host_issue_us = 1e6 * host_issue[0] / n
+    host_issue_us = 1e6 * host_issue[0] / max(1, host_issue[1])
     for c in copies:
         rc, detail = q.read_status(c.ws)
         if rc != 0:
@@ -510,51 +554,61 @@ def run_quest(args):
 
     # ---- end to end through the public API with host buffers (pinned), copies timed: each
     # step's q, k_new and v_new travel in one host->device copy of a packed staging row, and
-    # out + lse come back in one device->host copy, both on a copy stream, double-buffered,
-    # so that step i's copies overlap steps i-1 / i+1's kernels as in a serving loop; back to
-    # back over the rotating copies
+    # out + lse come back in one device->host copy, each on a copy stream of its own,
+    # double-buffered, so that step i's copies overlap steps i-1 / i+1's kernels as in a
+    # serving loop; back to back over the rotating copies
     nq, nk = w.q[0].numel(), w.k_new[0].numel()
     hstage = [torch.cat([c.w.q.reshape(c.w.steps, -1), c.w.k_new.reshape(c.w.steps, -1),
                          c.w.v_new.reshape(c.w.steps, -1)], dim=1).cpu().pin_memory()
               for c in copies]
     hstage_rows = [[h[t] for t in range(steps_per_copy)] for h in hstage]
     out_bytes, lse_bytes = out.numel() * 2, lse.numel() * 4
-    cs = torch.cuda.Stream(device=dev)
+    cs = torch.cuda.Stream(device=dev)      # inputs in
+    cs_out = torch.cuda.Stream(device=dev)  # results out (a stream of its own, so that the
+                                            # next step's input never queues behind a result)
+    main = torch.cuda.current_stream()
+    cu = _Driver()  # the copies and event calls straight through the driver: a fraction of
+                    # the host time of torch's stream context and copy calls
+    main_h, cs_h, out_h = main.cuda_stream, cs.cuda_stream, cs_out.cuda_stream
     slots = []
     for _ in range(2):
         dstage = torch.empty(hstage[0].shape[1], dtype=torch.float16, device=dev)
         dres = torch.empty(out_bytes + lse_bytes, dtype=torch.uint8, device=dev)
         eout = dres[:out_bytes].view(torch.float16).view_as(out)
         else_ = dres[out_bytes:].view(torch.float32).view_as(lse)
-        slots.append(types.SimpleNamespace(
+        sl = types.SimpleNamespace(
             dstage=dstage, dres=dres,
             dq=dstage[:nq].view_as(w.q[0]), dk=dstage[nq:nq + nk].view_as(w.k_new[0]),
             dv=dstage[nq + nk:].view_as(w.v_new[0]),
             hres=torch.empty(out_bytes + lse_bytes, dtype=torch.uint8).pin_memory(),
             plans=[q.DecodePlan(c.cache, K, c.ws, opts_main, out=eout, lse=else_)
                    for c in copies],
-            h2d=torch.cuda.Event(), comp=torch.cuda.Event(), d2h=torch.cuda.Event()))
-    main = torch.cuda.current_stream()
-    for sl in slots:  # every event starts recorded, so the first waits pass
+            h2d=torch.cuda.Event(), comp=torch.cuda.Event(), d2h=torch.cuda.Event())
+        sl.h2d.record(main)  # creates the events; every one starts recorded
         sl.comp.record(main)
         sl.d2h.record(main)
+        sl.ev = (sl.h2d.cuda_event, sl.comp.cuda_event, sl.d2h.cuda_event)
+        sl.dst_in, sl.src_res = sl.dstage.data_ptr(), sl.dres.data_ptr()
+        sl.hres_ptr, sl.nin, sl.nres = sl.hres.data_ptr(), sl.dstage.numel() * 2, sl.dres.numel()
+        slots.append(sl)
+    host_rows = [[r.data_ptr() for r in rows] for rows in hstage_rows]
+    torch.cuda.synchronize()
 
     def e2e_step(i):
         ci = i % ncopy
         t = (i // ncopy) % steps_per_copy
         sl = slots[i & 1]
-        cs.wait_event(sl.comp)         # step i-2 is done with this slot's input
-        with torch.cuda.stream(cs):
-            sl.dstage.copy_(hstage_rows[ci][t], non_blocking=True)
-        sl.h2d.record(cs)
-        main.wait_event(sl.h2d)
-        main.wait_event(sl.d2h)        # step i-2's result has left this slot
+        e_h2d, e_comp, e_d2h = sl.ev
+        cu.wait(cs_h, e_comp)          # step i-2 is done with this slot's input
+        cu.h2d(sl.dst_in, host_rows[ci][t], sl.nin, cs_h)
+        cu.record(e_h2d, cs_h)
+        cu.wait(main_h, e_h2d)
+        cu.wait(main_h, e_d2h)         # step i-2's result has left this slot
         sl.plans[ci].step(sl.dq, sl.dk, sl.dv)
-        sl.comp.record(main)
-        cs.wait_event(sl.comp)
-        with torch.cuda.stream(cs):
-            sl.hres.copy_(sl.dres, non_blocking=True)
-        sl.d2h.record(cs)
+        cu.record(e_comp, main_h)
+        cu.wait(out_h, e_comp)
+        cu.d2h(sl.hres_ptr, sl.src_res, sl.nres, out_h)
+        cu.record(e_d2h, out_h)
 
     def e2e_timed(count):
         total = 0.0
@@ -568,7 +622,7 @@ def run_quest(args):
             t0.record(main)
             for i in range(m):
                 e2e_step(i)
-            main.wait_stream(cs)  # the last result is on the host
+            main.wait_stream(cs_out)  # the last result is on the host
             t1.record(main)
             torch.cuda.synchronize()
             if world > 1:
