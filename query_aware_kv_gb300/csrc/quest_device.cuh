@@ -31,9 +31,13 @@ struct SmemMap {
 // wsc       : per consumer warp, G x P logits then weights of the page in hand
 // st        : per consumer warp and head: running max (log2 units), running sum, rescale
 // mscale    : per head, the merge scale of every split, then the merged max and sum
+// Pages of a decode ring stage: a page at page size 16, half a page at 32.
+__host__ __device__ constexpr int decode_sub(int P) { return P >= 32 ? P / 16 : 1; }
+
 __host__ __device__ inline SmemMap make_smem_map(int G, int P, int topk_keys, int stp) {
   SmemMap m{};
-  const size_t ring = (size_t)kStages * 2 * P * kHeadDim * 2;
+  const int PS = P / decode_sub(P);  // tokens of a stage
+  const size_t ring = (size_t)kStages * 2 * PS * kHeadDim * 2;
   const size_t red = (size_t)kConsumerWarps * G * kHeadDim * 4;
   const size_t keys = (size_t)topk_keys * 4;
   size_t a = ring;
@@ -44,7 +48,7 @@ __host__ __device__ inline SmemMap make_smem_map(int G, int P, int topk_keys, in
   m.full = o;    o += kStages * 8;
   m.empty = o;   o += kStages * 8;
   m.nvalid = o;  o = align_up(o + kStages * 4, 16);
-  m.wsc = o;     o = align_up(o + (size_t)kConsumerWarps * G * P * 4, 16);
+  m.wsc = o;     o = align_up(o + (size_t)kConsumerWarps * G * PS * 4, 16);
   m.st = o;      o = align_up(o + (size_t)kConsumerWarps * G * 3 * 4, 16);
   m.mscale = o;  o = align_up(o + (size_t)G * (kMaxSplits + 2) * 4, 16);
   m.hist = o;    o += 256 * 4;
@@ -866,7 +870,11 @@ template <int G, int P>
 __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap& m, int b,
                             int g, int split, int r0, int n_tile, int L, int N_b,
                             const int* sel_row, uint32_t pc) {
-  constexpr uint32_t kChunk = P * kHeadDim * 2;
+  // A ring stage holds PS tokens of K and of V: a whole page at page size 16, half a page
+  // at 32 (each page then fills SUB consecutive stages), so that the ring stays 64 KiB and
+  // three CTAs share an SM at either page size.
+  constexpr int SUB = decode_sub(P), PS = P / SUB;
+  constexpr uint32_t kChunk = PS * kHeadDim * 2;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   unsigned char* ring = smem + m.ring;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + m.full);
@@ -914,32 +922,37 @@ __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap&
       const int cnt = min(32, n_tile - base);
 #pragma unroll 1
       for (int j = 0; j < cnt; ++j) {
-        const int nvj = __shfl_sync(0xffffffffu, nv, j);
+        const int nvj0 = __shfl_sync(0xffffffffu, nv, j);
         const int phj = __shfl_sync(0xffffffffu, phys, j);
-        const uint32_t k = pc + (uint32_t)(base + j);
-        const int stage = (int)(k % kStages);
-        const uint32_t par = ((k / kStages) & 1u) ^ 1u;
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait_bounded(p, &empty[stage], par, kSiteWaitSlot);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        __syncwarp();  // the stage's last reads happen before any lane's copy into it
-        const int nvs = ok ? nvj : 0;
-        if (lane == 0) nvalid_s[stage] = nvs;
-        if (nvs > 0) {  // warp-uniform
-          const size_t off = (((size_t)phj * p.Hkv + g) * chunk_elems) * 2 + 16 * lane;
-          const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_pool) + off;
-          const unsigned char* vs = reinterpret_cast<const unsigned char*>(p.v_pool) + off;
-          unsigned char* dst = ring + (size_t)stage * 2 * kChunk + 16 * lane;
+#pragma unroll 1
+        for (int h = 0; h < SUB; ++h) {
+          const int nvj = max(0, min(PS, nvj0 - h * PS));
+          const uint32_t k = pc + (uint32_t)((base + j) * SUB + h);
+          const int stage = (int)(k % kStages);
+          const uint32_t par = ((k / kStages) & 1u) ^ 1u;
+          int ok = 1;
+          if (lane == 0) ok = mbar_wait_bounded(p, &empty[stage], par, kSiteWaitSlot);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          __syncwarp();  // the stage's last reads happen before any lane's copy into it
+          const int nvs = ok ? nvj : 0;
+          if (lane == 0) nvalid_s[stage] = nvs;
+          if (nvs > 0) {  // warp-uniform
+            const size_t off = (((size_t)phj * p.Hkv + g) * chunk_elems +
+                                (size_t)h * PS * kHeadDim) * 2 + 16 * lane;
+            const unsigned char* ks = reinterpret_cast<const unsigned char*>(p.k_pool) + off;
+            const unsigned char* vs = reinterpret_cast<const unsigned char*>(p.v_pool) + off;
+            unsigned char* dst = ring + (size_t)stage * 2 * kChunk + 16 * lane;
 #pragma unroll
-          for (int u = 0; u < (int)kChunk / 512; ++u) cp_async16(dst + 512 * u, ks + 512 * u);
+            for (int u = 0; u < (int)kChunk / 512; ++u) cp_async16(dst + 512 * u, ks + 512 * u);
 #pragma unroll
-          for (int u = 0; u < (int)kChunk / 512; ++u)
-            cp_async16(dst + kChunk + 512 * u, vs + 512 * u);
-          cp_async_arrive(&full[stage]);
-          __syncwarp();  // every lane's pending arrival is counted before lane 0's
+            for (int u = 0; u < (int)kChunk / 512; ++u)
+              cp_async16(dst + kChunk + 512 * u, vs + 512 * u);
+            cp_async_arrive(&full[stage]);
+            __syncwarp();  // every lane's pending arrival is counted before lane 0's
+          }
+          if (lane == 0) mbar_arrive(&full[stage]);
+          __syncwarp();
         }
-        if (lane == 0) mbar_arrive(&full[stage]);
-        __syncwarp();
       }
     }
   } else {
@@ -955,7 +968,7 @@ __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap&
       qf[j][2] = c.x * p.qscale;
       qf[j][3] = c.y * p.qscale;
     }
-    float* sc = reinterpret_cast<float*>(smem + m.wsc) + warp * G * P;
+    float* sc = reinterpret_cast<float*>(smem + m.wsc) + warp * G * PS;
     float* st = st_all + warp * G * 3;
     if (lane < G) {
       st[lane * 3 + 0] = -CUDART_INF_F;
@@ -963,7 +976,7 @@ __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap&
       st[lane * 3 + 2] = 1.f;
     }
     __syncwarp();
-    for (int r = warp; r < n_tile; r += kConsumerWarps) {
+    for (int r = warp; r < n_tile * SUB; r += kConsumerWarps) {
       const uint32_t k = pc + (uint32_t)r;
       const int stage = (int)(k % kStages);
       const uint32_t par = (k / kStages) & 1u;
@@ -971,7 +984,7 @@ __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap&
       const int nv = ok ? nvalid_s[stage] : 0;
       if (nv > 0) {
         const __half* Ks = reinterpret_cast<const __half*>(ring + (size_t)stage * 2 * kChunk);
-        page_update<G, P>(qf, acc, Ks, Ks + P * kHeadDim, nv, sc, st, lane);
+        page_update<G, PS>(qf, acc, Ks, Ks + PS * kHeadDim, nv, sc, st, lane);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
