@@ -386,16 +386,30 @@ def run_quest(args):
         c.plan.step(c.qs[t], c.kns[t], c.vns[t])
 
     host_issue = [0.0, 0]  # host seconds spent issuing calls, and those calls (last timed_steps)
+    # Position of the next step in the rotation (0..seg-1): step i appends to copy i % ncopy.
+    # The copies are rewound only when every one is full, so that a timed run follows its
+    # warm-up directly instead of starting behind a rewind (whose writes leave the L2 dirty).
+    cursor = [0]
+
+    def take(m_max):
+        """Room for up to m_max more steps before a rewind (rewinding first if there is
+        none); returns (first position, steps)."""
+        if cursor[0] >= seg:
+            rewind_all()
+            cursor[0] = 0
+        m = min(m_max, seg - cursor[0])
+        first = cursor[0]
+        cursor[0] += m
+        return first, m
 
     def timed_steps(count, fn):
-        """`count` calls of fn(i) back to back, in segments of at most `seg` calls (the copies
-        are rewound between segments, outside the timed intervals).  Returns total ms."""
+        """`count` calls of fn(position) back to back, in segments that end where the copies
+        must be rewound (outside the timed intervals).  Returns total ms."""
         total = 0.0
         done = 0
         host_issue[0], host_issue[1] = 0.0, 0
         while done < count:
-            m = min(seg, count - done)
-            rewind_all()
+            first, m = take(count - done)
             torch.cuda.synchronize()
             if world > 1:
                 dist.barrier()
@@ -404,11 +418,11 @@ def run_quest(args):
             # wait for room in the launch queue once the GPU falls behind
             h_n = min(m, 128)
             h0 = time.perf_counter()
-            for i in range(h_n):
+            for i in range(first, first + h_n):
                 fn(i)
             host_issue[0] += time.perf_counter() - h0
             host_issue[1] += h_n
-            for i in range(h_n, m):
+            for i in range(first + h_n, first + m):
                 fn(i)
             t1.record()
             torch.cuda.synchronize()
@@ -439,7 +453,8 @@ def run_quest(args):
     torch.cuda.synchronize()
     # warm-up: the flushed per-step loop's calls, then the timed loop's own (last, so that
     # the timed steps do not start behind a flush that evicted the kernels' code from L2)
-    for i in range(max(1, args.warmup)):
+    for _ in range(max(1, args.warmup)):
+        i, _m = take(1)
         flush_l2()
         t0.record()
         step(i)
@@ -469,19 +484,18 @@ def run_quest(args):
     fn_ = min(n, 256)
     fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(fn_)]
-    rewind_all()
     for i in range(fn_):
-        if i and i % seg == 0:
-            rewind_all()
+        pos, _m = take(1)
         flush_l2()
         fev[i][0].record()
-        step(i % seg)
+        step(pos)
         fev[i][1].record()
     torch.cuda.synchronize()
     flushed_us = [1e3 * a.elapsed_time(b) for a, b in fev]
 
     # ---- kernel-only: quest_decode alone at one context per copy (after its 64 tokens)
     rewind_all()
+    cursor[0] = seg  # every copy is filled below: the next step rewinds first
     for c in copies:
         for t in range(c.w.steps):
             q.append(c.cache, c.w.k_new[t], c.w.v_new[t], c.ws)
@@ -621,13 +635,12 @@ def run_quest(args):
         total = 0.0
         done = 0
         while done < count:
-            m = min(seg, count - done)
-            rewind_all()
+            first, m = take(count - done)
             torch.cuda.synchronize()
             if world > 1:
                 dist.barrier()
             t0.record(main)
-            for i in range(m):
+            for i in range(first, first + m):
                 e2e_step(i)
             main.wait_stream(cs_out)  # the last result is on the host
             t1.record(main)
