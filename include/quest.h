@@ -129,12 +129,17 @@ typedef struct quest_opts {
                                  Implementation step 2).  0 and 0 (the default): plain
                                  top-K.  Needs sink_pages, local_pages >= 0 and
                                  sink_pages + local_pages <= top_k (QUEST_ERR_INVALID_ARG) */
-    int32_t gqa_union;        /* quest_topk only: scores are per query head ([batch]
-                                 [num_q_heads][max_pages], quest_estimate_heads); each query
-                                 head keeps its top_k pages and the kv head keeps their union
-                                 ([Guide] Best Practices step 2), written to idx rows of
-                                 min(G * top_k, max_pages) entries.  Not with sink / local
-                                 pages; the fused calls answer QUEST_ERR_UNSUPPORTED.        */
+    int32_t gqa_union;        /* the union form of the group-level selection ([Guide] Best
+                                 Practices step 2): each query head keeps its top_k pages and
+                                 the kv head keeps their union, in selection rows of
+                                 min(G * top_k, max_pages) entries.  quest_topk: scores are
+                                 per query head ([batch][num_q_heads][max_pages],
+                                 quest_estimate_heads).  quest_decode / quest_decode_step: run
+                                 as a chain (the new token first, then every query head's
+                                 bounds, the union, the sparse decode over it; size the
+                                 workspace with the same opts); the one-launch paths and
+                                 quest_decode_layers answer QUEST_ERR_UNSUPPORTED.  Not with
+                                 sink / local pages (QUEST_ERR_INVALID_ARG).                  */
     int32_t path;             /* quest_decode*: QUEST_PATH_* (quest_decode_layers: see there).
                                  The chain
                                  computes the same step as separate kernels: estimate, top-K
@@ -181,7 +186,8 @@ int quest_decode_path(const quest_cache_t* cache, int32_t top_k, const quest_opt
 /* Kernel launches of one quest_decode or quest_decode_step call for this cache, top_k and
  * opts: 1 on the one-launch paths; on the chain 3 (estimate, top-K, sparse decode), or 2
  * when the sparse decode's work items take the top-K themselves (few pairs: see
- * QUEST_PATH_CHAIN).  Minus a QUEST_ERR_* status on invalid arguments; launches nothing. */
+ * QUEST_PATH_CHAIN); with gqa_union 3, and one more for quest_decode_step (its append).
+ * Minus a QUEST_ERR_* status on invalid arguments; launches nothing. */
 int quest_decode_launches(const quest_cache_t* cache, int32_t top_k, const quest_opts_t* opts);
 
 /* quest_decode only (one-launch paths): never publish the selection, so that every

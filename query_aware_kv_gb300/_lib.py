@@ -179,6 +179,15 @@ def _opts_ref(o: Optional[QuestOpts]):
     return None if o is None else ctypes.byref(o)
 
 
+def _sel_row(cache, top_k: int, o: Optional[QuestOpts]) -> int:
+    """Entries of a selection row of the decode calls: top_k, or min(G * top_k, max_pages)
+    in the union form (o.gqa_union)."""
+    if o is not None and o.gqa_union:
+        G = cache.desc.num_q_heads // cache.num_kv_heads
+        return min(G * int(top_k), cache.max_pages)
+    return int(top_k)
+
+
 @dataclass
 class PagedCache:
     """One layer's paged fp16 KV cache with per-page key min/max (device tensors).
@@ -349,11 +358,14 @@ def decode(cache: PagedCache, q: torch.Tensor, top_k: int, ws: torch.Tensor,
            idx_out: Optional[torch.Tensor] = None, count_out: Optional[torch.Tensor] = None,
            stream=None):
     """Estimate + top-K + sparse decode: one launch of the cluster or the stream kernel, or
-    the chain of three kernels (o.path; automatic by default, see decode_path)."""
+    a chain of kernels (o.path; automatic by default, see decode_path).  With o.gqa_union
+    the selection is the union of every query head's top-K (rows of min(G * top_k,
+    max_pages) in idx_out), on the chain."""
     _need(q, "q", torch.float16, (cache.batch, cache.desc.num_q_heads, HEAD_DIM))
     out, lse = _out(cache, q, out, lse, want_lse)
     if idx_out is not None:
-        _need(idx_out, "idx_out", torch.int32, (cache.batch, cache.num_kv_heads, top_k))
+        _need(idx_out, "idx_out", torch.int32,
+              (cache.batch, cache.num_kv_heads, _sel_row(cache, top_k, o)))
     if count_out is not None:
         _need(count_out, "count_out", torch.int32, (cache.batch, cache.num_kv_heads))
     _check(load().quest_decode(ctypes.byref(cache.desc), q.data_ptr(), int(top_k), out.data_ptr(),
@@ -374,7 +386,8 @@ def decode_step(cache: PagedCache, q: torch.Tensor, k_new: torch.Tensor, v_new: 
     _need(v_new, "v_new", torch.float16, shape)
     out, lse = _out(cache, q, out, lse, want_lse)
     if idx_out is not None:
-        _need(idx_out, "idx_out", torch.int32, (cache.batch, cache.num_kv_heads, top_k))
+        _need(idx_out, "idx_out", torch.int32,
+              (cache.batch, cache.num_kv_heads, _sel_row(cache, top_k, o)))
     if count_out is not None:
         _need(count_out, "count_out", torch.int32, (cache.batch, cache.num_kv_heads))
     _check(load().quest_decode_step(ctypes.byref(cache.desc), q.data_ptr(), k_new.data_ptr(),
@@ -405,7 +418,7 @@ class DecodePlan:
         probe = torch.empty(0, dtype=torch.float16, device=cache.k_pool.device)
         self.out, self.lse = _out(cache, probe, out, lse, want_lse)
         if idx_out is not None:
-            _need(idx_out, "idx_out", torch.int32, (B, Hkv, top_k))
+            _need(idx_out, "idx_out", torch.int32, (B, Hkv, _sel_row(cache, top_k, o)))
         if count_out is not None:
             _need(count_out, "count_out", torch.int32, (B, Hkv))
         _need(ws, "ws", torch.uint8)

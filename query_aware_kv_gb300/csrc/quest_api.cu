@@ -88,13 +88,19 @@ int check_window(const quest_opts_t* o, int top_k) {
 Tiling make_tiling(const quest_cache_t* c, int top_k, const quest_opts_t* o) {
   Tiling t{};
   t.topk_cap = top_k;
+  t.score_rows = 1;
+  if (o && o->gqa_union) {  // a fused call in the union form: per-head scores, union rows
+    const int G = c->num_kv_heads > 0 ? c->num_q_heads / c->num_kv_heads : 1;
+    t.topk_cap = (int)std::min<long long>((long long)G * top_k, c->max_pages);
+    t.score_rows = G;
+  }
   int stp = (o && o->score_tile_pages > 0) ? o->score_tile_pages : kDefaultScoreTilePages;
   if (stp > c->max_pages) stp = c->max_pages;
   t.score_tile_pages = stp;
   t.n_score_tiles = (int)cdiv(c->max_pages, stp);
   const int user_pps = (o && o->pages_per_split > 0) ? o->pages_per_split : 0;
   const int pps = user_pps ? user_pps : kDefaultPagesPerSplit;
-  const int kcap = top_k < c->max_pages ? top_k : c->max_pages;
+  const int kcap = t.topk_cap < c->max_pages ? t.topk_cap : c->max_pages;
   // by default about 8 sparse work items per (sequence, kv head), of at least 16 pages: a
   // work item of a few pages spends most of its time filling its ring and merging
   t.pps_sparse = user_pps ? (int)std::max<long long>(user_pps, cdiv(kcap, kMaxSplits))
@@ -118,7 +124,7 @@ WsLayout make_layout(const quest_cache_t* c, const Tiling& t) {
   L.decode_arrive = off; off = up256(off + nbg * 4);
   L.seq_done = off;      off = up256(off + (size_t)c->batch * 4);
   L.skeys = off;         off = up256(off + nbg * c->max_pages * 4);
-  L.scores = off;        off = up256(off + nbg * c->max_pages * 4);
+  L.scores = off;        off = up256(off + nbg * t.score_rows * c->max_pages * 4);
   L.sel_idx = off;       off = up256(off + nbg * (size_t)t.topk_cap * 4);
   L.sel_count = off;     off = up256(off + nbg * 4);
   L.part_ml = off;       off = up256(off + nbh * t.max_splits * 2 * 4);
@@ -431,6 +437,15 @@ static int decide_path(const quest_cache_t* cache, int32_t top_k, const quest_op
     return fail(QUEST_ERR_INVALID_ARG, "path %d: use QUEST_PATH_AUTO, _FUSED, _CHAIN or _STREAM",
                 path);
   const int G = group_of(cache);
+  if (opts && opts->gqa_union) {  // the union form runs as a chain of kernels only
+    if (path == QUEST_PATH_FUSED || path == QUEST_PATH_STREAM || cs > 0)
+      return fail(QUEST_ERR_UNSUPPORTED, "gqa_union runs on the chain path only (its one-launch "
+                  "kernels select per kv head)");
+    if (n_layers > 1)
+      return fail(QUEST_ERR_UNSUPPORTED, "gqa_union: quest_decode_layers selects per kv head");
+    *path_out = QUEST_PATH_CHAIN;
+    return QUEST_OK;
+  }
   if (path == QUEST_PATH_STREAM) {
     if (stream_slots(G, cache->page_size, cache->max_pages, top_k, cache->batch,
                      cache->num_q_heads) <= 0)
@@ -460,9 +475,9 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
   if (rc) return rc;
   if ((rc = check_topk(top_k))) return rc;
   if ((rc = check_window(opts, top_k))) return rc;
-  if (opts && opts->gqa_union)
-    return fail(QUEST_ERR_UNSUPPORTED, "gqa_union: use quest_estimate_heads + quest_topk + "
-                "quest_sparse_decode (the fused step selects per kv head)");
+  const bool uni = opts && opts->gqa_union;
+  if (uni && (opts->sink_pages || opts->local_pages))
+    return fail(QUEST_ERR_INVALID_ARG, "gqa_union does not combine with sink / local pages");
   if (cache->batch == 0) return QUEST_OK;
   if (!q || !out || !aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(idx_out, 4) || !aligned(count_out, 4))
@@ -502,6 +517,23 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
     const LayerPtrs lay{p.k_pool, p.v_pool, p.meta, p.q, p.k_new, p.v_new, p.out, p.lse};
     return launched(launch_stream(p, lay, G, opts ? opts->max_ctas : 0, s), what);
   }
+  if (path == QUEST_PATH_CHAIN && uni) {
+    // the union form of the group-level selection ([Guide] Best Practices step 2): the new
+    // token first (the lengths advance with it), then every query head's bounds, each
+    // head's top-K and their union per kv head (rows of topk_cap), and the sparse decode
+    // over the union; the selection goes to idx_out / count_out (rows of topk_cap) if given
+    const int cap = t.topk_cap;
+    cudaError_t e = cudaSuccess;
+    if (k_new) e = launch_append(p, p.k_new, p.v_new, s, true);
+    p.chain_append = 0;
+    p.k_new = p.v_new = nullptr;
+    if (e == cudaSuccess) e = launch_estimate(p, G, true, s);
+    if (e == cudaSuccess) e = launch_topk_union(p, cap, s);
+    Params d = p;
+    d.top_k = cap;  // row stride of the union selection
+    if (e == cudaSuccess) e = launch_decode(d, G, s);
+    return launched(e, what);
+  }
   if (path == QUEST_PATH_CHAIN) {
     // the same step as separate kernels: estimate (which also writes the new token's row
     // and widens its box), top-K (its own kernel, or inside every decode work item: see
@@ -535,6 +567,7 @@ int quest_decode_launches(const quest_cache_t* cache, int32_t top_k, const quest
   int path = QUEST_PATH_FUSED;
   if ((rc = decide_path(cache, top_k, opts, 1, &path))) return -rc;
   if (path != QUEST_PATH_CHAIN) return 1;
+  if (opts && opts->gqa_union) return 3;  // per-head bounds, union top-K, sparse decode
   const Tiling t = make_tiling(cache, top_k, opts);
   Params p{};
   p.B = cache->batch;

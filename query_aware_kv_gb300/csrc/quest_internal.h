@@ -39,7 +39,9 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 struct Tiling {
-  int topk_cap;          // min(top_k, max_pages): slots per selection row
+  int topk_cap;          // slots per selection row: top_k (min(G * top_k, max_pages) for the
+                         // union form of a fused call)
+  int score_rows;        // score rows per (b, kv head): 1, or G for the union form
   int score_tile_pages;  // pages per scoring work item
   int n_score_tiles;     // scoring work items per (b, g)
   int pps_sparse, n_splits_sparse;  // selected pages per decode item, items per (b, g)
@@ -52,7 +54,7 @@ struct WsLayout {
   size_t seq_done;                            // u32 [B]
   size_t skeys;                               // u32 [B*Hkv*max_pages] stream kernel's key
                                               // rows (0 = not written yet; kept zero)
-  size_t scores;                              // f32 [B*Hkv*max_pages]
+  size_t scores;                              // f32 [B*Hkv*score_rows*max_pages]
   size_t sel_idx, sel_count;                  // i32 [B*Hkv*topk_cap], [B*Hkv]
   size_t part_ml, part_acc;                   // f32 [B*Hq*max_splits*2], [..*128]
   size_t sel_pair;                            // i32x2 [B*Hkv*topk_cap] (logical, physical)

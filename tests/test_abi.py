@@ -96,11 +96,10 @@ def test_calls_reject_bad_arguments_without_launching(lib):
         assert lib.quest_decode(ctypes.byref(d), 16, 4, 16, None, None, None, 256, 1 << 20,
                                 ctypes.byref(o), None) == q.QUEST_ERR_INVALID_ARG
         assert "sink_pages" in lib.quest_last_error().decode()
-    # the union selection is for the separate calls only
-    ou = q.opts(gqa_union=True)
-    assert lib.quest_decode(ctypes.byref(d), 16, 4, 16, None, None, None, 256, 1 << 20,
-                            ctypes.byref(ou), None) == q.QUEST_ERR_UNSUPPORTED
+    # the union selection does not combine with a sink / local window
     ou2 = q.opts(gqa_union=True, sink_pages=1)
+    assert lib.quest_decode(ctypes.byref(d), 16, 4, 16, None, None, None, 256, 1 << 20,
+                            ctypes.byref(ou2), None) == q.QUEST_ERR_INVALID_ARG
     assert lib.quest_topk(ctypes.byref(d), 16, 4, 16, 16, 256, 1 << 20, ctypes.byref(ou2),
                           None) == q.QUEST_ERR_INVALID_ARG
     # multi-layer call: layer count out of range, k_new for some layers only
@@ -230,3 +229,21 @@ def test_decode_launches_without_a_device_query(lib):
     o = q.opts(path=7)
     assert lib.quest_decode_launches(ctypes.byref(d), 16, ctypes.byref(o)) == \
         -q.QUEST_ERR_INVALID_ARG
+
+
+def test_union_form_runs_on_the_chain(lib):
+    """gqa_union on the fused calls: the chain (no device query), three launches, a larger
+    workspace (per-head scores, union rows); the one-launch paths refuse it."""
+    d = desc(num_q_heads=16, num_kv_heads=4)
+    o = q.opts(gqa_union=True)
+    assert lib.quest_decode_path(ctypes.byref(d), 8, ctypes.byref(o), 1) == q.QUEST_PATH_CHAIN
+    assert lib.quest_decode_launches(ctypes.byref(d), 8, ctypes.byref(o)) == 3
+    assert lib.quest_workspace_size(ctypes.byref(d), 8, ctypes.byref(o)) > \
+        lib.quest_workspace_size(ctypes.byref(d), 8, None)
+    for path in (q.QUEST_PATH_FUSED, q.QUEST_PATH_STREAM):
+        o = q.opts(gqa_union=True, path=path)
+        assert lib.quest_decode_path(ctypes.byref(d), 8, ctypes.byref(o), 1) == \
+            -q.QUEST_ERR_UNSUPPORTED
+    o = q.opts(gqa_union=True)
+    assert lib.quest_decode_path(ctypes.byref(d), 8, ctypes.byref(o), 2) == \
+        -q.QUEST_ERR_UNSUPPORTED

@@ -737,3 +737,43 @@ def test_chain_launch_count_follows_the_work_item_rule():
         pair = H.on_device(w)
         assert q.decode_launches(pair.cache, w.top_k, o) == launches
         H.run_step_and_compare(pair, 0, w.top_k, opts=o, one_launch=True, check_cache=True)
+
+
+@pytest.mark.parametrize("append", [False, True], ids=["decode", "step"])
+def test_fused_union_form_matches_separate_calls_and_oracle(append):
+    """quest_decode / quest_decode_step with gqa_union (the chain: per-head bounds, union
+    top-K, sparse decode over the union) gives the same union, counts and outputs, bit for
+    bit, as the separate calls, and matches the oracle's attention over that union."""
+    w = small(lens=(3000, 700, 16 * 9), batch=3, hq=8, hkv=2, budget=256, outliers=4,
+              steps=1)
+    a, b = H.on_device(w), H.on_device(w)
+    K, G = w.top_k, 4
+    o = q.opts(gqa_union=True)
+    cap = min(G * K, a.cache.max_pages)
+    ws_a = q.workspace(a.cache, K, o)
+    idx = torch.empty((3, 2, cap), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((3, 2), dtype=torch.int32, device="cuda")
+    qd, kn, vn = w.q[0].cuda(), w.k_new[0].cuda(), w.v_new[0].cuda()
+    assert q.decode_path(a.cache, K, o) == q.QUEST_PATH_CHAIN
+    if append:
+        out, lse = q.decode_step(a.cache, qd, kn, vn, K, ws_a, o, idx_out=idx, count_out=cnt)
+        q.append(b.cache, kn, vn, b.ws)
+    else:
+        out, lse = q.decode(a.cache, qd, K, ws_a, o, idx_out=idx, count_out=cnt)
+    sh = q.estimate_heads(b.cache, qd, b.ws)
+    i2, c2 = q.topk(b.cache, sh, K, b.ws, o)
+    ws_u = q.workspace(b.cache, cap)
+    o2, l2 = q.sparse_decode(b.cache, qd, i2, c2, cap, ws_u)
+    H.assert_status_ok(ws_a)
+    H.assert_status_ok(b.ws)
+    assert torch.equal(idx, i2) and torch.equal(cnt, c2)
+    assert torch.equal(out, o2) and torch.equal(lse, l2)
+    assert torch.equal(a.cache.meta, b.cache.meta) and torch.equal(a.cache.seq_lens, b.cache.seq_lens)
+    if append:
+        oracle.append(a.ref, w.k_new[0].numpy(), w.v_new[0].numpy())
+    qh = w.q[0].numpy().astype(np.float32)
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    out_ref, lse_ref = oracle.attend(a.ref, qh, gi, gc)
+    H.assert_attention_close(out, lse, out_ref, lse_ref)
+    with pytest.raises(q.QuestError):
+        q.decode(a.cache, qd, K, ws_a, q.opts(gqa_union=True, sink_pages=1, local_pages=1))
