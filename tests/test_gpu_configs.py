@@ -69,3 +69,44 @@ def test_gqa_llama31(page_size, path):
     w = wl.gqa_llama31(seed=0, device="cuda", page_size=page_size)
     _run(w, 1, check_needles=False, path=path)
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("page_size", [16, 32])
+def test_gqa_llama31_union_form(page_size):
+    """The full-size GQA workload through quest_decode_step in the union form (gqa_union):
+    every query head's top-K pages, their union per kv head, attention over the union.
+    The union is compared with the oracle's (swaps only inside some head's tie window around
+    its K-th score) and the attention with the oracle's over the GPU's union."""
+    import numpy as np
+    import oracle
+    w = wl.gqa_llama31(seed=0, device="cuda", page_size=page_size)
+    pair = H.on_device(w)
+    K, G = w.top_k, w.num_q_heads // w.num_kv_heads
+    o = q.opts(gqa_union=True)
+    cap = min(G * K, pair.cache.max_pages)
+    ws = q.workspace(pair.cache, K, o)
+    idx = torch.empty((w.batch, w.num_kv_heads, cap), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((w.batch, w.num_kv_heads), dtype=torch.int32, device="cuda")
+    out, lse = q.decode_step(pair.cache, w.q[0], w.k_new[0], w.v_new[0], K, ws, o,
+                             idx_out=idx, count_out=cnt)
+    H.assert_status_ok(ws)
+    oracle.append(pair.ref, w.k_new[0].cpu().numpy(), w.v_new[0].cpu().numpy())
+    assert pair.cache.seq_lens.cpu().numpy().tolist() == pair.ref.seq_lens.tolist()
+    qh = w.q[0].cpu().numpy().astype(np.float32)
+    ref_sh = oracle.score_heads(pair.ref, qh)
+    ri, rc = oracle.topk_union(pair.ref, ref_sh, K)
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    for b in range(w.batch):
+        n = wl.pages_for(int(pair.ref.seq_lens[b]), page_size)
+        for g in range(w.num_kv_heads):
+            got = set(gi[b, g, :gc[b, g]].tolist())
+            want = set(ri[b, g, :rc[b, g]].tolist())
+            window = set()
+            for h in range(g * G, (g + 1) * G):
+                row = ref_sh[b, h, :n]
+                sk = float(np.sort(row)[::-1][K - 1])
+                window |= {p for p in range(n) if abs(float(row[p]) - sk) <= H.TIE_REL * abs(sk)}
+            assert got - window == want - window, (b, g)
+    out_ref, lse_ref = oracle.attend(pair.ref, qh, gi, gc)
+    H.assert_attention_close(out, lse, out_ref, lse_ref)
+    torch.cuda.empty_cache()
