@@ -5,7 +5,8 @@
 //   topk_fast     : exact top-K of a row of score keys, ties to the lower page index
 //   topk_row        ("Guide to Quest", Solution step 3); topk_row loads the row first.
 //   decode_tile   : flash-decode over a run of kept pages, staged into shared memory by
-//                   1-D bulk copies (TMA) with an mbarrier ring; writes one split-K partial
+//                   per-lane 16-byte cp.async copies into an mbarrier ring; writes one
+//                   split-K partial
 //                   (Tang 2024 summary: exact attention over the Top-K pages).
 //   merge_splits  : log-sum-exp merge of the partials of one (sequence, kv head).
 #pragma once
@@ -865,7 +866,7 @@ __device__ __forceinline__ void page_update(const float (&qf)[G][4], float (&acc
 // logical pages r0.. when sel_row is null) and write this work item's split-K partial.
 // pc: pages this CTA has already pushed through its ring (mbarrier phase bookkeeping).
 // Called by the whole block (kDecodeThreads threads): warps 0..7 compute, warp 8 issues
-// the bulk copies.  n_tile >= 1.
+// the copies.  n_tile >= 1.
 template <int G, int P>
 __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap& m, int b,
                             int g, int split, int r0, int n_tile, int L, int N_b,
@@ -890,8 +891,8 @@ __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap&
   if (warp == kConsumerWarps) {
     // ---- producer warp: resolve pages 32 at a time, then fill their stages in order.  A
     // page's K and V chunks lie anywhere in the pool: the whole warp copies them, 16 bytes a
-    // lane per instruction (scattered 4-8 KB chunks come in faster through the load path
-    // than as bulk copies), and the stage completes on its full barrier through the copies'
+    // lane per instruction (the same rate as one bulk copy per chunk measured here, with no
+    // byte count to arm), and the stage completes on its full barrier through the copies'
     // own arrivals (each lane's, plus one plain arrival of lane 0).
     const size_t chunk_elems = (size_t)P * kHeadDim;
     for (int base = 0; base < n_tile; base += 32) {
@@ -1023,7 +1024,8 @@ __device__ void decode_tile(const Params& p, unsigned char* smem, const SmemMap&
       p.part_ml[slot * 2 + 1] = Ls;
     }
   }
-  fence_proxy_async_smem();  // generic use of the ring ends before the next bulk copies
+  fence_proxy_async_smem();  // generic use of the ring (the merge buffer) is ordered before
+                             // any later bulk copy into it
 }
 
 // Log-sum-exp merge of the first n_live partials of every head of (b, g) into out / lse.

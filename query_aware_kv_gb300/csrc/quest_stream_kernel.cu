@@ -12,8 +12,8 @@
 //       streams it into a shared-memory ring: first its scoring pieces (the boxes of up
 //       to P pages of one pair, "Guide to Quest", Solution step 1, one 1-D bulk copy
 //       (TMA) each), then its decode pieces (the K and V chunks of up to 8 kept pages of
-//       one pair, once that pair's selection is published; scattered 4 KB chunks, which
-//       per-lane 16-byte asynchronous copies fetch faster than bulk copies).
+//       one pair, once that pair's selection is published: scattered 4 KB chunks, copied
+//       by the whole warp 16 bytes a lane with cp.async).
 //   consumer warps (0..7)  stage s belongs to consumer s mod 8.  Scoring stage: the
 //       bound of each page (Solution step 2) becomes an order-preserving key in global
 //       memory, and the piece is counted on its pair (a release reduction).  Decode
