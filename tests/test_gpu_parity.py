@@ -739,6 +739,68 @@ def test_chain_launch_count_follows_the_work_item_rule():
         H.run_step_and_compare(pair, 0, w.top_k, opts=o, one_launch=True, check_cache=True)
 
 
+@pytest.mark.parametrize("hq,hkv,max_pages,chain_launches",
+                         [(4, 4, 4096, 2), (4, 4, 4097, 3), (8, 4, 4096, 3)],
+                         ids=["mha_4096", "mha_4097", "gqa_4096"])
+def test_exact_ties_on_every_path_go_to_the_lower_page(hq, hkv, max_pages, chain_launches):
+    """Every page's keys are one vector per kv head scaled by one of four factors, so the
+    page scores take four values, each shared by hundreds of pages, and the rule that ties
+    go to the lower page alone fixes the selection.  Each decode path (the top-K inside
+    the decode's work items on MHA rows of up to 4096 pages, the top-K kernel on longer
+    rows and on GQA, the cluster kernel, the stream kernel) returns the oracle's pages bit
+    for bit, and the oracle's attention over them."""
+    B, P, K = 2, 16, 128
+    w = wl.build("ties", batch=B, num_q_heads=hq, num_kv_heads=hkv, page_size=P,
+                 prefill_lens=[P * 3000 + 5, P * 900], steps=1, budget=K * P, seed=11,
+                 max_pages=max_pages)
+    gen = torch.Generator().manual_seed(5)
+    u = torch.randn(hkv, 128, generator=gen)
+    u = 4.0 * u / u.norm(dim=1, keepdim=True)
+    for b in range(B):
+        n = int((w.block_table[b] >= 0).sum())
+        p = torch.arange(n).unsqueeze(1)
+        c = 1 + (7 * p + 3 * torch.arange(hkv).unsqueeze(0) + b) % 4          # [n][Hkv]
+        w.k_pool[w.block_table[b, :n].long()] = (
+            (c[:, :, None, None] * u[None, :, None, :]).expand(n, hkv, P, 128).to(torch.float16))
+    G = hq // hkv
+    for h in range(hq):
+        sign = 1.0 if (h // G) % 2 == 0 else -1.0                 # the top or the bottom class
+        w.q[0, :, h] = (sign * u[h // G]).to(torch.float16)
+
+    qh = w.q[0].numpy().astype(np.float32)
+    ref = H.on_device(w).ref
+    ref_scores = oracle.score(ref, qh)
+    ref_idx, ref_cnt = oracle.topk(ref, ref_scores, K)
+    for b in range(B):
+        for g in range(hkv):
+            s = np.sort(ref_scores[b, g][np.isfinite(ref_scores[b, g])])[::-1]
+            assert s[K - 1] == s[K], "the K-th and the next page must tie"
+    want = np.sort(ref_idx, axis=2)
+    out_ref, lse_ref = oracle.attend(ref, qh, want, ref_cnt)
+
+    ran = []
+    for path in (q.QUEST_PATH_AUTO, q.QUEST_PATH_CHAIN, q.QUEST_PATH_FUSED,
+                 q.QUEST_PATH_STREAM):
+        o = q.opts(path=path)
+        pair = H.on_device(w, opts=o)
+        try:
+            q.decode_path(pair.cache, K, o)
+        except q.QuestError:
+            continue                            # a one-launch kernel this shape does not fit
+        if path == q.QUEST_PATH_CHAIN:
+            assert q.decode_launches(pair.cache, K, o) == chain_launches
+        idx = torch.empty((B, hkv, K), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((B, hkv), dtype=torch.int32, device="cuda")
+        out, lse = q.decode(pair.cache, w.q[0].cuda(), K, pair.ws, o, idx_out=idx,
+                            count_out=cnt)
+        H.assert_status_ok(pair.ws)
+        np.testing.assert_array_equal(cnt.cpu().numpy(), ref_cnt)
+        np.testing.assert_array_equal(idx.cpu().numpy(), want)
+        H.assert_attention_close(out, lse, out_ref, lse_ref)
+        ran.append(path)
+    assert q.QUEST_PATH_AUTO in ran and q.QUEST_PATH_CHAIN in ran, ran
+
+
 @pytest.mark.parametrize("append", [False, True], ids=["decode", "step"])
 def test_fused_union_form_matches_separate_calls_and_oracle(append):
     """quest_decode / quest_decode_step with gqa_union (the chain: per-head bounds, union
