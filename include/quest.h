@@ -262,8 +262,8 @@ int quest_estimate_heads(const quest_cache_t* cache, const void* q, float* score
                          size_t ws_bytes, quest_stream_t stream);
 
 /*
- * Top-K page selection.  [Guide] Solution step 3; [Summary] "Top-K highest-scoring
- * pages".  For each (b, g) keeps K_b = min(top_k, N_b) pages, N_b = ceil(seq_len / P):
+ * Top-K page selection.  [Guide] Solution step 3; [Summary] Summary (the K best-scoring
+ * pages).  For each (b, g) keeps K_b = min(top_k, N_b) pages, N_b = ceil(seq_len / P):
  * the pages with the largest scores, equal scores going to the lower page index.  If
  * N_b <= top_k every page is kept.  idx: int32 [batch][num_kv_heads][top_k], the kept
  * logical pages in ASCENDING page order, -1 after the first K_b; count: int32

@@ -235,7 +235,7 @@ int oq_score_heads(const oq_dims* s, const float* q, const float* meta, const in
 
 /* ---------------------------------------------------------------------------------
  * Page selection.  [Guide] Solution, step 3: keep the K pages with the highest bounds
- * ([Summary]: "Top-K highest-scoring pages").  Pages are ordered by score, larger
+ * ([Summary], Summary: the K best-scoring pages).  Pages are ordered by score, larger
  * first, and equal scores by page index, lower first; the first K_b = min(K, N_b) are
  * kept.  When the sequence has no more than K pages every page is kept ([Guide],
  * Implementation step 2, the short-sequence case).

@@ -518,10 +518,11 @@ static int decode_impl(const quest_cache_t* cache, const void* q, const void* k_
     return launched(launch_stream(p, lay, G, opts ? opts->max_ctas : 0, s), what);
   }
   if (path == QUEST_PATH_CHAIN && uni) {
-    // the union form of the group-level selection ([Guide] Best Practices step 2): the new
-    // token first (the lengths advance with it), then every query head's bounds, each
-    // head's top-K and their union per kv head (rows of topk_cap), and the sparse decode
-    // over the union; the selection goes to idx_out / count_out (rows of topk_cap) if given
+    // the union form of the group-level selection ("Guide to Quest", Best Practices step
+    // 2): the new token first (the lengths advance with it), then every query head's
+    // bounds, each head's top-K and their union per kv head (rows of topk_cap), and the
+    // sparse decode over the union; the selection goes to idx_out / count_out (rows of
+    // topk_cap) if given
     const int cap = t.topk_cap;
     cudaError_t e = cudaSuccess;
     if (k_new) e = launch_append(p, p.k_new, p.v_new, s, true);

@@ -13,7 +13,8 @@
 //      every CTA's selection barrier;
 //   3. each CTA's producer reads its share of the selection from rank 0, resolves the pages
 //      through the block table and streams their K / V chunks; the consumer warps run
-//      flash-decode over them (Tang 2024 summary: exact attention over the Top-K) and store
+//      flash-decode over them (exact attention over the kept pages only: "Quest:
+//      Query-Aware Sparsity for Efficient Long-Context LLM Inference", Summary) and store
 //      the partial (max, sum, accumulator) into rank 0;
 //   4. rank 0 merges the partials by log-sum-exp and writes the output.
 // Rank 0's buffers alternate between consecutive pairs, so the other CTAs can start scoring

@@ -6,8 +6,9 @@
 //   topk_row        ("Guide to Quest", Solution step 3); topk_row loads the row first.
 //   decode_tile   : flash-decode over a run of kept pages, staged into shared memory by
 //                   per-lane 16-byte cp.async copies into an mbarrier ring; writes one
-//                   split-K partial
-//                   (Tang 2024 summary: exact attention over the Top-K pages).
+//                   split-K partial (exact attention over the kept pages only: "Quest:
+//                   Query-Aware Sparsity for Efficient Long-Context LLM Inference",
+//                   Summary).
 //   merge_splits  : log-sum-exp merge of the partials of one (sequence, kv head).
 #pragma once
 
@@ -26,10 +27,12 @@ struct SmemMap {
   size_t ring, full, empty, nvalid, wsc, st, mscale, hist, scratch, misc, bt, total;
 };
 
-// ring      : kStages x (K chunk + V chunk) of one (page, kv head); also reused, when idle,
+// ring      : kStages x (K chunk + V chunk) of one stage of one kv head (a page, or half a
+//             page at page size 32); also reused, when idle,
 //             for the warp-merge buffer and for the top-K keys
 // full/empty: mbarriers of the ring
-// wsc       : per consumer warp, G x P logits then weights of the page in hand
+// wsc       : per consumer warp, G x PS logits then weights of the stage in hand (PS
+//             tokens a stage)
 // st        : per consumer warp and head: running max (log2 units), running sum, rescale
 // mscale    : per head, the merge scale of every split, then the merged max and sum
 // Pages of a decode ring stage: a page at page size 16, half a page at 32.
@@ -733,7 +736,8 @@ __device__ void topk_row(const float* row, int N, int K, int sink, int local, in
 
 
 // ------------------------------------------------------------------------------------
-// decode: one page of one kv head against the G query heads of its group, in one warp.
+// decode: one ring stage (P tokens here: a page, or half a page at page size 32) of one
+// kv head against the G query heads of its group, in one warp.
 // Lane l owns dims [4l, 4l+4).  Logits: 16 (head, token) partial dot products per chunk
 // are summed across the warp with a transposing butterfly (15 shuffles leave each lane
 // pair holding one full logit).  Softmax: running max / sum per head (log2 domain).

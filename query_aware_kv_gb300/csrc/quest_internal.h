@@ -14,7 +14,7 @@ namespace quest {
 constexpr int kHeadDim = 128;
 constexpr int kConsumerWarps = 8;           // warps that compute
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kDecodeThreads = kConsumerThreads + 32;  // + one bulk-copy producer warp
+constexpr int kDecodeThreads = kConsumerThreads + 32;  // + one copy-producer warp
 constexpr int kStages = 8;                  // smem ring depth (pages in flight per CTA)
 constexpr int kMaxSplits = 256;             // split-K partials per (sequence, q head)
 constexpr int kDefaultPagesPerSplit = 8;    // dense decode work items (at least)
@@ -158,7 +158,7 @@ cudaError_t ensure_smem(const void* fn, size_t bytes);
 
 // Host-side checks of quest_decode's cache / top_k arguments (status code, error text
 // set), and the workspace bytes it needs: `total`, of which the first `zeroed` bytes
-// (status word, queue, counters, selection flags) must be zero when a call starts.
+// (header, arrival counters, ready flags, key rows) must be zero when a call starts.
 int decode_workspace_requirement(const quest_cache_t* cache, int top_k, size_t* total,
                                  size_t* zeroed);
 // Record a failure for quest_last_error(); returns `code`.

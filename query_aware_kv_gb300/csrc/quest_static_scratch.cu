@@ -59,8 +59,9 @@ extern "C" int quest_decode_static(const quest_cache_t* cache, const void* q, in
   }
   void* ws = nullptr;
   if ((rc = scratch_address(&ws))) return rc;
-  // The array keeps whatever the previous call left: clear the status word, the work
-  // queue, the counters and the selection flags before this call uses them.
+  // The array keeps whatever the previous call left: clear the header (status word and
+  // counters), the arrival counters, the ready flags and the key rows before this call
+  // uses them.
   cudaError_t e = cudaMemsetAsync(ws, 0, zeroed, s);
   if (e != cudaSuccess) return quest::set_last_error(QUEST_ERR_CUDA, cudaGetErrorString(e));
   rc = quest_decode(cache, q, top_k, out, lse, idx_out, count_out, ws, kStaticScratchBytes,

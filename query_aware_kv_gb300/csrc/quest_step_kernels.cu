@@ -1,5 +1,6 @@
 // quest_step_kernels.cu - the three steps of a Quest decode step as separate launches:
-// page scoring, top-K selection, split-K sparse (or dense) flash-decode.
+// page scoring, top-K selection, split-K sparse (or dense) flash-decode, whose work items
+// can also take their pair's top-K themselves (two launches per step).
 #include <mutex>
 #include <unordered_map>
 

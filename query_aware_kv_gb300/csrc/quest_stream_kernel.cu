@@ -17,8 +17,9 @@
 //   consumer warps (0..7)  stage s belongs to consumer s mod 8.  Scoring stage: the
 //       bound of each page (Solution step 2) becomes an order-preserving key in global
 //       memory, and the piece is counted on its pair (a release reduction).  Decode
-//       stage: flash-decode of one kept page (Tang 2024 summary: exact attention over the
-//       Top-K pages); the 8 warps' states of a piece are combined in shared memory into
+//       stage: flash-decode of one kept page (exact attention over the kept pages only:
+//       "Quest: Query-Aware Sparsity for Efficient Long-Context LLM Inference", Summary);
+//       the 8 warps' states of a piece are combined in shared memory into
 //       one split-K partial, which is counted on its pair.
 //   selector CTAs          the last few CTAs of the grid stream nothing: each owns every
 //       sel_ctas-th pair and, with 12 warps, takes the exact top-K of a pair's keys as

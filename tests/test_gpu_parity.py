@@ -142,9 +142,9 @@ def test_topk_near_ties_over_a_wide_range():
 
 @pytest.mark.parametrize("sink,local", [(2, 2), (0, 3), (4, 0), (8, 8)])
 def test_topk_sink_and_local_pages(sink, local):
-    """[Guide] Solution step 3 / Implementation step 2: the first `sink` and last `local`
-    pages of a long sequence are always kept, the rest of the budget goes to the best of
-    the others; short sequences keep everything."""
+    """Sink and local pages ("Guide to Quest", Solution step 3 / Implementation step 2):
+    the first `sink` and last `local` pages of a long sequence are always kept, the rest of
+    the budget goes to the best of the others; short sequences keep everything."""
     w = small(lens=(16 * 300 - 7, 16 * 12, 16 * 64), batch=3, hq=4, hkv=2)
     pair = H.on_device(w, build_meta=False)
     rng = np.random.default_rng(sink * 10 + local)
@@ -201,8 +201,8 @@ def test_estimate_heads_and_group_max():
 
 @pytest.mark.parametrize("K", [1, 9, 40])
 def test_topk_union_matches_oracle_on_identical_scores(K):
-    """[Guide] Best Practices step 2, union form: given the oracle's own per-head scores the
-    union must be exactly the oracle's."""
+    """Union form ("Guide to Quest", Best Practices step 2): given the oracle's own
+    per-head scores the union must be exactly the oracle's."""
     w = small(lens=(16 * 200 - 3, 16 * 6, 16 * 41), batch=3, hq=8, hkv=2, budget=16 * K)
     pair = H.on_device(w)
     sh = oracle.score_heads(pair.ref, w.q[0].numpy().astype(np.float32))
