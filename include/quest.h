@@ -214,8 +214,8 @@ int quest_build_meta(const quest_cache_t* cache, void* ws, size_t ws_bytes,
                      quest_stream_t stream);
 
 /*
- * Decode-time append.  [Guide] Solution step 1: the box is formed as pages fill during
- * prompt prefill or token generation.  k_new, v_new: fp16 [batch][num_kv_heads][128].
+ * Decode-time append.  [Guide] Solution step 1: a page's box is built as the page fills,
+ * in prefill and in generation alike.  k_new, v_new: fp16 [batch][num_kv_heads][128].
  * For each sequence b the token goes to position L = seq_lens[b] (page L / P, which the
  * caller must have mapped in block_table, slot L % P); slot 0 starts the page's box,
  * any other slot widens it; then seq_lens[b] becomes L + 1.  A sequence with no room

@@ -108,8 +108,8 @@ int oq_build_meta(const oq_dims* s, const float* k_pool, const int32_t* block_ta
 }
 
 /* ---------------------------------------------------------------------------------
- * Decode-time append.  [Guide] Solution, step 1 says the box is formed while a page is
- * filled during prompt prefill *or token generation*: the new token of sequence b goes
+ * Decode-time append.  [Guide] Solution, step 1: a page's box is built as the page fills,
+ * in generation as in prefill: the new token of sequence b goes
  * to position seq_lens[b] (page seq_len / P, slot seq_len % P); a token that opens a
  * page starts that page's box, any other token widens the existing box.  The length
  * then grows by one.
