@@ -231,6 +231,18 @@ def test_decode_launches_without_a_device_query(lib):
         -q.QUEST_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("kw", [dict(num_q_heads=16, num_kv_heads=4),
+                                dict(max_pages=4097, num_phys=4097)],
+                         ids=["gqa", "mha_4097_pages"])
+def test_chain_keeps_the_topk_kernel_on_gqa_and_long_rows(lib, kw):
+    """On GQA rows, and on rows longer than 4096 pages, the chain selects in a top-K kernel
+    of its own whatever the GPU (three launches)."""
+    d = desc(**kw)
+    o = q.opts(path=q.QUEST_PATH_CHAIN)
+    assert lib.quest_decode_path(ctypes.byref(d), 16, ctypes.byref(o), 1) == q.QUEST_PATH_CHAIN
+    assert lib.quest_decode_launches(ctypes.byref(d), 16, ctypes.byref(o)) == 3
+
+
 def test_union_form_runs_on_the_chain(lib):
     """gqa_union on the fused calls: the chain (no device query), three launches, a larger
     workspace (per-head scores, union rows); the one-launch paths refuse it."""
